@@ -1,0 +1,66 @@
+"""Plant one plausible mistake at a time in a copy of the oracle (on the CPU) and require the pins to catch it.
+
+Each mutation is a textual replacement in a temporary copy of ``oracle/oracle.c``; the copy is compiled with the
+oracle's own flags and every pin is run against it. A mutation that no pin catches would mean the pins cannot tell
+that mistake from the page's arithmetic.
+"""
+import os
+import shutil
+
+import pytest
+
+import oracle
+import pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+MUTATIONS = {
+    "decay_dropped": ("float wdec = decoupled ? wi * s->dec : wi;", "float wdec = wi;"),
+    "step_sign": ("float neg_step = -s->step;", "float neg_step = s->step;"),
+    "c1_c2_swapped_in_m": ("mi + s->c1 * (gh - mi)", "mi + s->c2 * (gh - mi)"),
+    "b1_in_bc2": ("s->bc2 = (float)sqrt(1.0 - pow(b2, tt));", "s->bc2 = (float)sqrt(1.0 - pow(b1, tt));"),
+    "no_bias_correction1": ("s->step = (float)(lr / (1.0 - pow(b1, tt)));", "s->step = (float)lr;"),
+    "eps_inside_sqrt": ("sqrtf(v_new) / s->bc2 + s->eps", "sqrtf(v_new + s->eps) / s->bc2"),
+    "v_linear_in_g": ("(s->c2 * gh) * gh", "(s->c2 * gh)"),
+    "w_reads_unrounded_m": ("m_new = ora_f32_from_bf16(hm);", ";"),
+    "w_reads_unrounded_v": ("v_new = ora_f32_from_bf16(hv);", ";"),
+    "bf16_truncates": ("return (uint16_t)((u + 0x7FFFu + keep_lsb) >> 16);", "return (uint16_t)(u >> 16);"),
+    "bf16_ties_up": ("return (uint16_t)((u + 0x7FFFu + keep_lsb) >> 16);",
+                     "return (uint16_t)((u + 0x8000u) >> 16);"),
+    "bf16_nan_canonical": ("if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0xFFFFu;",
+                           "if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0x7FC0u;"),
+    "halves_swapped": ("return (uint16_t)((i & 1) ? (word >> 16) : (word & 0xFFFFu));",
+                       "return (uint16_t)((i & 1) ? (word & 0xFFFFu) : (word >> 16));"),
+    "norm_ignores_unscale": ("float x = grad_at(g[k], gdt, i) * inv_scale;", "float x = grad_at(g[k], gdt, i);"),
+    "norm_summed_in_f32": ("double S = 0.0;\n    for (int32_t k = 0; k < T; ++k) {",
+                           "float S = 0.0f;\n    for (int32_t k = 0; k < T; ++k) {"),
+    "clip_not_clamped": ("float clip = (coef > 1.0f) ? 1.0f : coef;", "float clip = coef;"),
+    "clip_eps_dropped": ("float denom = norm + 1e-6f;", "float denom = norm;"),
+    "c2_taken_in_f32": ("s->c2 = (float)(1.0 - b2);", "s->c2 = 1.0f - (float)b2;"),
+    "zero_grad_ignored": ("        if (zero_grad) {\n", "        if (0) {\n"),
+    "f16_exponent_bias": ("mag = ldexpf((float)(f | 0x400), e - 25);", "mag = ldexpf((float)(f | 0x400), e - 24);"),
+    "f16_round_down": ("if (rem > half || (rem == half && (kept & 1u))) kept += 1u;", ";"),
+    "scale_ignores_factor": ("p[i] = p[i] * factor;", "p[i] = p[i];"),
+    "odd_tail_clobbered": ("if (i & 1) return (word & 0x0000FFFFu) | ((uint32_t)h << 16);\n    return (word & 0xFFFF0000u) | (uint32_t)h;",
+                           "if (i & 1) return (word & 0x0000FFFFu) | ((uint32_t)h << 16);\n    return (uint32_t)h;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_mutation_is_caught(name, tmp_path):
+    old, new = MUTATIONS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation {name}: the text to replace is not in oracle.c exactly once"
+    mutant_c = tmp_path / "mutant.c"
+    mutant_c.write_text(src.replace(old, new))
+    lib = oracle.build(str(mutant_c), str(tmp_path / f"libmutant_{name}.so"))
+    o = oracle.Oracle(lib)
+    caught = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin(o)
+        except AssertionError:
+            caught.append(pin.__name__)
+        except (FloatingPointError, OverflowError, ValueError, ZeroDivisionError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin catches the planted mistake {name}"
