@@ -1,0 +1,429 @@
+#!/usr/bin/env python3
+"""Benchmark of the clip + AdamW optimizer step: parameters per second and achieved HBM bandwidth on one GB300.
+
+One step = ClipGradNorms (norm partials + fixed-order finalize) and AdamWSteps over the whole parameter list, both
+through the C ABI (via the Python binding), inputs resident in HBM. Prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload gpt2_small] [--impl mica|reference]
+
+--impl reference times the CPU oracle (the plain single-threaded C step) on the host cores instead, on a bounded
+sample of the same workload. Under torchrun with N > 1 every rank runs the whole step on its own GPU (each rank a
+replica, as data-parallel training steps its replicated parameters); the time is the slowest rank's.
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "clip+AdamW params/sec and achieved HBM GB/s (% of 8 TB/s roofline), 1 GB300"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SRC = os.path.join(ROOT, "clip_tensor_adamw_gb300", "csrc", "kernels.cu")
+PROFILE = os.path.join(ROOT, "profiles", "adamw_gpt2_small.md")
+
+
+# ----------------------------------------------------------------------------------------------------------------
+# the byte model: algorithmic bytes per parameter
+# ----------------------------------------------------------------------------------------------------------------
+
+def adamw_bytes_per_param(wl: workloads.Workload, zero_grad: bool = False) -> float:
+    """AdamW kernel: w read + write (8), g read (4 or 2), m and v read + write (16 float32, 4 packed BF16); the
+    gradient's zero write (4 or 2) only with zero_grad."""
+    g = 2.0 if wl.grad_dtype == "f16" else 4.0
+    mv = 4.0 if wl.moments == "bf16x2" else 16.0
+    return 8.0 + g + mv + (g if zero_grad else 0.0)
+
+
+def step_bytes_per_param(wl: workloads.Workload, zero_grad: bool = False) -> float:
+    """The whole step: the norm's read of g plus the AdamW kernel (28 / 20 B + 4 B with float32 gradients)."""
+    g = 2.0 if wl.grad_dtype == "f16" else 4.0
+    return g + adamw_bytes_per_param(wl, zero_grad)
+
+
+def describe(wl: workloads.Workload) -> str:
+    return (f"{wl.name}: {len(wl.sizes)} tensors, {wl.params:,} params, {wl.grad_dtype} grads, "
+            f"{'packed BF16' if wl.moments == 'bf16x2' else 'f32'} moments")
+
+
+# ----------------------------------------------------------------------------------------------------------------
+# peaks, profiles, clocks
+# ----------------------------------------------------------------------------------------------------------------
+
+def hbm_peak() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        for k in ("hbm_gbs", "hbm_copy_gbs", "hbm_GBps"):
+            if k in d and float(d[k]) > 0:
+                return float(d[k]), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic() -> float | None:
+    """DRAM bytes per AdamW launch from the committed ncu summary, if it was taken on the current kernel source."""
+    try:
+        text = open(PROFILE).read()
+    except OSError:
+        return None
+    sha = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
+    m_sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]{16})", text)
+    m_b = re.search(r"dram_bytes_per_launch_full_size:\s*([0-9.eE+]+)", text)
+    if not m_sha or not m_b or m_sha.group(1) != sha:
+        return None
+    return float(m_b.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms while running."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows: list[tuple[float, list[str]]] = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.time()
+        while not self.rows and time.time() - t0 < 5.0:
+            time.sleep(0.02)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [r for t, r in self.rows if t0 - 0.05 <= t <= t1 + 0.15]
+        if not inside:  # a region shorter than the sampling period: the nearest sample after it began
+            after = [r for t, r in self.rows if t >= t0]
+            inside = after[:1] or [r for _, r in self.rows[-1:]]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in inside if num(r[1]) is not None]
+        mx = [num(r[2]) for r in inside if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i in range(4) if len(r) > 5 + i and r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ----------------------------------------------------------------------------------------------------------------
+# the CPU oracle: the reference arm and the cpu_baseline
+# ----------------------------------------------------------------------------------------------------------------
+
+def oracle_sample(wl: workloads.Workload, target_params: int):
+    """A bounded sample of the workload for the oracle: its first tensors up to ~target_params parameters (at
+    least one tensor), on the host."""
+    sizes, tot = [], 0
+    for n in wl.sizes:
+        if sizes and tot + n > target_params:
+            break
+        sizes.append(n)
+        tot += n
+    st = workloads.make_state(wl, "cpu", sizes=sizes)
+    workloads.fill_grad(st, 1)
+    return workloads.host_lists(st), tot, len(sizes)
+
+
+def time_oracle(wl: workloads.Workload, target_params: int, min_seconds: float, max_steps: int):
+    import oracle
+    ora = oracle.Oracle()
+    host, params, ntens = oracle_sample(wl, target_params)
+    hp = oracle.Hyper(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps, weight_decay=wl.weight_decay, step=1)
+    times = []
+    t_all = time.perf_counter()
+    t = 0
+    while t < max_steps and (time.perf_counter() - t_all < min_seconds or t == 0):
+        t += 1
+        t0 = time.perf_counter()
+        ora.clip_adamw_step(*host, oracle.Hyper(**{**hp.__dict__, "step": t}), wl.max_norm, wl.inv_scale)
+        times.append(time.perf_counter() - t0)
+    return params, ntens, times
+
+
+def run_reference(args, wl: workloads.Workload) -> None:
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    params, ntens, times = None, None, []
+    import oracle
+    ora = oracle.Oracle()
+    host, params, ntens = oracle_sample(wl, max(1, wl.params // 8))
+    hp0 = dict(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps, weight_decay=wl.weight_decay)
+    for t in range(1, args.warmup + args.steps + 1):
+        t0 = time.perf_counter()
+        ora.clip_adamw_step(*host, oracle.Hyper(step=t, **hp0), wl.max_norm, wl.inv_scale)
+        if t > args.warmup:
+            times.append(time.perf_counter() - t0)
+    sec = sum(times)
+    value = params * len(times) / sec
+    sample = f"first {ntens} of {len(wl.sizes)} tensors of {wl.name} ({params:,} of {wl.params:,} params) per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": describe(wl), "params_per_step": params, "oracle": "plain single-threaded C, -O2"},
+        "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------------------------------------------
+# the GPU step
+# ----------------------------------------------------------------------------------------------------------------
+
+def measure(wl: workloads.Workload, steps: int, warmup: int, zero_grad: bool, dist=None, sampler=None):
+    """Times `steps` steps of the whole hot path on the device (inputs resident). Returns a dict of figures."""
+    import clip_tensor_adamw_gb300 as mica
+    st = workloads.make_state(wl, "cuda")
+    workloads.fill_grad(st, 1)
+    W = mica.TensorList(st.w)
+    G = mica.TensorList(st.g)
+    M = mica.TensorList(st.m, W.counts)
+    V = mica.TensorList(st.v, W.counts)
+    norm = torch.empty(1, device="cuda")
+    factor = torch.empty(1, device="cuda")
+    kw = dict(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps, weight_decay=wl.weight_decay,
+              zero_grad=zero_grad, factor=factor)
+    stream = torch.cuda.current_stream()
+
+    def step(t, ev_mid=None):
+        mica.mica_clip_grad_norms(G, wl.max_norm, wl.inv_scale, norm_out=norm, factor_out=factor)
+        if ev_mid is not None:
+            ev_mid.record(stream)
+        mica.mica_adamw_steps(W, G, M, V, step=t, **kw)
+
+    for t in range(1, warmup + 1):
+        step(t)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    launches0 = mica.mica_launch_count()
+    t_wall0 = time.time()
+    for i in range(steps):
+        ev[i][0].record(stream)
+        step(warmup + 1 + i, ev[i][1])
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    launches = mica.mica_launch_count() - launches0
+    total_ms = ev[0][0].elapsed_time(ev[-1][2])
+    adamw_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    clip_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    if dist is not None:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    out = {"total_ms": total_ms, "ms_per_step": total_ms / steps, "adamw_ms": statistics.mean(adamw_ms),
+           "clip_ms": statistics.mean(clip_ms), "launches": launches, "t_wall": (t_wall0, t_wall1),
+           "norm": float(norm.item())}
+    del st
+    return out, (W, G, M, V, norm, factor, kw)
+
+
+def measure_e2e(wl: workloads.Workload, steps: int, warmup: int):
+    """The same step through the public API with the step's gradient arriving from pinned host memory and the norm
+    read back to the host, both inside the timed region."""
+    import clip_tensor_adamw_gb300 as mica
+    st = workloads.make_state(wl, "cuda")
+    workloads.fill_grad(st, 1)
+    g_host = torch.empty(st.g_flat.shape, dtype=st.g_flat.dtype, pin_memory=True)
+    g_host.copy_(st.g_flat)
+    norm_host = torch.empty(1, dtype=torch.float32, pin_memory=True)
+    W = mica.TensorList(st.w)
+    G = mica.TensorList(st.g)
+    M = mica.TensorList(st.m, W.counts)
+    V = mica.TensorList(st.v, W.counts)
+    norm = torch.empty(1, device="cuda")
+    factor = torch.empty(1, device="cuda")
+    kw = dict(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps, weight_decay=wl.weight_decay, factor=factor)
+    stream = torch.cuda.current_stream()
+
+    def step(t):
+        st.g_flat.copy_(g_host, non_blocking=True)
+        mica.mica_clip_grad_norms(G, wl.max_norm, wl.inv_scale, norm_out=norm, factor_out=factor)
+        mica.mica_adamw_steps(W, G, M, V, step=t, **kw)
+        norm_host.copy_(norm, non_blocking=True)
+
+    for t in range(1, warmup + 1):
+        step(t)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        step(warmup + 1 + i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    h2d = st.g_flat.numel() * st.g_flat.element_size()
+    del st
+    return ms, h2d, 4
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="gpt2_small", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--impl", default="mica", choices=["mica", "reference"])
+    ap.add_argument("--no-extras", action="store_true", help="skip the other workloads, e2e and the CPU baseline")
+    ap.add_argument("--subset-params", type=int, default=0,
+                    help="keep only the workload's first tensors up to this many parameters (small profiling case)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    wl = workloads.WORKLOADS[args.workload]
+    if args.subset_params:
+        shapes, tot = [], 0
+        for s_, n in zip(wl.shapes, wl.sizes):
+            if shapes and tot + n > args.subset_params:
+                break
+            shapes.append(s_)
+            tot += n
+        wl = dataclasses.replace(wl, name=f"{wl.name}[first {len(shapes)} tensors]", shapes=tuple(shapes))
+
+    if args.impl == "reference":
+        run_reference(args, wl)
+        return
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    if world != args.gpus and rank == 0:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+
+    import clip_tensor_adamw_gb300 as mica
+    mica.lib()
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    main_fig, _ = measure(wl, args.steps, args.warmup, zero_grad=False, dist=dist)
+    if sampler:
+        sampler.stop()
+    clocks = sampler.summary(*main_fig["t_wall"]) if sampler else None
+
+    P = wl.params
+    sec = main_fig["total_ms"] / 1e3
+    value = world * P * args.steps / sec
+    step_bpp = step_bytes_per_param(wl)
+    step_gbs = P * step_bpp * args.steps / sec / 1e9
+    a_bpp = adamw_bytes_per_param(wl)
+    a_gbs = P * a_bpp / (main_fig["adamw_ms"] / 1e3) / 1e9
+    peak, peak_src = hbm_peak()
+
+    extras = {}
+    e2e = None
+    cpu = None
+    if not args.no_extras and rank == 0:
+        zg, _ = measure(wl, max(20, args.steps // 4), args.warmup, zero_grad=True)
+        extras["zero_grad"] = {"ms_per_step": zg["ms_per_step"],
+                               "hbm_gbs_model": P * step_bytes_per_param(wl) / (zg["ms_per_step"] / 1e3) / 1e9,
+                               "hbm_gbs_actual": P * step_bytes_per_param(wl, True) / (zg["ms_per_step"] / 1e3) / 1e9,
+                               "bytes_per_param_actual": step_bytes_per_param(wl, True)}
+        for other in ("gpt2_small_bf16", "gpt2_xl", "fp16_scaled", "tiny"):
+            if other == wl.name:
+                continue
+            owl = workloads.WORKLOADS[other]
+            k = 40 if other == "gpt2_xl" else max(20, args.steps // 4)
+            f, _ = measure(owl, k, args.warmup, zero_grad=False)
+            torch.cuda.empty_cache()
+            extras[other] = {"params": owl.params, "ms_per_step": f["ms_per_step"],
+                             "params_per_s": owl.params / (f["ms_per_step"] / 1e3),
+                             "hbm_gbs": owl.params * step_bytes_per_param(owl) / (f["ms_per_step"] / 1e3) / 1e9,
+                             "pct_of_8tbs": 100 * owl.params * step_bytes_per_param(owl) /
+                             (f["ms_per_step"] / 1e3) / 1e9 / NOMINAL_HBM_GBS,
+                             "adamw_ms": f["adamw_ms"], "clip_ms": f["clip_ms"],
+                             "bytes_per_param": step_bytes_per_param(owl)}
+        ms, h2d, d2h = measure_e2e(wl, max(20, args.steps // 4), args.warmup)
+        e2e = {"value": P / (ms / 1e3), "unit": "params/s", "ms_per_step": ms, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
+        params, ntens, times = time_oracle(wl, target_params=wl.params, min_seconds=10.0, max_steps=20)
+        cpu = {"value": params * len(times) / sum(times), "unit": "params/s", "cores": 1, "kind": "oracle",
+               "sample": f"{len(times)} full steps of the first {ntens} of {len(wl.sizes)} tensors "
+                         f"({params:,} params) of {wl.name}, single-threaded C oracle"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": main_fig["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": describe(wl), "params": P, "tensors": len(wl.sizes), "moments": wl.moments,
+                       "grad_dtype": wl.grad_dtype, "zero_grad": False, "bytes_per_param": step_bpp,
+                       "l2": f"inputs larger than L2 ({P * step_bpp / 1e9:.2f} GB moved per step; no flush)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "hbm_gbs": step_gbs, "pct_of_8tbs": 100 * step_gbs / NOMINAL_HBM_GBS,
+            "pct_of_measured_copy": 100 * step_gbs / peak if peak_src == "measured" else None,
+            "roofline": {"bound": "hbm", "kernel": "adamw_kernel", "achieved": a_gbs, "peak": peak, "unit": "GB/s",
+                         "frac": a_gbs / peak, "peak_source": peak_src, "traffic": profiled_traffic(),
+                         "bytes_per_param": a_bpp, "launch_ms": main_fig["adamw_ms"]},
+            "clip_ms": main_fig["clip_ms"], "norm": main_fig["norm"],
+            "clocks": clocks, "gpu_launches": main_fig["launches"],
+            "e2e": e2e, "cpu_baseline": cpu, "also": extras,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

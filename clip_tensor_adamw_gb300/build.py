@@ -1,0 +1,55 @@
+"""Builds libmica_optim.so in the package directory: the CUDA kernels and the C ABI, for sm_103a only.
+
+Each translation unit is compiled by nvcc in parallel, then linked into one shared library with the CUDA runtime
+linked statically and only the ``mica_*`` symbols exported. ``python -m clip_tensor_adamw_gb300.build`` runs it.
+"""
+from __future__ import annotations
+
+import os
+import subprocess
+import sys
+from concurrent.futures import ThreadPoolExecutor
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+BUILD = os.path.join(PKG, "_build")
+LIB = os.path.join(PKG, "libmica_optim.so")
+SOURCES = ["kernels.cu", "api.cpp"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+NVCC = os.environ.get("NVCC", "nvcc")
+CFLAGS = [*ARCH, "-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC,-O2,-fvisibility=hidden",
+          "-I", os.path.join(ROOT, "include"), "-I", CSRC]
+
+
+def _run(cmd):
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"command failed ({r.returncode}): {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
+    return r.stdout + r.stderr
+
+
+def build(verbose: bool = False, ptxas_info: bool = False) -> str:
+    os.makedirs(BUILD, exist_ok=True)
+    extra = ["-Xptxas", "-v"] if ptxas_info else []
+
+    def compile_one(src):
+        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+        out = _run([NVCC, *CFLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj])
+        return obj, out
+
+    with ThreadPoolExecutor(len(SOURCES)) as ex:
+        results = list(ex.map(compile_one, SOURCES))
+    objs = [o for o, _ in results]
+    tmp = LIB + ".tmp"
+    _run([NVCC, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs,
+          "-Xlinker", f"--version-script={os.path.join(CSRC, 'exports.map')}"])
+    os.replace(tmp, LIB)
+    if verbose or ptxas_info:
+        for _, out in results:
+            sys.stdout.write(out)
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(verbose=True, ptxas_info="-v" in sys.argv))

@@ -1,0 +1,569 @@
+// The C ABI of include/mica_optim.h: host-side validation, the per-list device tables (cached), the step's scalars,
+// and the launches. Nothing here touches tensor data; every element is read and written by the kernels.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <memory>
+#include <mutex>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include "mica_optim.h"
+#include "plan.h"
+
+namespace mica {
+
+// ------------------------------------------------------------------------------------------------------------------
+// bookkeeping: launch count, per-thread error detail, debug synchronisation
+// ------------------------------------------------------------------------------------------------------------------
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launches(uint64_t k) { g_launches.fetch_add(k, std::memory_order_relaxed); }
+
+static thread_local std::string t_detail;
+
+static mica_status fail(mica_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_detail = buf;
+    return s;
+}
+
+static mica_status ok() {
+    t_detail.clear();
+    return MICA_OK;
+}
+
+static mica_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(MICA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+static bool sync_debug() {
+    static const bool on = [] {
+        const char* s = std::getenv("MICA_SYNC_DEBUG");
+        return s && s[0] && std::strcmp(s, "0") != 0;
+    }();
+    return on;
+}
+
+static mica_status after_launch(int err, void* stream, const char* what) {
+    if (err != (int)cudaSuccess) return cuda_fail((cudaError_t)err, what);
+    if (sync_debug()) {
+        const cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, what);
+    }
+    return ok();
+}
+
+// ------------------------------------------------------------------------------------------------------------------
+// pointer checks (only when a list's table is built, and for the scalar outputs of each call)
+// ------------------------------------------------------------------------------------------------------------------
+
+using MemGetAddressRange = int (*)(unsigned long long* base, size_t* size, unsigned long long ptr);
+
+static MemGetAddressRange address_range_fn() {
+    static MemGetAddressRange fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return (MemGetAddressRange) nullptr;
+        }
+        return reinterpret_cast<MemGetAddressRange>(p);
+    }();
+    return fn;
+}
+
+// `p` must be device (or managed) memory of `device`, aligned to `align`, and [p, p + bytes) must lie inside the
+// allocation that holds p when the driver can tell its extent.
+static mica_status check_device_span(const void* p, size_t bytes, size_t align, int device, const char* what,
+                                     int64_t index) {
+    if (reinterpret_cast<uintptr_t>(p) % align != 0)
+        return fail(MICA_ERR_ADDRESS, "%s[%lld] = %p is not %zu-byte aligned", what, (long long)index, p, align);
+    cudaPointerAttributes a{};
+    const cudaError_t e = cudaPointerGetAttributes(&a, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(MICA_ERR_ADDRESS, "%s[%lld] = %p: cudaPointerGetAttributes failed (%s)", what, (long long)index,
+                    p, cudaGetErrorName(e));
+    }
+    if (a.type == cudaMemoryTypeDevice) {
+        if (a.device != device)
+            return fail(MICA_ERR_ADDRESS, "%s[%lld] = %p is memory of device %d, not of the current device %d", what,
+                        (long long)index, p, a.device, device);
+    } else if (a.type != cudaMemoryTypeManaged) {
+        return fail(MICA_ERR_ADDRESS, "%s[%lld] = %p is not device memory", what, (long long)index, p);
+    }
+    if (MemGetAddressRange fn = address_range_fn()) {
+        unsigned long long base = 0;
+        size_t size = 0;
+        if (fn(&base, &size, (unsigned long long)reinterpret_cast<uintptr_t>(p)) == 0) {
+            const unsigned long long end = base + size, q = (unsigned long long)reinterpret_cast<uintptr_t>(p);
+            if (q + bytes > end)
+                return fail(MICA_ERR_ADDRESS, "%s[%lld] = %p: %zu bytes run past the end of its allocation", what,
+                            (long long)index, p, bytes);
+        }
+    }
+    return MICA_OK;
+}
+
+struct Span {
+    uintptr_t lo, hi;  // [lo, hi)
+    int32_t kind, index;
+};
+
+static const char* span_name(int32_t kind) {
+    static const char* names[] = {"w", "g", "m", "v", "t"};
+    return names[kind];
+}
+
+// sorts `spans` and fails when two overlap
+static mica_status check_disjoint(std::vector<Span>& spans) {
+    std::sort(spans.begin(), spans.end(), [](const Span& a, const Span& b) { return a.lo < b.lo; });
+    for (size_t i = 1; i < spans.size(); ++i)
+        if (spans[i].lo < spans[i - 1].hi)
+            return fail(MICA_ERR_OVERLAP, "%s[%d] overlaps %s[%d]", span_name(spans[i].kind), spans[i].index,
+                        span_name(spans[i - 1].kind), spans[i - 1].index);
+    return MICA_OK;
+}
+
+static bool overlaps_any(const std::vector<Span>& sorted, const void* p, size_t bytes) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p), hi = lo + bytes;
+    auto it = std::upper_bound(sorted.begin(), sorted.end(), lo, [](uintptr_t x, const Span& s) { return x < s.lo; });
+    if (it != sorted.end() && it->lo < hi) return true;
+    if (it != sorted.begin() && std::prev(it)->hi > lo) return true;
+    return false;
+}
+
+// ------------------------------------------------------------------------------------------------------------------
+// per-list device tables
+// ------------------------------------------------------------------------------------------------------------------
+
+enum Kind : uint64_t { kAdamW = 1, kNorm = 2, kScale = 3 };
+
+struct Plan {
+    int device = 0;
+    std::vector<uint64_t> key;
+    void* dev = nullptr;  // one allocation: TensorRec[T] | WorkItem[I] | double[I] (norm)
+    TensorRec* recs = nullptr;
+    WorkItem* items = nullptr;
+    double* partials = nullptr;
+    int32_t num_items = 0;
+    int32_t item_quads = 0;
+    std::vector<Span> spans;  // the list's buffers, sorted (for checking a call's scalar outputs)
+    ~Plan() {
+        if (dev) {
+            int cur = 0;
+            cudaGetDevice(&cur);
+            cudaSetDevice(device);
+            cudaFree(dev);
+            cudaSetDevice(cur);
+        }
+    }
+};
+
+static std::mutex g_mu;
+static std::unordered_map<uint64_t, std::vector<std::unique_ptr<Plan>>> g_plans;
+static size_t g_plan_count = 0;
+constexpr size_t kMaxPlans = 1024;
+
+static uint64_t hash_key(const std::vector<uint64_t>& k) {
+    uint64_t h = 0x243F6A8885A308D3ull;
+    for (uint64_t x : k) {
+        h ^= x + 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
+        h *= 0xFF51AFD7ED558CCDull;
+    }
+    return h;
+}
+
+static int sm_count(int device) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        n = 148;
+    }
+    return n;
+}
+
+// Quads per work item: 4096 (16,384 elements) when the list is large enough to give every SM many items, halved
+// down to 256 for small lists so that all SMs still get work. MICA_ITEM_QUADS overrides it (a power of two).
+static int32_t choose_item_quads(int64_t total_quads, int sms) {
+    if (const char* s = std::getenv("MICA_ITEM_QUADS")) {
+        const long v = std::strtol(s, nullptr, 10);
+        if (v >= 32 && v <= (1 << 20) && (v & (v - 1)) == 0) return (int32_t)v;
+    }
+    int32_t iq = 4096;
+    const int64_t target = (int64_t)sms * 16;
+    while (iq > 256 && total_quads / iq < target) iq /= 2;
+    return iq;
+}
+
+// Work items over the tensors' quads (see plan.h).
+static std::vector<WorkItem> build_items(const int64_t* n, int32_t T, int32_t iq) {
+    std::vector<WorkItem> items;
+    const int64_t small = iq / 2;
+    bool open = false;
+    WorkItem pack{};
+    int64_t pack_q = 0;
+    auto close = [&] {
+        if (open) items.push_back(pack);
+        open = false;
+    };
+    for (int32_t k = 0; k < T; ++k) {
+        const int64_t nq = (n[k] + 3) / 4;
+        if (nq == 0) {
+            if (open) pack.count += 1;  // an empty tensor inside a pack costs nothing
+            continue;
+        }
+        if (nq <= small) {
+            if (open && pack_q + nq <= iq) {
+                pack.count += 1;
+                pack_q += nq;
+            } else {
+                close();
+                pack = WorkItem{k, 1, 0};
+                pack_q = nq;
+                open = true;
+            }
+            continue;
+        }
+        close();
+        for (int64_t q = 0; q < nq; q += iq) items.push_back(WorkItem{k, 1, q});
+    }
+    close();
+    return items;
+}
+
+static uint64_t ptr_u(const void* p) { return (uint64_t) reinterpret_cast<uintptr_t>(p); }
+
+struct ListDesc {
+    Kind kind;
+    int32_t T;
+    const int64_t* n;
+    float* const* w;     // adamw: weights; scale: the tensors
+    void* const* g;      // adamw, norm
+    void* const* m;      // adamw
+    void* const* v;      // adamw
+    Dtype gdt, mdt;      // scale: gdt is the tensors' type
+};
+
+static size_t elem_bytes(Dtype d) { return d == kF16 ? 2 : 4; }
+
+static mica_status build_plan(const ListDesc& L, int device, std::vector<uint64_t>&& key, Plan** out,
+                              void* stream) {
+    auto plan = std::make_unique<Plan>();
+    plan->device = device;
+    plan->key = std::move(key);
+
+    // pointer checks and the overlap check, over every non-empty buffer of the list
+    std::vector<Span> spans;
+    std::vector<TensorRec> recs((size_t)L.T);
+    int64_t total_quads = 0;
+    for (int32_t k = 0; k < L.T; ++k) {
+        const int64_t n = L.n[k];
+        TensorRec& r = recs[k];
+        r = TensorRec{nullptr, nullptr, nullptr, nullptr, n, 0, 0};
+        if (n == 0) continue;
+        total_quads += (n + 3) / 4;
+        mica_status s;
+        if (L.kind == kScale) {
+            const size_t b = (size_t)n * elem_bytes(L.gdt);
+            if ((s = check_device_span(L.w[k], b, elem_bytes(L.gdt), device, "t", k)) != MICA_OK) return s;
+            r.w = L.w[k];
+            r.vec = (ptr_u(r.w) % (L.gdt == kF16 ? 8 : 16)) == 0;
+            spans.push_back({(uintptr_t)ptr_u(r.w), (uintptr_t)(ptr_u(r.w) + b), 4, k});
+            continue;
+        }
+        const size_t gb = (size_t)n * elem_bytes(L.gdt);
+        if ((s = check_device_span(L.g[k], gb, elem_bytes(L.gdt), device, "g", k)) != MICA_OK) return s;
+        r.g = L.g[k];
+        spans.push_back({(uintptr_t)ptr_u(r.g), (uintptr_t)(ptr_u(r.g) + gb), 1, k});
+        bool vec = (ptr_u(r.g) % (L.gdt == kF16 ? 8 : 16)) == 0;
+        if (L.kind == kAdamW) {
+            const size_t wb = (size_t)n * 4;
+            const size_t mb = (L.mdt == kBF16x2) ? (size_t)((n + 1) / 2) * 4 : (size_t)n * 4;
+            if ((s = check_device_span(L.w[k], wb, 4, device, "w", k)) != MICA_OK) return s;
+            if ((s = check_device_span(L.m[k], mb, 4, device, "m", k)) != MICA_OK) return s;
+            if ((s = check_device_span(L.v[k], mb, 4, device, "v", k)) != MICA_OK) return s;
+            r.w = L.w[k];
+            r.m = L.m[k];
+            r.v = L.v[k];
+            spans.push_back({(uintptr_t)ptr_u(r.w), (uintptr_t)(ptr_u(r.w) + wb), 0, k});
+            spans.push_back({(uintptr_t)ptr_u(r.m), (uintptr_t)(ptr_u(r.m) + mb), 2, k});
+            spans.push_back({(uintptr_t)ptr_u(r.v), (uintptr_t)(ptr_u(r.v) + mb), 3, k});
+            const uint64_t ma = (L.mdt == kBF16x2) ? 8 : 16;
+            vec = vec && ptr_u(r.w) % 16 == 0 && ptr_u(r.m) % ma == 0 && ptr_u(r.v) % ma == 0;
+        }
+        r.vec = vec ? 1 : 0;
+    }
+    if (L.kind != kNorm) {
+        mica_status s = check_disjoint(spans);
+        if (s != MICA_OK) return s;
+    } else {
+        std::sort(spans.begin(), spans.end(), [](const Span& a, const Span& b) { return a.lo < b.lo; });
+    }
+    plan->spans = std::move(spans);
+
+    plan->item_quads = choose_item_quads(total_quads, sm_count(device));
+    std::vector<WorkItem> items = build_items(L.n, L.T, plan->item_quads);
+    if (items.size() > (size_t)INT32_MAX) return fail(MICA_ERR_COUNT, "too many work items (%zu)", items.size());
+    plan->num_items = (int32_t)items.size();
+
+    const size_t rec_b = recs.size() * sizeof(TensorRec);
+    const size_t item_off = (rec_b + 255) / 256 * 256;
+    const size_t item_b = items.size() * sizeof(WorkItem);
+    const size_t part_off = (item_off + item_b + 255) / 256 * 256;
+    const size_t part_b = (L.kind == kNorm) ? std::max<size_t>(items.size(), 1) * sizeof(double) : 0;
+    const size_t total = part_off + part_b;
+    cudaError_t e = cudaMalloc(&plan->dev, std::max<size_t>(total, 256));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        plan->dev = nullptr;
+        return fail(MICA_ERR_NOMEM, "cudaMalloc of a %zu-byte tensor-list table failed (%s)", total,
+                    cudaGetErrorName(e));
+    }
+    char* base = static_cast<char*>(plan->dev);
+    plan->recs = reinterpret_cast<TensorRec*>(base);
+    plan->items = reinterpret_cast<WorkItem*>(base + item_off);
+    plan->partials = (L.kind == kNorm) ? reinterpret_cast<double*>(base + part_off) : nullptr;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (rec_b && (e = cudaMemcpyAsync(plan->recs, recs.data(), rec_b, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+        return cuda_fail(e, "uploading the tensor records");
+    if (item_b && (e = cudaMemcpyAsync(plan->items, items.data(), item_b, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+        return cuda_fail(e, "uploading the work items");
+    if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cuda_fail(e, "waiting for the table upload");
+    *out = plan.get();
+
+    uint64_t h = hash_key(plan->key);
+    if (g_plan_count >= kMaxPlans) {
+        cudaDeviceSynchronize();
+        g_plans.clear();
+        g_plan_count = 0;
+    }
+    g_plans[h].push_back(std::move(plan));
+    ++g_plan_count;
+    return MICA_OK;
+}
+
+static mica_status get_plan(const ListDesc& L, int device, Plan** out, void* stream) {
+    std::vector<uint64_t> key;
+    key.reserve(5 + (size_t)L.T * 5);
+    key.push_back((uint64_t)L.kind);
+    key.push_back((uint64_t)device);
+    key.push_back((uint64_t)L.gdt);
+    key.push_back((uint64_t)L.mdt);
+    key.push_back((uint64_t)L.T);
+    for (int32_t k = 0; k < L.T; ++k) {
+        key.push_back((uint64_t)L.n[k]);
+        if (L.kind == kScale) {
+            key.push_back(ptr_u(L.w[k]));
+        } else if (L.kind == kNorm) {
+            key.push_back(ptr_u(L.g[k]));
+        } else {
+            key.push_back(ptr_u(L.w[k]));
+            key.push_back(ptr_u(L.g[k]));
+            key.push_back(ptr_u(L.m[k]));
+            key.push_back(ptr_u(L.v[k]));
+        }
+    }
+    const uint64_t h = hash_key(key);
+    std::lock_guard<std::mutex> lock(g_mu);
+    auto it = g_plans.find(h);
+    if (it != g_plans.end())
+        for (auto& p : it->second)
+            if (p->key == key) {
+                *out = p.get();
+                return MICA_OK;
+            }
+    return build_plan(L, device, std::move(key), out, stream);
+}
+
+// ------------------------------------------------------------------------------------------------------------------
+// argument checks shared by the entry points
+// ------------------------------------------------------------------------------------------------------------------
+
+static mica_status check_list(int32_t T, const int64_t* n, std::initializer_list<const void* const*> arrays,
+                              int64_t* total) {
+    *total = 0;
+    if (T < 0 || T > MICA_MAX_TENSORS) return fail(MICA_ERR_COUNT, "T = %d is outside [0, %d]", T, MICA_MAX_TENSORS);
+    if (T == 0) return MICA_OK;
+    if (!n) return fail(MICA_ERR_NULL, "the element-count array is NULL");
+    for (auto a : arrays)
+        if (!a) return fail(MICA_ERR_NULL, "a pointer array is NULL");
+    for (int32_t k = 0; k < T; ++k) {
+        if (n[k] < 0) return fail(MICA_ERR_COUNT, "n[%d] = %lld is negative", k, (long long)n[k]);
+        if (n[k] > ((int64_t)1 << 40)) return fail(MICA_ERR_COUNT, "n[%d] = %lld is too large", k, (long long)n[k]);
+        if (n[k] == 0) continue;
+        int j = 0;
+        for (auto a : arrays) {
+            if (!a[k]) return fail(MICA_ERR_NULL, "pointer %d of tensor %d is NULL (n = %lld)", j, k, (long long)n[k]);
+            ++j;
+        }
+        *total += n[k];
+    }
+    return MICA_OK;
+}
+
+static mica_status current_device(int* dev) {
+    const cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(MICA_ERR_DEVICE, "no usable CUDA device (%s)", cudaGetErrorName(e));
+    }
+    return MICA_OK;
+}
+
+static bool finite_nonneg(double x) { return std::isfinite(x) && x >= 0.0; }
+
+}  // namespace mica
+
+using namespace mica;
+
+// ----------------------------------------------------------------------------------------------------------------------
+// entry points
+// ----------------------------------------------------------------------------------------------------------------------
+
+extern "C" mica_status mica_scale_tensors(void* const* t, const int64_t* n, int32_t T, mica_dtype dt, float factor,
+                                          const float* d_factor, void* stream) {
+    if (dt != MICA_F32 && dt != MICA_F16) return fail(MICA_ERR_DTYPE, "ScaleTensors takes float32 or float16 tensors");
+    if (!d_factor && !std::isfinite(factor)) return fail(MICA_ERR_HYPER, "factor %g is not finite", (double)factor);
+    int64_t total = 0;
+    mica_status s = check_list(T, n, {t}, &total);
+    if (s != MICA_OK) return s;
+    if (total == 0) return ok();
+    int dev = 0;
+    if ((s = current_device(&dev)) != MICA_OK) return s;
+    if (d_factor && (s = check_device_span(d_factor, 4, 4, dev, "d_factor", 0)) != MICA_OK) return s;
+    ListDesc L{kScale, T, n, reinterpret_cast<float* const*>(t), nullptr, nullptr, nullptr, (Dtype)dt, kF32};
+    Plan* p = nullptr;
+    if ((s = get_plan(L, dev, &p, stream)) != MICA_OK) return s;
+    if (d_factor && overlaps_any(p->spans, d_factor, 4))
+        return fail(MICA_ERR_OVERLAP, "d_factor lies inside one of the tensors");
+    return after_launch(launch_scale(p->recs, p->items, p->num_items, p->item_quads, (Dtype)dt, factor, d_factor,
+                                     stream),
+                        stream, "ScaleTensors launch");
+}
+
+extern "C" mica_status mica_clip_grad_norms(const void* const* g, const int64_t* n, int32_t T, mica_dtype gdt,
+                                            float max_norm, float inv_scale, float* d_norm, float* d_factor,
+                                            void* stream) {
+    if (gdt != MICA_F32 && gdt != MICA_F16) return fail(MICA_ERR_DTYPE, "gradients must be float32 or float16");
+    if (!d_factor) return fail(MICA_ERR_NULL, "d_factor is NULL");
+    if (std::isnan(max_norm) || !(max_norm > 0.0f)) return fail(MICA_ERR_HYPER, "max_norm %g is not > 0", (double)max_norm);
+    if (!std::isfinite(inv_scale) || !(inv_scale > 0.0f))
+        return fail(MICA_ERR_HYPER, "inv_scale %g is not finite and > 0", (double)inv_scale);
+    int64_t total = 0;
+    mica_status s = check_list(T, n, {g}, &total);
+    if (s != MICA_OK) return s;
+    int dev = 0;
+    if ((s = current_device(&dev)) != MICA_OK) return s;
+    if ((s = check_device_span(d_factor, 4, 4, dev, "d_factor", 0)) != MICA_OK) return s;
+    if (d_norm && (s = check_device_span(d_norm, 4, 4, dev, "d_norm", 0)) != MICA_OK) return s;
+    if (d_norm && reinterpret_cast<uintptr_t>(d_norm) + 4 > reinterpret_cast<uintptr_t>(d_factor) &&
+        reinterpret_cast<uintptr_t>(d_factor) + 4 > reinterpret_cast<uintptr_t>(d_norm))
+        return fail(MICA_ERR_OVERLAP, "d_norm and d_factor overlap");
+    // An empty list still gets its norm (0) and factor written: the table then holds no tensors and no items.
+    ListDesc L{kNorm, total ? T : 0, n, nullptr, const_cast<void* const*>(reinterpret_cast<const void* const*>(g)),
+               nullptr, nullptr, (Dtype)gdt, kF32};
+    Plan* p = nullptr;
+    if ((s = get_plan(L, dev, &p, stream)) != MICA_OK) return s;
+    if (overlaps_any(p->spans, d_factor, 4) || (d_norm && overlaps_any(p->spans, d_norm, 4)))
+        return fail(MICA_ERR_OVERLAP, "d_norm or d_factor lies inside a gradient");
+    return after_launch(launch_norm(p->recs, p->items, p->num_items, p->item_quads, (Dtype)gdt, inv_scale,
+                                    p->partials, max_norm, d_norm, d_factor, stream),
+                        stream, "ClipGradNorms launch");
+}
+
+extern "C" mica_status mica_adamw_steps(float* const* w, void* const* g, void* const* m, void* const* v,
+                                        const int64_t* n, int32_t T, mica_dtype gdt, mica_dtype mdt,
+                                        const mica_adamw_hp* hp, const float* d_factor, void* stream) {
+    if (!hp) return fail(MICA_ERR_NULL, "hp is NULL");
+    if (gdt != MICA_F32 && gdt != MICA_F16) return fail(MICA_ERR_DTYPE, "gradients must be float32 or float16");
+    if (mdt != MICA_F32 && mdt != MICA_BF16X2) return fail(MICA_ERR_DTYPE, "moments must be float32 or packed BF16");
+    if (!finite_nonneg(hp->lr)) return fail(MICA_ERR_HYPER, "lr %g is not finite and >= 0", hp->lr);
+    if (!finite_nonneg(hp->eps)) return fail(MICA_ERR_HYPER, "eps %g is not finite and >= 0", hp->eps);
+    if (!finite_nonneg(hp->weight_decay))
+        return fail(MICA_ERR_HYPER, "weight_decay %g is not finite and >= 0", hp->weight_decay);
+    if (hp->step < 1) return fail(MICA_ERR_HYPER, "step %lld is not >= 1", (long long)hp->step);
+    if (hp->reserved != 0) return fail(MICA_ERR_HYPER, "hp->reserved must be 0");
+    if (!(hp->beta1 >= 0.0 && hp->beta1 < 1.0)) return fail(MICA_ERR_BETA, "beta1 %g is outside [0, 1)", hp->beta1);
+    if (!(hp->beta2 >= 0.0 && hp->beta2 < 1.0)) return fail(MICA_ERR_BETA, "beta2 %g is outside [0, 1)", hp->beta2);
+    int64_t total = 0;
+    mica_status s = check_list(T, n, {reinterpret_cast<const void* const*>(w), g, m, v}, &total);
+    if (s != MICA_OK) return s;
+    if (total == 0) return ok();
+    int dev = 0;
+    if ((s = current_device(&dev)) != MICA_OK) return s;
+    if (d_factor && (s = check_device_span(d_factor, 4, 4, dev, "d_factor", 0)) != MICA_OK) return s;
+    ListDesc L{kAdamW, T, n, w, g, m, v, (Dtype)gdt, (Dtype)mdt};
+    Plan* p = nullptr;
+    if ((s = get_plan(L, dev, &p, stream)) != MICA_OK) return s;
+    if (d_factor && overlaps_any(p->spans, d_factor, 4))
+        return fail(MICA_ERR_OVERLAP, "d_factor lies inside one of the step's buffers");
+
+    // the step's scalars: PyTorch's, each in double and rounded once to float32
+    const double t = (double)hp->step;
+    StepScalars sc{};
+    sc.c1 = (float)(1.0 - hp->beta1);
+    sc.b2 = (float)hp->beta2;
+    sc.c2 = (float)(1.0 - hp->beta2);
+    sc.neg_step = -(float)(hp->lr / (1.0 - std::pow(hp->beta1, t)));
+    sc.bc2 = (float)std::sqrt(1.0 - std::pow(hp->beta2, t));
+    sc.dec = (float)(1.0 - hp->lr * hp->weight_decay);
+    sc.eps = (float)hp->eps;
+    sc.zero_grad = hp->zero_grad ? 1 : 0;
+    return after_launch(launch_adamw(p->recs, p->items, p->num_items, p->item_quads, (Dtype)gdt, (Dtype)mdt, sc,
+                                     d_factor, stream),
+                        stream, "AdamWSteps launch");
+}
+
+extern "C" mica_status mica_sync(void* stream) {
+    const cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "mica_sync");
+    return ok();
+}
+
+extern "C" mica_status mica_release_cache(void) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    cudaError_t e = cudaSuccess;
+    if (g_plan_count) e = cudaDeviceSynchronize();
+    g_plans.clear();
+    g_plan_count = 0;
+    if (e != cudaSuccess) return cuda_fail(e, "mica_release_cache");
+    return ok();
+}
+
+extern "C" const char* mica_status_string(mica_status s) {
+    switch (s) {
+        case MICA_OK: return "MICA_OK";
+        case MICA_ERR_NULL: return "MICA_ERR_NULL";
+        case MICA_ERR_COUNT: return "MICA_ERR_COUNT";
+        case MICA_ERR_DTYPE: return "MICA_ERR_DTYPE";
+        case MICA_ERR_HYPER: return "MICA_ERR_HYPER";
+        case MICA_ERR_BETA: return "MICA_ERR_BETA";
+        case MICA_ERR_OVERLAP: return "MICA_ERR_OVERLAP";
+        case MICA_ERR_DEVICE: return "MICA_ERR_DEVICE";
+        case MICA_ERR_ADDRESS: return "MICA_ERR_ADDRESS";
+        case MICA_ERR_CUDA: return "MICA_ERR_CUDA";
+        case MICA_ERR_NOMEM: return "MICA_ERR_NOMEM";
+    }
+    return "MICA_ERR_UNKNOWN";
+}
+
+extern "C" const char* mica_last_error_detail(void) { return t_detail.c_str(); }
+
+extern "C" uint64_t mica_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+extern "C" int32_t mica_abi_version(void) { return 1; }

@@ -1,0 +1,183 @@
+"""Python binding of libmica_optim.so: the same three verbs as the C ABI (include/mica_optim.h), taking torch tensors.
+
+This module only marshals arguments: it collects data pointers, element counts, the current CUDA stream and the
+hyperparameters into the C call, and turns a non-OK status into an exception. Every element of the step is read and
+written by the library's kernels; there is no fallback when the library is missing or the call fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmica_optim.so")
+
+MICA_F32, MICA_F16, MICA_BF16X2 = 0, 1, 2
+STATUS = ["MICA_OK", "MICA_ERR_NULL", "MICA_ERR_COUNT", "MICA_ERR_DTYPE", "MICA_ERR_HYPER", "MICA_ERR_BETA",
+          "MICA_ERR_OVERLAP", "MICA_ERR_DEVICE", "MICA_ERR_ADDRESS", "MICA_ERR_CUDA", "MICA_ERR_NOMEM"]
+
+
+class MicaError(RuntimeError):
+    """A non-OK status from the library; ``status`` is its name, the message the library's one-line detail."""
+
+    def __init__(self, status: int, detail: str):
+        self.status = STATUS[status] if 0 <= status < len(STATUS) else f"status {status}"
+        super().__init__(f"{self.status}: {detail}")
+
+
+class _HP(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double), ("beta2", ctypes.c_double),
+                ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double), ("step", ctypes.c_int64),
+                ("zero_grad", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+_P = ctypes.c_void_p
+_I64P = ctypes.POINTER(ctypes.c_int64)
+_lib: ctypes.CDLL | None = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library. Raises if it has not been built: nothing here runs without it."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m clip_tensor_adamw_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        L.mica_scale_tensors.argtypes = [_P, _I64P, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, _P, _P]
+        L.mica_clip_grad_norms.argtypes = [_P, _I64P, ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
+                                           ctypes.c_float, _P, _P, _P]
+        L.mica_adamw_steps.argtypes = [_P, _P, _P, _P, _I64P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                       ctypes.POINTER(_HP), _P, _P]
+        for f in ("mica_scale_tensors", "mica_clip_grad_norms", "mica_adamw_steps", "mica_sync",
+                  "mica_release_cache"):
+            getattr(L, f).restype = ctypes.c_int
+        L.mica_sync.argtypes = [_P]
+        L.mica_release_cache.argtypes = []
+        L.mica_status_string.argtypes = [ctypes.c_int]
+        L.mica_status_string.restype = ctypes.c_char_p
+        L.mica_last_error_detail.argtypes = []
+        L.mica_last_error_detail.restype = ctypes.c_char_p
+        L.mica_launch_count.argtypes = []
+        L.mica_launch_count.restype = ctypes.c_uint64
+        L.mica_abi_version.argtypes = []
+        L.mica_abi_version.restype = ctypes.c_int32
+        _lib = L
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        raise MicaError(status, lib().mica_last_error_detail().decode())
+
+
+class TensorList:
+    """The pointer and size arrays of a list of tensors, built once and reusable across calls (the tensors must stay
+    alive and in place). Element counts are those of the tensors, or ``sizes`` when given (packed moments hold
+    ceil(n/2) words for n elements, so their list carries the elements' counts)."""
+
+    def __init__(self, tensors: Sequence[torch.Tensor], sizes: Sequence[int] | None = None):
+        self.tensors = list(tensors)
+        T = len(self.tensors)
+        self.T = T
+        self.ptrs = (ctypes.c_void_p * max(T, 1))()
+        for i, t in enumerate(self.tensors):
+            if not t.is_contiguous():
+                raise ValueError(f"tensor {i} is not contiguous")
+            self.ptrs[i] = t.data_ptr() if t.numel() else None
+        counts = [t.numel() for t in self.tensors] if sizes is None else list(sizes)
+        self.n = (ctypes.c_int64 * max(T, 1))(*counts)
+        self.counts = counts
+
+
+def _as_list(x, sizes=None) -> TensorList:
+    return x if isinstance(x, TensorList) else TensorList(x, sizes)
+
+
+def _dtype_code(t: torch.Tensor | None, what: str) -> int:
+    if t is None:
+        return MICA_F32
+    if t.dtype == torch.float32:
+        return MICA_F32
+    if t.dtype == torch.float16:
+        return MICA_F16
+    if t.dtype == torch.int32 or str(t.dtype) == "torch.uint32":  # packed BF16 words
+        return MICA_BF16X2
+    raise TypeError(f"{what}: unsupported dtype {t.dtype}")
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else t.data_ptr()
+
+
+def mica_scale_tensors(tensors, factor: float = 1.0, d_factor: torch.Tensor | None = None, stream=None) -> None:
+    """ScaleTensors: every cell of every tensor times ``factor`` (or the device scalar ``d_factor``), in place."""
+    L = _as_list(tensors)
+    dt = _dtype_code(L.tensors[0] if L.T else None, "tensors")
+    _check(lib().mica_scale_tensors(L.ptrs, L.n, L.T, dt, float(factor), _ptr(d_factor), _stream(stream)))
+
+
+def mica_clip_grad_norms(grads, max_norm: float, inv_scale: float = 1.0, norm_out: torch.Tensor | None = None,
+                         factor_out: torch.Tensor | None = None, stream=None):
+    """ClipGradNorms: the joint norm of the unscaled gradients and the folded clip factor, as two one-element
+    float32 device tensors (``norm_out`` / ``factor_out`` when given). Nothing is copied to the host."""
+    L = _as_list(grads)
+    dev = L.tensors[0].device if L.T else torch.device("cuda", torch.cuda.current_device())
+    if norm_out is None:
+        norm_out = torch.empty(1, dtype=torch.float32, device=dev)
+    if factor_out is None:
+        factor_out = torch.empty(1, dtype=torch.float32, device=dev)
+    gdt = _dtype_code(L.tensors[0] if L.T else None, "grads")
+    _check(lib().mica_clip_grad_norms(L.ptrs, L.n, L.T, gdt, float(max_norm), float(inv_scale), _ptr(norm_out),
+                                      _ptr(factor_out), _stream(stream)))
+    return norm_out, factor_out
+
+
+@dataclass
+class AdamWHyper:
+    lr: float
+    beta1: float
+    beta2: float
+    eps: float
+    weight_decay: float
+
+
+def mica_adamw_steps(w, g, m, v, *, lr: float, beta1: float, beta2: float, eps: float, weight_decay: float,
+                     step: int, zero_grad: bool = False, factor: torch.Tensor | None = None, stream=None) -> None:
+    """AdamWSteps over every group in one launch, in place. ``m`` and ``v`` are float32 tensors of the weights'
+    shapes, or int32 tensors of ceil(n/2) packed BF16 words; ``factor`` is the device scalar from
+    mica_clip_grad_norms (None: 1)."""
+    W = _as_list(w)
+    sizes = W.counts
+    G = _as_list(g)
+    M = _as_list(m, sizes)
+    V = _as_list(v, sizes)
+    if not (W.T == G.T == M.T == V.T):
+        raise ValueError("w, g, m and v must list the same number of tensors")
+    gdt = _dtype_code(G.tensors[0] if G.T else None, "g")
+    mdt = _dtype_code(M.tensors[0] if M.T else None, "m")
+    hp = _HP(float(lr), float(beta1), float(beta2), float(eps), float(weight_decay), int(step), int(bool(zero_grad)),
+             0)
+    _check(lib().mica_adamw_steps(W.ptrs, G.ptrs, M.ptrs, V.ptrs, W.n, W.T, gdt, mdt, ctypes.byref(hp), _ptr(factor),
+                                  _stream(stream)))
+
+
+def mica_sync(stream=None) -> None:
+    _check(lib().mica_sync(_stream(stream)))
+
+
+def mica_release_cache() -> None:
+    _check(lib().mica_release_cache())
+
+
+def mica_launch_count() -> int:
+    return int(lib().mica_launch_count())

@@ -1,0 +1,157 @@
+/*
+ * mica_optim: the clip + AdamW optimizer step on one GB300 (sm_103a), as a C ABI.
+ *
+ * Three verbs, named for those of the Mica 7.7 release note ("Mica 7.7: a training step on the card, in every float
+ * type", section "The whole model in one call"):
+ *
+ *   mica_scale_tensors    ScaleTensors: every cell of several tensors times one factor (a float16 step's unscale).
+ *   mica_clip_grad_norms  ClipGradNorms: the joint L2 norm of every listed gradient and the clip factor, both left
+ *                         in device memory ("Values that stay on the card"); the gradients are not rewritten.
+ *   mica_adamw_steps      AdamWSteps: AdamW over every (w, g, m, v) group in one launch, each group updated exactly
+ *                         as a single-group step would update it.
+ *
+ * The per-element arithmetic is BendTorch "main.bend", section "Optimizers" (AdamW in PyTorch's order of operations;
+ * the part "AdamW over packed BF16 moments (CAdamWBF16)" for packed moments), with PyTorch's scalars:
+ *   step = lr / (1 - beta1^t), bc2 = sqrt(1 - beta2^t), decay w *= 1 - lr*wd,
+ * each computed in double on the host and rounded once to float32.
+ *
+ * Conventions shared by every entry point:
+ *   - Pointer arrays (`w`, `g`, `m`, `v`, `t`) are HOST arrays of DEVICE pointers; `n` is a host array of element
+ *     counts. The library reads them during the call only and keeps no reference to the host arrays.
+ *   - Every tensor buffer belongs to the caller and must be device memory of the current CUDA device. The library
+ *     never allocates per call; it allocates once, per distinct tensor list, a small device table (tensor records,
+ *     work items and, for the norm, one double per work item), kept until mica_release_cache().
+ *   - Work is queued on `stream` (a cudaStream_t; NULL is the legacy default stream) and returns at once. Calls that
+ *     share a tensor list must be ordered on one stream: they share that list's cached table.
+ *   - Validation happens on the host before anything is queued; a call that returns an error has queued nothing.
+ *     A fault of earlier queued work surfaces as MICA_ERR_CUDA from a later call or from mica_sync(). With the
+ *     environment variable MICA_SYNC_DEBUG=1 every call waits for its own kernels, so a fault is reported by the
+ *     call that caused it.
+ *   - A tensor with n[i] == 0 is skipped and its pointers may be NULL. T == 0 is allowed.
+ *   - mica_last_error_detail() gives a one-line description of the last error on the calling thread.
+ */
+#ifndef MICA_OPTIM_H
+#define MICA_OPTIM_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MICA_API __attribute__((visibility("default")))
+#else
+#define MICA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MICA_OK = 0,
+    MICA_ERR_NULL = 1,     /* a required pointer (array, tensor with n > 0, output, hp) is NULL */
+    MICA_ERR_COUNT = 2,    /* T < 0 or T > MICA_MAX_TENSORS, or some n[i] < 0 */
+    MICA_ERR_DTYPE = 3,    /* an element type the call does not take */
+    MICA_ERR_HYPER = 4,    /* lr, eps, weight_decay, step, max_norm, inv_scale or factor out of range / not finite */
+    MICA_ERR_BETA = 5,     /* beta1 or beta2 outside [0, 1), or NaN */
+    MICA_ERR_OVERLAP = 6,  /* two buffers the call writes (or one it writes and one it reads) overlap */
+    MICA_ERR_DEVICE = 7,   /* no usable CUDA device */
+    MICA_ERR_ADDRESS = 8,  /* a pointer is not device memory of the current device, is not aligned to its element,
+                              or its extent runs past the end of its allocation */
+    MICA_ERR_CUDA = 9,     /* a CUDA call failed, including a fault of earlier queued work */
+    MICA_ERR_NOMEM = 10    /* the per-list device table could not be allocated */
+} mica_status;
+
+/* Element types.
+ *   MICA_F32     float32.
+ *   MICA_F16     IEEE binary16 (gradients, and tensors of mica_scale_tensors).
+ *   MICA_BF16X2  packed BF16 moments: a tensor of n elements is ceil(n/2) uint32 words; element 2k is the low 16 bits
+ *                of word k and element 2k+1 the high 16 bits (BendTorch "main.bend", section "The layer protocol",
+ *                the PTree comment). Rounding into it is to nearest, ties to even; a NaN is stored as 0xFFFF. For odd
+ *                n the high half of the last word is never written. */
+typedef enum { MICA_F32 = 0, MICA_F16 = 1, MICA_BF16X2 = 2 } mica_dtype;
+
+#define MICA_MAX_TENSORS (1 << 24)
+
+/* One AdamW step's hyperparameters. */
+typedef struct {
+    double lr;            /* finite, >= 0 */
+    double beta1;         /* [0, 1) */
+    double beta2;         /* [0, 1) */
+    double eps;           /* finite, >= 0 */
+    double weight_decay;  /* finite, >= 0; decoupled: w *= 1 - lr * weight_decay */
+    int64_t step;         /* t, 1-based: the count of steps including this one (>= 1) */
+    int32_t zero_grad;    /* nonzero: the gradient is written back as zeros (BendTorch "main.bend", section "The layer
+                             protocol": a step hands the gradient back zeroed) */
+    int32_t reserved;     /* must be 0 */
+} mica_adamw_hp;
+
+/*
+ * ScaleTensors. For every tensor k and element i < n[k]:  t[k][i] = t[k][i] * f, in place, where f = *d_factor when
+ * d_factor is not NULL (a device float32, read by the kernel) and f = factor otherwise. float16 cells are widened to
+ * float32, multiplied, and rounded back to nearest-even. dt: MICA_F32 or MICA_F16.
+ * Source: "Mica 7.7 ...", section "The whole model in one call" (ScaleTensors).
+ * Errors: NULL / COUNT / DTYPE / HYPER (host factor not finite when d_factor is NULL) / ADDRESS / OVERLAP (two
+ * tensors overlap) / DEVICE / CUDA / NOMEM.
+ */
+MICA_API mica_status mica_scale_tensors(void* const* t, const int64_t* n, int32_t T, mica_dtype dt, float factor,
+                               const float* d_factor, void* stream);
+
+/*
+ * ClipGradNorms, with the unscale folded in. Reads g[k][i] (gdt MICA_F32 or MICA_F16) for every tensor k and
+ * element i < n[k], and writes two device float32 scalars:
+ *   *d_norm   = the joint L2 norm of x = f32(g * inv_scale) over every element of every tensor: the squares are
+ *               formed exactly and summed in double precision in a fixed order, the square root taken in double
+ *               and rounded to float32;
+ *   *d_factor = inv_scale * min(1, max_norm / (norm + 1e-6)) in float32 (PyTorch's clip_grad_norm_ coefficient; a
+ *               NaN norm gives a NaN factor), the one factor mica_adamw_steps multiplies every gradient by.
+ * Neither is copied to the host. d_norm may be NULL (not written); d_factor may not. The gradients are only read.
+ * max_norm: > 0, not NaN (infinity means never clip). inv_scale: finite, > 0 (1 when the loss is not scaled).
+ * Sources: "Mica 7.7 ...", sections "The whole model in one call" and "Values that stay on the card"; BendTorch
+ * "main.bend", section "Losses over arrays" (a running float32 sum of many squares drifts).
+ * Errors: NULL / COUNT / DTYPE / HYPER / ADDRESS / DEVICE / CUDA / NOMEM.
+ */
+MICA_API mica_status mica_clip_grad_norms(const void* const* g, const int64_t* n, int32_t T, mica_dtype gdt, float max_norm,
+                                 float inv_scale, float* d_norm, float* d_factor, void* stream);
+
+/*
+ * AdamWSteps. For every group k and element i < n[k], in float32, each operation rounded on its own:
+ *   gh = g * f                          f = *d_factor (device float32) or 1 when d_factor is NULL
+ *   w' = w * (1 - lr*wd)
+ *   m  = m + (1 - beta1) * (gh - m)
+ *   v  = v * beta2 + ((1 - beta2) * gh) * gh
+ *   [mdt == MICA_BF16X2: m and v rounded to BF16, stored, and read back exactly]
+ *   w  = w' + (-step * m) / (sqrt(v) / bc2 + eps)
+ *   g  = 0                              when hp->zero_grad
+ * w: float32 [n]; g: gdt (MICA_F32 or MICA_F16) [n]; m, v: float32 [n] or packed words [ceil(n/2)] (mdt).
+ * All in place. The results are bit-identical to stepping each group alone, and to the same step on the CPU.
+ * Sources: "Mica 7.7 ...", section "The whole model in one call" (AdamWSteps); BendTorch "main.bend", section
+ * "Optimizers" (the per-element order) and its part "AdamW over packed BF16 moments (CAdamWBF16)".
+ * Errors: NULL / COUNT / DTYPE / HYPER / BETA / ADDRESS / OVERLAP / DEVICE / CUDA / NOMEM.
+ */
+MICA_API mica_status mica_adamw_steps(float* const* w, void* const* g, void* const* m, void* const* v, const int64_t* n,
+                             int32_t T, mica_dtype gdt, mica_dtype mdt, const mica_adamw_hp* hp,
+                             const float* d_factor, void* stream);
+
+/* Waits for `stream` and reports a fault of any work queued on it (MICA_OK or MICA_ERR_CUDA). */
+MICA_API mica_status mica_sync(void* stream);
+
+/* Waits for the current device, then frees every cached per-list device table. Returns MICA_OK or MICA_ERR_CUDA. */
+MICA_API mica_status mica_release_cache(void);
+
+/* A static, human-readable name for a status. */
+MICA_API const char* mica_status_string(mica_status s);
+
+/* One line describing the last error returned on the calling thread ("" if none); valid until the thread's next
+ * call into the library. */
+MICA_API const char* mica_last_error_detail(void);
+
+/* How many kernels this library has queued since it was loaded, over all threads. */
+MICA_API uint64_t mica_launch_count(void);
+
+/* The ABI version of this header: 1. */
+MICA_API int32_t mica_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MICA_OPTIM_H */

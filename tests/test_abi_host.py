@@ -1,0 +1,121 @@
+"""The C ABI without a GPU: the library loads, exports every entry point its header declares, and rejects bad
+arguments on the host, before anything reaches a device, with the documented status codes."""
+import ctypes
+import glob
+import math
+import os
+import re
+
+import pytest
+
+import clip_tensor_adamw_gb300 as mica
+from clip_tensor_adamw_gb300.mica import _HP
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+OK, NULL, COUNT, DTYPE, HYPER, BETA, OVERLAP, DEVICE, ADDRESS, CUDA, NOMEM = range(11)
+
+
+def declared_symbols():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        names += re.findall(r"MICA_API\s+[\w\s\*]+?\b(mica_\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol():
+    L = mica.lib()
+    names = declared_symbols()
+    assert len(names) >= 9
+    for name in names:
+        assert hasattr(L, name), name
+    assert L.mica_abi_version() == 1
+
+
+def test_status_strings():
+    L = mica.lib()
+    for code, name in enumerate(mica.mica.STATUS):
+        assert L.mica_status_string(code).decode() == name
+
+
+def _arr(ctype, vals):
+    return (ctype * max(1, len(vals)))(*vals)
+
+
+def _hp(**kw):
+    d = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, step=1, zero_grad=0, reserved=0)
+    d.update(kw)
+    return _HP(**d)
+
+
+def adamw(T=1, n=(4,), ptrs=0x1000, gdt=0, mdt=0, hp=None, null_arrays=False):
+    L = mica.lib()
+    P = _arr(ctypes.c_void_p, [ptrs] * T)
+    N = _arr(ctypes.c_int64, list(n)[:T])
+    arrays = [None] * 4 if null_arrays else [P, P, P, P]
+    hp_ref = ctypes.byref(hp) if hp is not None else None
+    return L.mica_adamw_steps(*arrays, N, T, gdt, mdt, hp_ref, None, None)
+
+
+def test_adamw_host_validation():
+    assert adamw(hp=None) == NULL
+    assert adamw(hp=_hp(), gdt=2) == DTYPE
+    assert adamw(hp=_hp(), mdt=1) == DTYPE
+    for bad in (dict(lr=math.nan), dict(lr=-1.0), dict(lr=math.inf), dict(eps=-1e-8), dict(eps=math.inf),
+                dict(weight_decay=-0.1), dict(step=0), dict(step=-3), dict(reserved=1)):
+        assert adamw(hp=_hp(**bad)) == HYPER, bad
+    for bad in (dict(beta1=1.0), dict(beta1=-0.1), dict(beta2=math.nan), dict(beta2=1.5)):
+        assert adamw(hp=_hp(**bad)) == BETA, bad
+    assert adamw(T=-1, hp=_hp()) == COUNT
+    assert adamw(T=1, n=(-5,), hp=_hp()) == COUNT
+    assert adamw(T=1, hp=_hp(), null_arrays=True) == NULL
+    assert adamw(T=1, ptrs=0, hp=_hp()) == NULL            # a NULL tensor with n > 0
+    assert adamw(T=1, n=(0,), ptrs=0, hp=_hp()) == OK       # empty tensors may be NULL: nothing to do
+    assert adamw(T=0, hp=_hp()) == OK
+
+
+def test_adamw_needs_device_memory():
+    """A well-formed call with pointers that are not device memory never launches: without a GPU it reports no
+    device, with one it reports the address."""
+    import torch
+    status = adamw(hp=_hp())
+    assert status == (ADDRESS if torch.cuda.is_available() else DEVICE)
+    assert mica.lib().mica_last_error_detail().decode()
+
+
+def test_clip_host_validation():
+    L = mica.lib()
+    G = _arr(ctypes.c_void_p, [0x1000])
+    N = _arr(ctypes.c_int64, [4])
+    f = ctypes.c_void_p(0x2000)
+    assert L.mica_clip_grad_norms(G, N, 1, 0, 1.0, 1.0, None, None, None) == NULL
+    assert L.mica_clip_grad_norms(G, N, 1, 2, 1.0, 1.0, None, f, None) == DTYPE
+    for mx, inv in ((0.0, 1.0), (-1.0, 1.0), (math.nan, 1.0), (1.0, 0.0), (1.0, math.inf), (1.0, -2.0)):
+        assert L.mica_clip_grad_norms(G, N, 1, 0, mx, inv, None, f, None) == HYPER, (mx, inv)
+    assert L.mica_clip_grad_norms(G, N, -2, 0, 1.0, 1.0, None, f, None) == COUNT
+
+
+def test_scale_host_validation():
+    L = mica.lib()
+    t = _arr(ctypes.c_void_p, [0x1000])
+    N = _arr(ctypes.c_int64, [4])
+    assert L.mica_scale_tensors(t, N, 1, 2, 1.0, None, None) == DTYPE
+    assert L.mica_scale_tensors(t, N, 1, 0, math.inf, None, None) == HYPER
+    assert L.mica_scale_tensors(t, N, 1, 0, math.nan, None, None) == HYPER
+    assert L.mica_scale_tensors(None, N, 1, 0, 1.0, None, None) == NULL
+    assert L.mica_scale_tensors(t, N, 0, 0, 1.0, None, None) == OK
+
+
+def test_no_kernels_without_a_device():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("counts launches only on a host without a GPU")
+    assert mica.mica_launch_count() == 0
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    from clip_tensor_adamw_gb300 import mica as m
+    monkeypatch.setattr(m, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(m, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        m.lib()

@@ -1,0 +1,277 @@
+"""The CUDA path (through the C ABI) against the oracle, element by element, on the same seeded inputs.
+
+Small cases span many work items and ragged tails and run 10 consecutive steps compared after every step; the
+full-size workloads run in the launch configuration the benchmark times (the same cached tables, item sizes and
+grids), compared in full (GPT-2 small, the loss-scaled list) or on sampled elements (GPT-2 XL)."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import clip_tensor_adamw_gb300 as mica
+import oracle
+import parity
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+W = workloads.WORKLOADS
+
+
+def small_gpt2_sizes(d=90, layers=2, vocab=1003, ctx=67):
+    return [int(np.prod(s)) for s in workloads._gpt2_shapes(d, layers, vocab, ctx)]
+
+
+RAGGED = [1, 2, 3, 5, 7, 9, 31, 33, 1025, 4097, 16385, 65537, 262147]
+
+
+@pytest.fixture(scope="module")
+def ora():
+    return oracle.Oracle()
+
+
+def test_tiny_ten_steps(ora):
+    r = parity.run_parity(W["tiny"], ora=ora)
+    assert r["same_factor_every_step"]
+
+
+@pytest.mark.parametrize("name", ["gpt2_small", "gpt2_small_bf16", "gpt2_xl"])
+@pytest.mark.parametrize("zero_grad", [False, True])
+def test_small_gpt2_lists(ora, name, zero_grad):
+    r = parity.run_parity(W[name], sizes=small_gpt2_sizes(), ora=ora, zero_grad=zero_grad)
+    assert r["same_factor_every_step"]
+
+
+@pytest.mark.parametrize("name", ["gpt2_small", "gpt2_small_bf16", "fp16_scaled"])
+def test_ragged_sizes(ora, name):
+    r = parity.run_parity(W[name], sizes=RAGGED, ora=ora)
+    assert r["same_factor_every_step"]
+
+
+def test_loss_scaled_small(ora):
+    sizes = list(W["fp16_scaled"].sizes[:700]) + [768 * 3072]
+    r = parity.run_parity(W["fp16_scaled"], sizes=sizes, ora=ora, zero_grad=True)
+    assert r["same_factor_every_step"]
+
+
+def test_fp16_grads_packed_moments(ora):
+    wl = dataclasses.replace(W["fp16_scaled"], name="fp16_packed", moments="bf16x2")
+    r = parity.run_parity(wl, sizes=RAGGED + [3000, 70000], ora=ora)
+    assert r["same_factor_every_step"]
+
+
+def test_empty_tensors_and_list(ora):
+    sizes = [0, 5, 0, 0, 4096, 0, 3]
+    r = parity.run_parity(W["gpt2_small_bf16"], sizes=sizes, ora=ora, steps=3)
+    assert r["same_factor_every_step"]
+    # an empty list: norm 0, factor exactly inv_scale, nothing else happens
+    norm, factor = mica.mica_clip_grad_norms([], 1.0, 0.25)
+    torch.cuda.synchronize()
+    assert norm.item() == 0.0 and factor.item() == 0.25
+    mica.mica_adamw_steps([], [], [], [], lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, step=1)
+
+
+def _misaligned_state(wl, sizes, off):
+    """Tensors placed `off` elements (or packed words) past a 16-byte boundary: the element-by-element path."""
+    st = workloads.make_state(wl, "cuda", sizes=[n + 8 for n in sizes])
+    packed = st.packed
+    st.w = [t[off:off + n] for t, n in zip(st.w, sizes)]
+    st.g = [t[off:off + n] for t, n in zip(st.g, sizes)]
+    words = [(n + 1) // 2 if packed else n for n in sizes]
+    st.m = [t[off:off + k] for t, k in zip(st.m, words)]
+    st.v = [t[off:off + k] for t, k in zip(st.v, words)]
+    st.sizes = list(sizes)
+    return st
+
+
+@pytest.mark.parametrize("name", ["gpt2_small", "gpt2_small_bf16", "fp16_scaled"])
+def test_unaligned_pointers(ora, name):
+    wl = W[name]
+    st = _misaligned_state(wl, [3, 17, 1000, 5001], off=1)
+    lists = parity.tensor_lists(st)
+    host = workloads.host_lists(st)
+    for t in range(1, 4):
+        for g in st.g:
+            g.copy_(torch.randn(g.numel(), device="cuda", generator=workloads._gen("cuda", 100 + t)).to(g.dtype)
+                    * (1e-3 if g.dtype == torch.float32 else 6.0))
+        host = (host[0], [x.copy() for x in workloads.host_lists(st)[1]], host[2], host[3])
+        _, d_factor = parity.gpu_step(st, lists, t)
+        _, o_factor = ora.clip_adamw_step(*host, parity.hp_of(wl, t), wl.max_norm, wl.inv_scale)
+        torch.cuda.synchronize()
+        same = np.float32(d_factor.item()).view(np.uint32) == o_factor.view(np.uint32)
+        parity.compare_state(st, host, bool(same), f"unaligned {name} step {t}")
+
+
+def _plant(values):
+    def hook(st, t):
+        if t == 2:
+            flat = st.g[1]
+            k = min(len(values), flat.numel())
+            flat[:k] = torch.tensor(values[:k], dtype=flat.dtype, device=flat.device)
+    return hook
+
+
+@pytest.mark.parametrize("values", [[float("nan")], [float("inf")], [-float("inf"), 1.0],
+                                    [1e30, -1e30, 3e-39, 1e-45], [3e38, 3e38]],
+                         ids=["nan", "inf", "neg_inf", "huge_and_subnormal", "near_max"])
+@pytest.mark.parametrize("name", ["gpt2_small", "gpt2_small_bf16"])
+def test_special_gradient_values(ora, name, values):
+    r = parity.run_parity(W[name], sizes=[4096, 333, 64], ora=ora, steps=3, grad_hook=_plant(values))
+    assert len(r["norms"]) == 3
+
+
+def test_no_clip_moments_overflow_to_bf16_infinity(ora):
+    wl = dataclasses.replace(W["gpt2_small_bf16"], max_norm=float("inf"))
+    r = parity.run_parity(wl, sizes=[64, 9], ora=ora, steps=2, grad_hook=_plant([1e30, -2e35, 3e38]))
+    assert len(r["norms"]) == 2
+
+
+def test_list_call_equals_per_group_calls():
+    wl = W["gpt2_small_bf16"]
+    sizes = small_gpt2_sizes()
+    a = workloads.make_state(wl, "cuda", sizes=sizes)
+    b = workloads.make_state(wl, "cuda", sizes=sizes)
+    for st in (a, b):
+        workloads.fill_grad(st, 1)
+    factor = torch.tensor([0.37], device="cuda")
+    kw = dict(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps, weight_decay=wl.weight_decay, step=1,
+              factor=factor)
+    mica.mica_adamw_steps(a.w, a.g, a.m, a.v, **kw)
+    for k in range(len(sizes)):
+        mica.mica_adamw_steps(b.w[k:k + 1], b.g[k:k + 1], b.m[k:k + 1], b.v[k:k + 1], **kw)
+    torch.cuda.synchronize()
+    for x, y in ((a.w_flat, b.w_flat), (a.m_flat, b.m_flat), (a.v_flat, b.v_flat)):
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+
+
+def test_deterministic_bits():
+    wl = W["gpt2_small_bf16"]
+    out = []
+    for _ in range(2):
+        st = workloads.make_state(wl, "cuda", sizes=small_gpt2_sizes())
+        lists = parity.tensor_lists(st)
+        norms = []
+        for t in range(1, 4):
+            workloads.fill_grad(st, t)
+            n, _ = parity.gpu_step(st, lists, t)
+            norms.append(n.item())
+        out.append((norms, st.w_flat.clone(), st.m_flat.clone(), st.v_flat.clone()))
+    assert out[0][0] == out[1][0]
+    for x, y in zip(out[0][1:], out[1][1:]):
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+
+
+def test_padding_between_tensors_untouched():
+    """Guard bands: the bytes between tensors in the flat buffers (and past the last) never change."""
+    wl = W["gpt2_small_bf16"]
+    sizes = RAGGED
+    st = workloads.make_state(wl, "cuda", sizes=sizes)
+    sentinel = {}
+    for name in ("w_flat", "g_flat", "m_flat", "v_flat"):
+        flat = getattr(st, name)
+        mask = torch.ones(flat.numel(), dtype=torch.bool, device="cuda")
+        for view in getattr(st, name[0]):
+            if view.numel():
+                start = (view.data_ptr() - flat.data_ptr()) // flat.element_size()
+                mask[start:start + view.numel()] = False
+        as_int = flat.view(torch.int16) if flat.element_size() == 2 else flat.view(torch.int32)
+        bits = torch.randint(-2**15, 2**15, (flat.numel(),), device="cuda").to(as_int.dtype)
+        as_int[mask] = bits[mask]
+        sentinel[name] = (mask, as_int[mask].clone())
+    lists = parity.tensor_lists(st)
+    for t in range(1, 3):
+        workloads.fill_grad(st, t)
+        for name in ("g_flat",):  # fill_grad writes the whole flat gradient: restore the guard bands
+            mask, vals = sentinel[name]
+            flat = getattr(st, name)
+            (flat.view(torch.int16) if flat.element_size() == 2 else flat.view(torch.int32))[mask] = vals
+        parity.gpu_step(st, lists, t, zero_grad=True)
+    torch.cuda.synchronize()
+    for name, (mask, vals) in sentinel.items():
+        flat = getattr(st, name)
+        as_int = flat.view(torch.int16) if flat.element_size() == 2 else flat.view(torch.int32)
+        assert torch.equal(as_int[mask], vals), f"{name}: a guard band changed"
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.float16])
+def test_scale_tensors(ora, dtype):
+    gen = workloads._gen("cuda", 7)
+    ts = [torch.randn(n, device="cuda", generator=gen).mul(300.0).to(dtype) for n in RAGGED]
+    ts[3][0] = float("nan")
+    ts[4][1] = float("inf")
+    host = [t.cpu().numpy().copy() for t in ts]
+    mica.mica_scale_tensors(ts, 0.3)
+    ora.scale_tensors(host, 0.3)
+    dev_factor = torch.tensor([2.0 ** -16], device="cuda")
+    mica.mica_scale_tensors(ts, 123.0, d_factor=dev_factor)  # the device factor wins over the host one
+    ora.scale_tensors(host, 2.0 ** -16)
+    torch.cuda.synchronize()
+    for k, t in enumerate(ts):
+        parity.exact(t.cpu().numpy(), host[k], f"scale {dtype} [{k}]")
+
+
+# ------------------------------------------------------------------------------------------------------------------
+# the full-size workloads, in the benchmark's launch configuration
+# ------------------------------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["gpt2_small", "gpt2_small_bf16", "fp16_scaled"])
+def test_full_size_ten_steps(ora, name):
+    r = parity.run_parity(W[name], ora=ora, check_every_step=False)
+    assert r["same_factor_every_step"]
+    if name != "fp16_scaled":  # the clip fires on these two (expected norms ~11 and ~112)
+        assert all(g > 1.0 for g, _, _, _ in r["norms"])
+
+
+def test_gpt2_xl_sampled(ora):
+    """GPT-2 XL (1.56e9 parameters): the norm checked in full every step against the oracle's norm of the whole
+    gradient; the update checked on ~200k sampled elements (whole packed words), stepped by the oracle on their own
+    with the oracle's factor."""
+    wl = W["gpt2_xl"]
+    st = workloads.make_state(wl, "cuda")
+    lists = parity.tensor_lists(st)
+    rng = np.random.Generator(np.random.PCG64(123))
+    # sampled words per tensor: a few at random plus the first and the last (ragged ends)
+    picks = []
+    for k, n in enumerate(st.sizes):
+        words = (n + 1) // 2
+        sel = np.unique(np.concatenate([rng.integers(0, words, size=min(words, 300)), [0, words - 1]]))
+        picks.append(sel)
+    def gather(tensors, elem):  # elem: element-indexed (w, g) or word-indexed (m, v)
+        out = []
+        for t, sel, n in zip(tensors, picks, st.sizes):
+            idx = torch.from_numpy(sel).cuda()
+            if elem:
+                e = torch.stack([2 * idx, torch.clamp(2 * idx + 1, max=n - 1)], 1).reshape(-1)
+                out.append(t[e].cpu().numpy())
+            else:
+                out.append(t[idx].cpu().numpy().view(np.uint32))
+        return np.concatenate(out)
+    odd_last = np.concatenate([np.r_[np.zeros(2 * len(sel) - 1, bool), [n % 2 == 1]] for sel, n in
+                               zip(picks, st.sizes)])
+    w_s = gather(st.w, True).astype(np.float32)
+    m_s = gather(st.m, False)
+    v_s = gather(st.v, False)
+    for t in range(1, wl.steps + 1):
+        workloads.fill_grad(st, t)
+        g_host = st.g_flat.cpu().numpy()
+        g_views = [g_host[(x.data_ptr() - st.g_flat.data_ptr()) // 4:][:x.numel()] for x in st.g]
+        o_norm, o_factor, _ = ora.clip_grad_norms(g_views, wl.max_norm)
+        g_s = gather(st.g, True).astype(np.float32)
+        g_s[odd_last] = 0.0  # the duplicated index of an odd tensor's last word: its element does not exist
+        ora.adamw_steps([w_s], [g_s], [m_s], [v_s], parity.hp_of(wl, t), factor=o_factor)
+        d_norm, d_factor = parity.gpu_step(st, lists, t)
+        torch.cuda.synchronize()
+        assert abs(d_norm.item() - float(o_norm)) <= parity.NORM_RTOL * float(o_norm)
+        same = np.float32(d_factor.item()).view(np.uint32) == o_factor.view(np.uint32)
+        gw, gm, gv = gather(st.w, True), gather(st.m, False), gather(st.v, False)
+        keep = ~odd_last
+        parity.f32_close(gw[keep], w_s[keep], f"xl w step {t}")
+        if same:
+            parity.exact(gw[keep], w_s[keep], f"xl w bits step {t}")
+            # odd tensors' last words: only the low half is an element; the high half stays as it started (0)
+            parity.exact(gm, m_s, f"xl m bits step {t}")
+            parity.exact(gv, v_s, f"xl v bits step {t}")
+        else:
+            parity.bf16_within_one_ulp(gm, m_s, 2 * gm.size, f"xl m step {t}")
+            parity.bf16_within_one_ulp(gv, v_s, 2 * gv.size, f"xl v step {t}")
