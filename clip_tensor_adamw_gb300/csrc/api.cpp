@@ -29,6 +29,8 @@ void count_launches(uint64_t k) { g_launches.fetch_add(k, std::memory_order_rela
 
 static thread_local std::string t_detail;
 
+void set_error_detail(const char* msg) { t_detail = msg; }
+
 static mica_status fail(mica_status s, const char* fmt, ...) {
     char buf[512];
     va_list ap;
@@ -159,9 +161,12 @@ struct Plan {
     void* dev = nullptr;  // one allocation: TensorRec[T] | WorkItem[I] | double[I] (norm)
     TensorRec* recs = nullptr;
     WorkItem* items = nullptr;
-    double* partials = nullptr;
     int32_t num_items = 0;
-    int32_t item_quads = 0;
+    int32_t item_octs = 0;
+    // norm plans
+    ChunkTable chunks{};
+    double* partials = nullptr;
+    unsigned int* ticket = nullptr;  // the finishing-order counter of the fused finalize
     std::vector<Span> spans;  // the list's buffers, sorted (for checking a call's scalar outputs)
     ~Plan() {
         if (dev) {
@@ -197,50 +202,50 @@ static int sm_count(int device) {
     return n;
 }
 
-// Quads per work item: 4096 (16,384 elements) when the list is large enough to give every SM many items, halved
-// down to 256 for small lists so that all SMs still get work. MICA_ITEM_QUADS overrides it (a power of two).
-static int32_t choose_item_quads(int64_t total_quads, int sms) {
-    if (const char* s = std::getenv("MICA_ITEM_QUADS")) {
+// Octets per work item: 2048 (16,384 elements) when the list is large enough to give every SM many items, halved
+// down to 128 for small lists so that all SMs still get work. MICA_ITEM_OCTS overrides it (a power of two).
+static int32_t choose_item_octs(int64_t total_octs, int sms) {
+    if (const char* s = std::getenv("MICA_ITEM_OCTS")) {
         const long v = std::strtol(s, nullptr, 10);
-        if (v >= 32 && v <= (1 << 20) && (v & (v - 1)) == 0) return (int32_t)v;
+        if (v >= 16 && v <= (1 << 20) && (v & (v - 1)) == 0) return (int32_t)v;
     }
-    int32_t iq = 4096;
+    int32_t io = 2048;
     const int64_t target = (int64_t)sms * 16;
-    while (iq > 256 && total_quads / iq < target) iq /= 2;
-    return iq;
+    while (io > 128 && total_octs / io < target) io /= 2;
+    return io;
 }
 
-// Work items over the tensors' quads (see plan.h).
-static std::vector<WorkItem> build_items(const int64_t* n, int32_t T, int32_t iq) {
+// Work items over the tensors' octets (see plan.h).
+static std::vector<WorkItem> build_items(const int64_t* n, int32_t T, int32_t io) {
     std::vector<WorkItem> items;
-    const int64_t small = iq / 2;
+    const int64_t small = io / 2;
     bool open = false;
     WorkItem pack{};
-    int64_t pack_q = 0;
+    int64_t pack_o = 0;
     auto close = [&] {
         if (open) items.push_back(pack);
         open = false;
     };
     for (int32_t k = 0; k < T; ++k) {
-        const int64_t nq = (n[k] + 3) / 4;
-        if (nq == 0) {
+        const int64_t no = (n[k] + kOct - 1) / kOct;
+        if (no == 0) {
             if (open) pack.count += 1;  // an empty tensor inside a pack costs nothing
             continue;
         }
-        if (nq <= small) {
-            if (open && pack_q + nq <= iq) {
+        if (no <= small) {
+            if (open && pack_o + no <= io) {
                 pack.count += 1;
-                pack_q += nq;
+                pack_o += no;
             } else {
                 close();
                 pack = WorkItem{k, 1, 0};
-                pack_q = nq;
+                pack_o = no;
                 open = true;
             }
             continue;
         }
         close();
-        for (int64_t q = 0; q < nq; q += iq) items.push_back(WorkItem{k, 1, q});
+        for (int64_t o = 0; o < no; o += io) items.push_back(WorkItem{k, 1, o});
     }
     close();
     return items;
@@ -270,19 +275,19 @@ static mica_status build_plan(const ListDesc& L, int device, std::vector<uint64_
     // pointer checks and the overlap check, over every non-empty buffer of the list
     std::vector<Span> spans;
     std::vector<TensorRec> recs((size_t)L.T);
-    int64_t total_quads = 0;
+    int64_t total_octs = 0;
     for (int32_t k = 0; k < L.T; ++k) {
         const int64_t n = L.n[k];
         TensorRec& r = recs[k];
         r = TensorRec{nullptr, nullptr, nullptr, nullptr, n, 0, 0};
         if (n == 0) continue;
-        total_quads += (n + 3) / 4;
+        total_octs += (n + kOct - 1) / kOct;
         mica_status s;
         if (L.kind == kScale) {
             const size_t b = (size_t)n * elem_bytes(L.gdt);
             if ((s = check_device_span(L.w[k], b, elem_bytes(L.gdt), device, "t", k)) != MICA_OK) return s;
             r.w = L.w[k];
-            r.vec = (ptr_u(r.w) % (L.gdt == kF16 ? 8 : 16)) == 0;
+            r.vec = (ptr_u(r.w) % (L.gdt == kF16 ? 16 : 32)) == 0;
             spans.push_back({(uintptr_t)ptr_u(r.w), (uintptr_t)(ptr_u(r.w) + b), 4, k});
             continue;
         }
@@ -290,7 +295,7 @@ static mica_status build_plan(const ListDesc& L, int device, std::vector<uint64_
         if ((s = check_device_span(L.g[k], gb, elem_bytes(L.gdt), device, "g", k)) != MICA_OK) return s;
         r.g = L.g[k];
         spans.push_back({(uintptr_t)ptr_u(r.g), (uintptr_t)(ptr_u(r.g) + gb), 1, k});
-        bool vec = (ptr_u(r.g) % (L.gdt == kF16 ? 8 : 16)) == 0;
+        bool vec = (ptr_u(r.g) % (L.gdt == kF16 ? 16 : 32)) == 0;
         if (L.kind == kAdamW) {
             const size_t wb = (size_t)n * 4;
             const size_t mb = (L.mdt == kBF16x2) ? (size_t)((n + 1) / 2) * 4 : (size_t)n * 4;
@@ -303,8 +308,8 @@ static mica_status build_plan(const ListDesc& L, int device, std::vector<uint64_
             spans.push_back({(uintptr_t)ptr_u(r.w), (uintptr_t)(ptr_u(r.w) + wb), 0, k});
             spans.push_back({(uintptr_t)ptr_u(r.m), (uintptr_t)(ptr_u(r.m) + mb), 2, k});
             spans.push_back({(uintptr_t)ptr_u(r.v), (uintptr_t)(ptr_u(r.v) + mb), 3, k});
-            const uint64_t ma = (L.mdt == kBF16x2) ? 8 : 16;
-            vec = vec && ptr_u(r.w) % 16 == 0 && ptr_u(r.m) % ma == 0 && ptr_u(r.v) % ma == 0;
+            const uint64_t ma = (L.mdt == kBF16x2) ? 16 : 32;
+            vec = vec && ptr_u(r.w) % 32 == 0 && ptr_u(r.m) % ma == 0 && ptr_u(r.v) % ma == 0;
         }
         r.vec = vec ? 1 : 0;
     }
@@ -316,17 +321,46 @@ static mica_status build_plan(const ListDesc& L, int device, std::vector<uint64_
     }
     plan->spans = std::move(spans);
 
-    plan->item_quads = choose_item_quads(total_quads, sm_count(device));
-    std::vector<WorkItem> items = build_items(L.n, L.T, plan->item_quads);
-    if (items.size() > (size_t)INT32_MAX) return fail(MICA_ERR_COUNT, "too many work items (%zu)", items.size());
-    plan->num_items = (int32_t)items.size();
+    const int sms = sm_count(device);
+    std::vector<WorkItem> items;
+    std::vector<int64_t> prefix;
+    std::vector<int32_t> first;
+    if (L.kind == kNorm) {
+        // contiguous equal chunks, four CTAs per SM (at least one octet per thread)
+        prefix.resize((size_t)L.T + 1);
+        prefix[0] = 0;
+        for (int32_t k = 0; k < L.T; ++k) prefix[k + 1] = prefix[k] + (L.n[k] + kOct - 1) / kOct;
+        const int64_t want = std::max<int64_t>(1, (total_octs + kThreads - 1) / kThreads);
+        const int32_t grid = (int32_t)std::min<int64_t>((int64_t)kNormCtasPerSm * sms, want);
+        first.resize((size_t)grid);
+        for (int32_t b = 0; b < grid; ++b) {
+            const int64_t c0 = total_octs * b / grid;
+            // the last tensor whose range starts at or before c0 (empty tensors share their start with the next)
+            int32_t k = (int32_t)(std::upper_bound(prefix.begin(), prefix.end(), c0) - prefix.begin()) - 1;
+            first[b] = std::max(0, std::min(k, std::max(0, L.T - 1)));
+        }
+        plan->chunks.T = L.T;
+        plan->chunks.grid = grid;
+        plan->chunks.total_octs = total_octs;
+    } else {
+        plan->item_octs = choose_item_octs(total_octs, sms);
+        items = build_items(L.n, L.T, plan->item_octs);
+        if (items.size() > (size_t)INT32_MAX) return fail(MICA_ERR_COUNT, "too many work items (%zu)", items.size());
+        plan->num_items = (int32_t)items.size();
+    }
 
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
     const size_t rec_b = recs.size() * sizeof(TensorRec);
-    const size_t item_off = (rec_b + 255) / 256 * 256;
+    const size_t item_off = up(rec_b);
     const size_t item_b = items.size() * sizeof(WorkItem);
-    const size_t part_off = (item_off + item_b + 255) / 256 * 256;
-    const size_t part_b = (L.kind == kNorm) ? std::max<size_t>(items.size(), 1) * sizeof(double) : 0;
-    const size_t total = part_off + part_b;
+    const size_t prefix_off = up(item_off + item_b);
+    const size_t prefix_b = prefix.size() * sizeof(int64_t);
+    const size_t first_off = up(prefix_off + prefix_b);
+    const size_t first_b = first.size() * sizeof(int32_t);
+    const size_t part_off = up(first_off + first_b);
+    const size_t part_b = first.size() * sizeof(double);
+    const size_t ticket_off = up(part_off + part_b);
+    const size_t total = ticket_off + ((L.kind == kNorm) ? 256 : 0);
     cudaError_t e = cudaMalloc(&plan->dev, std::max<size_t>(total, 256));
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -337,12 +371,26 @@ static mica_status build_plan(const ListDesc& L, int device, std::vector<uint64_
     char* base = static_cast<char*>(plan->dev);
     plan->recs = reinterpret_cast<TensorRec*>(base);
     plan->items = reinterpret_cast<WorkItem*>(base + item_off);
-    plan->partials = (L.kind == kNorm) ? reinterpret_cast<double*>(base + part_off) : nullptr;
+    if (L.kind == kNorm) {
+        plan->chunks.recs = plan->recs;
+        plan->chunks.prefix = reinterpret_cast<const int64_t*>(base + prefix_off);
+        plan->chunks.first = reinterpret_cast<const int32_t*>(base + first_off);
+        plan->partials = reinterpret_cast<double*>(base + part_off);
+        plan->ticket = reinterpret_cast<unsigned int*>(base + ticket_off);
+    }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (plan->ticket && (e = cudaMemsetAsync(plan->ticket, 0, sizeof(unsigned int), st)) != cudaSuccess)
+        return cuda_fail(e, "clearing the norm's ticket");
     if (rec_b && (e = cudaMemcpyAsync(plan->recs, recs.data(), rec_b, cudaMemcpyHostToDevice, st)) != cudaSuccess)
         return cuda_fail(e, "uploading the tensor records");
     if (item_b && (e = cudaMemcpyAsync(plan->items, items.data(), item_b, cudaMemcpyHostToDevice, st)) != cudaSuccess)
         return cuda_fail(e, "uploading the work items");
+    if (prefix_b && (e = cudaMemcpyAsync(base + prefix_off, prefix.data(), prefix_b, cudaMemcpyHostToDevice, st)) !=
+                        cudaSuccess)
+        return cuda_fail(e, "uploading the octet prefix");
+    if (first_b && (e = cudaMemcpyAsync(base + first_off, first.data(), first_b, cudaMemcpyHostToDevice, st)) !=
+                       cudaSuccess)
+        return cuda_fail(e, "uploading the chunk starts");
     if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cuda_fail(e, "waiting for the table upload");
     *out = plan.get();
 
@@ -451,7 +499,7 @@ extern "C" mica_status mica_scale_tensors(void* const* t, const int64_t* n, int3
     if ((s = get_plan(L, dev, &p, stream)) != MICA_OK) return s;
     if (d_factor && overlaps_any(p->spans, d_factor, 4))
         return fail(MICA_ERR_OVERLAP, "d_factor lies inside one of the tensors");
-    return after_launch(launch_scale(p->recs, p->items, p->num_items, p->item_quads, (Dtype)dt, factor, d_factor,
+    return after_launch(launch_scale(p->recs, p->items, p->num_items, p->item_octs, (Dtype)dt, factor, d_factor,
                                      stream),
                         stream, "ScaleTensors launch");
 }
@@ -481,8 +529,8 @@ extern "C" mica_status mica_clip_grad_norms(const void* const* g, const int64_t*
     if ((s = get_plan(L, dev, &p, stream)) != MICA_OK) return s;
     if (overlaps_any(p->spans, d_factor, 4) || (d_norm && overlaps_any(p->spans, d_norm, 4)))
         return fail(MICA_ERR_OVERLAP, "d_norm or d_factor lies inside a gradient");
-    return after_launch(launch_norm(p->recs, p->items, p->num_items, p->item_quads, (Dtype)gdt, inv_scale,
-                                    p->partials, max_norm, d_norm, d_factor, stream),
+    return after_launch(launch_norm(p->chunks, (Dtype)gdt, inv_scale, p->partials, p->ticket, max_norm, d_norm,
+                                    d_factor, stream),
                         stream, "ClipGradNorms launch");
 }
 
@@ -524,7 +572,7 @@ extern "C" mica_status mica_adamw_steps(float* const* w, void* const* g, void* c
     sc.dec = (float)(1.0 - hp->lr * hp->weight_decay);
     sc.eps = (float)hp->eps;
     sc.zero_grad = hp->zero_grad ? 1 : 0;
-    return after_launch(launch_adamw(p->recs, p->items, p->num_items, p->item_quads, (Dtype)gdt, (Dtype)mdt, sc,
+    return after_launch(launch_adamw(p->recs, p->items, p->num_items, p->item_octs, (Dtype)gdt, (Dtype)mdt, sc,
                                      d_factor, stream),
                         stream, "AdamWSteps launch");
 }

@@ -1,7 +1,8 @@
-// The hot path's kernels for sm_103a: the joint-norm partials and their fixed-order finalize, the multi-tensor AdamW
-// update, and ScaleTensors. All three are streams over HBM with no data reuse, so they are built for bandwidth:
-// 16-byte vector accesses that coalesce across a warp, several quads in flight per thread, evict-first cache hints,
-// and enough CTAs per SM to keep ~100 KB of loads outstanding on each of the 152 SMs.
+// The hot path's kernels for sm_103a: the joint norm (per-item partial square sums with a fused, fixed-order
+// finalize), the multi-tensor AdamW update, and ScaleTensors. All three stream HBM with no data reuse, so they are
+// built for bandwidth: 32-byte vector accesses (sm_100's 256-bit loads and stores) that coalesce across a warp,
+// evict-first cache hints, several hundred bytes in flight per thread, and the AdamW kernel launched as a
+// programmatic dependent of the norm so that its loads start while the norm finishes.
 //
 // Per-element arithmetic follows BendTorch "main.bend", section "Optimizers": every float32 operation is a separate
 // correctly rounded intrinsic (__fmul_rn, __fadd_rn, __fdiv_rn, __fsqrt_rn), which the compiler never fuses into an
@@ -16,30 +17,48 @@
 namespace mica {
 namespace {
 
-constexpr int kUnrollAdam = 2;   // quads each thread keeps in flight per round (AdamW: 4 streams)
-constexpr int kUnrollNorm = 8;   // (norm: the gradient only)
-constexpr int kUnrollScale = 4;  // (scale: one stream)
+constexpr int kUnrollScale = 2;  // octets in flight per thread and round in ScaleTensors
+
+// AdamW: octets per thread and round; float32 moments move 128 B per octet, packed ones 96 B
+template <Dtype M>
+struct AdamUnroll { static constexpr int value = 1; };
 
 // ------------------------------------------------------------------------------------------------------------------
-// memory access: streaming (evict-first) 16- and 8-byte vectors
+// memory access
 // ------------------------------------------------------------------------------------------------------------------
 
-__device__ __forceinline__ float4 ld_f4(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
-__device__ __forceinline__ void st_f4(float* p, float4 x) { __stcs(reinterpret_cast<float4*>(p), x); }
-__device__ __forceinline__ uint2 ld_u2(const void* p) { return __ldcs(reinterpret_cast<const uint2*>(p)); }
-__device__ __forceinline__ void st_u2(void* p, uint2 x) { __stcs(reinterpret_cast<uint2*>(p), x); }
-
-__device__ __forceinline__ void f4_to(const float4& x, float (&a)[4]) {
-    a[0] = x.x; a[1] = x.y; a[2] = x.z; a[3] = x.w;
+// 32 bytes, not kept in L1, first to leave L2 (each byte is used once)
+__device__ __forceinline__ void ld8_stream(const float* p, float (&a)[8]) {
+    asm volatile("ld.global.L1::no_allocate.L2::evict_first.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=f"(a[0]), "=f"(a[1]), "=f"(a[2]), "=f"(a[3]), "=f"(a[4]), "=f"(a[5]), "=f"(a[6]), "=f"(a[7])
+                 : "l"(p));
 }
-__device__ __forceinline__ float4 f4_of(const float (&a)[4]) { return make_float4(a[0], a[1], a[2], a[3]); }
+__device__ __forceinline__ void st8(float* p, const float (&a)[8]) {
+    asm volatile("st.global.cs.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(a[0]), "f"(a[1]), "f"(a[2]),
+                 "f"(a[3]), "f"(a[4]), "f"(a[5]), "f"(a[6]), "f"(a[7])
+                 : "memory");
+}
+__device__ __forceinline__ uint4 ld16_stream(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.cs.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+__device__ __forceinline__ void st16(void* p, uint4 x) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(x.x), "r"(x.y), "r"(x.z), "r"(x.w)
+                 : "memory");
+}
 
-// four binary16 values (8 bytes) -> float32 (exact)
-__device__ __forceinline__ void h4_to(const uint2& x, float (&a)[4]) {
-    __half2 lo = *reinterpret_cast<const __half2*>(&x.x);
-    __half2 hi = *reinterpret_cast<const __half2*>(&x.y);
-    float2 l = __half22float2(lo), h = __half22float2(hi);
-    a[0] = l.x; a[1] = l.y; a[2] = h.x; a[3] = h.y;
+// eight binary16 values (16 bytes) -> float32 (exact)
+__device__ __forceinline__ void h8_to(const uint4& x, float (&a)[8]) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+        a[2 * k] = f.x;
+        a[2 * k + 1] = f.y;
+    }
 }
 
 // ------------------------------------------------------------------------------------------------------------------
@@ -48,6 +67,15 @@ __device__ __forceinline__ void h4_to(const uint2& x, float (&a)[4]) {
 
 __device__ __forceinline__ float bf16_lo(uint32_t word) { return __uint_as_float(word << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t word) { return __uint_as_float(word & 0xFFFF0000u); }
+
+__device__ __forceinline__ void bf8_to(const uint4& x, float (&a)[8]) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        a[2 * k] = bf16_lo(w[k]);
+        a[2 * k + 1] = bf16_hi(w[k]);
+    }
+}
 
 // Two float32 -> one word, each rounded to nearest-even by the hardware conversion; a NaN is stored as 0xFFFF.
 __device__ __forceinline__ uint32_t pack_bf16x2(float even, float odd) {
@@ -59,17 +87,43 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float even, float odd) {
 }
 
 // ------------------------------------------------------------------------------------------------------------------
-// AdamW on one quad, in registers
+// programmatic dependent launch
+// ------------------------------------------------------------------------------------------------------------------
+
+// Lets the kernel queued after this one start launching (it still waits for this one before using its results).
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Waits until the kernel queued before this one has completed and its writes are visible (returns at once when this
+// kernel was not launched as a programmatic dependent).
+__device__ __forceinline__ void wait_prerequisite() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// The gradient factor, read once per thread right before its first update (after the prerequisite has finished).
+struct Factor {
+    const float* src;
+    float value;
+    bool ready;
+    __device__ __forceinline__ float get() {
+        if (!ready) {
+            wait_prerequisite();
+            value = src ? __ldcg(src) : 1.0f;
+            ready = true;
+        }
+        return value;
+    }
+};
+
+// ------------------------------------------------------------------------------------------------------------------
+// AdamW on one octet, in registers
 // ------------------------------------------------------------------------------------------------------------------
 
 // m, v hold the moments read (float32, or the exact widening of the stored BF16); on return they hold the new
 // moments as the weight update reads them (rounded through BF16 when kPacked), and pm, pv the packed words to store.
 template <bool kPacked>
-__device__ __forceinline__ void adam_quad(float (&w)[4], const float (&g)[4], float (&m)[4], float (&v)[4],
-                                          uint32_t (&pm)[2], uint32_t (&pv)[2], const StepScalars& s, float f) {
-    float wdec[4];
+__device__ __forceinline__ void adam8(float (&w)[8], const float (&g)[8], float (&m)[8], float (&v)[8],
+                                      uint32_t (&pm)[4], uint32_t (&pv)[4], const StepScalars& s, float f) {
+    float wdec[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < 8; ++j) {
         const float gh = __fmul_rn(g[j], f);
         wdec[j] = __fmul_rn(w[j], s.dec);
         m[j] = __fadd_rn(m[j], __fmul_rn(s.c1, __fsub_rn(gh, m[j])));
@@ -77,7 +131,7 @@ __device__ __forceinline__ void adam_quad(float (&w)[4], const float (&g)[4], fl
     }
     if constexpr (kPacked) {
 #pragma unroll
-        for (int p = 0; p < 2; ++p) {
+        for (int p = 0; p < 4; ++p) {
             pm[p] = pack_bf16x2(m[2 * p], m[2 * p + 1]);
             pv[p] = pack_bf16x2(v[2 * p], v[2 * p + 1]);
             m[2 * p] = bf16_lo(pm[p]);
@@ -87,31 +141,39 @@ __device__ __forceinline__ void adam_quad(float (&w)[4], const float (&g)[4], fl
         }
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < 8; ++j) {
         const float denom = __fadd_rn(__fdiv_rn(__fsqrt_rn(v[j]), s.bc2), s.eps);
         w[j] = __fadd_rn(wdec[j], __fdiv_rn(__fmul_rn(s.neg_step, m[j]), denom));
     }
 }
 
-// One quad element by element: for bases not 16-byte aligned and for a tensor's last, partial quad. Elements past n
-// are neither read nor written, nor is the high half of a last packed word that holds no element.
+// One octet element by element: for bases not aligned for the vectors, and for a tensor's last, partial octet.
+// Elements past n are neither read nor written, nor is the high half of a last packed word that holds no element.
 template <Dtype G, Dtype M>
-__device__ void adam_quad_elements(const TensorRec& r, int64_t q, const StepScalars& s, float f) {
-    const int64_t i0 = q * 4;
+__device__ __noinline__ void adam_oct_elements(const TensorRec& r, int64_t o, const StepScalars& s, Factor& fac) {
+    const int64_t i0 = o * kOct;
     const int64_t left = r.n - i0;
-    const int cnt = left < 4 ? (int)left : 4;
-    float w[4] = {0.f, 0.f, 0.f, 0.f}, g[4] = {0.f, 0.f, 0.f, 0.f};
-    float m[4] = {0.f, 0.f, 0.f, 0.f}, v[4] = {0.f, 0.f, 0.f, 0.f};
-    uint32_t om[2] = {0u, 0u}, ov[2] = {0u, 0u}, pm[2], pv[2];
-    for (int j = 0; j < cnt; ++j) {
-        w[j] = r.w[i0 + j];
-        g[j] = (G == kF16) ? __half2float(static_cast<const __half*>(r.g)[i0 + j]) : static_cast<const float*>(r.g)[i0 + j];
+    const int cnt = left < kOct ? (int)left : kOct;
+    float w[8], g[8], m[8], v[8];
+    uint32_t om[4], ov[4], pm[4], pv[4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) w[j] = g[j] = m[j] = v[j] = 0.f;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) om[p] = ov[p] = 0u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        if (j < cnt) {
+            w[j] = r.w[i0 + j];
+            g[j] = (G == kF16) ? __half2float(static_cast<const __half*>(r.g)[i0 + j])
+                               : static_cast<const float*>(r.g)[i0 + j];
+        }
     }
     if constexpr (M == kBF16x2) {
-        for (int p = 0; p < 2; ++p) {
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
             if (2 * p < cnt) {
-                om[p] = static_cast<const uint32_t*>(r.m)[2 * q + p];
-                ov[p] = static_cast<const uint32_t*>(r.v)[2 * q + p];
+                om[p] = static_cast<const uint32_t*>(r.m)[4 * o + p];
+                ov[p] = static_cast<const uint32_t*>(r.v)[4 * o + p];
                 m[2 * p] = bf16_lo(om[p]);
                 m[2 * p + 1] = bf16_hi(om[p]);
                 v[2 * p] = bf16_lo(ov[p]);
@@ -119,196 +181,240 @@ __device__ void adam_quad_elements(const TensorRec& r, int64_t q, const StepScal
             }
         }
     } else {
-        for (int j = 0; j < cnt; ++j) {
-            m[j] = static_cast<const float*>(r.m)[i0 + j];
-            v[j] = static_cast<const float*>(r.v)[i0 + j];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (j < cnt) {
+                m[j] = static_cast<const float*>(r.m)[i0 + j];
+                v[j] = static_cast<const float*>(r.v)[i0 + j];
+            }
         }
     }
-    adam_quad<M == kBF16x2>(w, g, m, v, pm, pv, s, f);
-    for (int j = 0; j < cnt; ++j) {
-        r.w[i0 + j] = w[j];
-        if (s.zero_grad) {
-            if (G == kF16) static_cast<__half*>(r.g)[i0 + j] = __ushort_as_half(0);
-            else static_cast<float*>(r.g)[i0 + j] = 0.f;
+    const float f = fac.get();
+    adam8<M == kBF16x2>(w, g, m, v, pm, pv, s, f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        if (j < cnt) {
+            r.w[i0 + j] = w[j];
+            if (s.zero_grad) {
+                if (G == kF16) static_cast<__half*>(r.g)[i0 + j] = __ushort_as_half(0);
+                else static_cast<float*>(r.g)[i0 + j] = 0.f;
+            }
         }
     }
     if constexpr (M == kBF16x2) {
-        for (int p = 0; p < 2; ++p) {
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
             if (2 * p < cnt) {
                 uint32_t nm = pm[p], nv = pv[p];
                 if (2 * p + 1 >= cnt) {  // the word's high half holds no element: keep it as it was
                     nm = (nm & 0x0000FFFFu) | (om[p] & 0xFFFF0000u);
                     nv = (nv & 0x0000FFFFu) | (ov[p] & 0xFFFF0000u);
                 }
-                static_cast<uint32_t*>(r.m)[2 * q + p] = nm;
-                static_cast<uint32_t*>(r.v)[2 * q + p] = nv;
+                static_cast<uint32_t*>(r.m)[4 * o + p] = nm;
+                static_cast<uint32_t*>(r.v)[4 * o + p] = nv;
             }
         }
     } else {
-        for (int j = 0; j < cnt; ++j) {
-            static_cast<float*>(r.m)[i0 + j] = m[j];
-            static_cast<float*>(r.v)[i0 + j] = v[j];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (j < cnt) {
+                static_cast<float*>(r.m)[i0 + j] = m[j];
+                static_cast<float*>(r.v)[i0 + j] = v[j];
+            }
         }
     }
 }
 
-// Quads [qb, qe) of one tensor, quad qb + lane first, then every `stride`-th.
+// Octets [ob, oe) of one tensor: octet ob + lane first, then every `stride`-th.
 template <Dtype G, Dtype M>
-__device__ __forceinline__ void adam_range(const TensorRec& r, int64_t qb, int64_t qe, int lane, int stride,
-                                           const StepScalars& s, float f) {
-    const int64_t full = r.n >> 2;  // quads with all four elements
+__device__ __forceinline__ void adam_range(const TensorRec& r, int64_t ob, int64_t oe, int lane, int stride,
+                                           const StepScalars& s, Factor& fac) {
+    constexpr int U = AdamUnroll<M>::value;
+    const int64_t full = r.n / kOct;  // octets with all eight elements
     if (r.vec) {
-        const int64_t vend = min(qe, full);
-        for (int64_t q0 = qb + lane; q0 < vend; q0 += (int64_t)stride * kUnrollAdam) {
-            float4 W[kUnrollAdam], Gf[kUnrollAdam], Mf[kUnrollAdam], Vf[kUnrollAdam];
-            uint2 Gh[kUnrollAdam], Mp[kUnrollAdam], Vp[kUnrollAdam];
+        const int64_t vend = oe < full ? oe : full;
+        for (int64_t o0 = ob + lane; o0 < vend; o0 += (int64_t)stride * U) {
+            float W[U][8], Gf[U][8], Mf[U][8], Vf[U][8];
+            uint4 Gh[U], Mp[U], Vp[U];
 #pragma unroll
-            for (int u = 0; u < kUnrollAdam; ++u) {
-                const int64_t q = q0 + (int64_t)u * stride;
-                if (q < vend) {
-                    W[u] = ld_f4(r.w + 4 * q);
-                    if constexpr (G == kF16) Gh[u] = ld_u2(static_cast<const __half*>(r.g) + 4 * q);
-                    else Gf[u] = ld_f4(static_cast<const float*>(r.g) + 4 * q);
+            for (int u = 0; u < U; ++u) {
+                const int64_t o = o0 + (int64_t)u * stride;
+                if (o < vend) {
+                    ld8_stream(r.w + kOct * o, W[u]);
+                    if constexpr (G == kF16) Gh[u] = ld16_stream(static_cast<const __half*>(r.g) + kOct * o);
+                    else ld8_stream(static_cast<const float*>(r.g) + kOct * o, Gf[u]);
                     if constexpr (M == kBF16x2) {
-                        Mp[u] = ld_u2(static_cast<const uint32_t*>(r.m) + 2 * q);
-                        Vp[u] = ld_u2(static_cast<const uint32_t*>(r.v) + 2 * q);
+                        Mp[u] = ld16_stream(static_cast<const uint32_t*>(r.m) + 4 * o);
+                        Vp[u] = ld16_stream(static_cast<const uint32_t*>(r.v) + 4 * o);
                     } else {
-                        Mf[u] = ld_f4(static_cast<const float*>(r.m) + 4 * q);
-                        Vf[u] = ld_f4(static_cast<const float*>(r.v) + 4 * q);
+                        ld8_stream(static_cast<const float*>(r.m) + kOct * o, Mf[u]);
+                        ld8_stream(static_cast<const float*>(r.v) + kOct * o, Vf[u]);
                     }
                 }
             }
+            const float f = fac.get();
 #pragma unroll
-            for (int u = 0; u < kUnrollAdam; ++u) {
-                const int64_t q = q0 + (int64_t)u * stride;
-                if (q < vend) {
-                    float w[4], g[4], m[4], v[4];
-                    uint32_t pm[2], pv[2];
-                    f4_to(W[u], w);
-                    if constexpr (G == kF16) h4_to(Gh[u], g);
-                    else f4_to(Gf[u], g);
+            for (int u = 0; u < U; ++u) {
+                const int64_t o = o0 + (int64_t)u * stride;
+                if (o < vend) {
+                    uint32_t pm[4], pv[4];
+                    if constexpr (G == kF16) h8_to(Gh[u], Gf[u]);
                     if constexpr (M == kBF16x2) {
-                        m[0] = bf16_lo(Mp[u].x); m[1] = bf16_hi(Mp[u].x);
-                        m[2] = bf16_lo(Mp[u].y); m[3] = bf16_hi(Mp[u].y);
-                        v[0] = bf16_lo(Vp[u].x); v[1] = bf16_hi(Vp[u].x);
-                        v[2] = bf16_lo(Vp[u].y); v[3] = bf16_hi(Vp[u].y);
-                    } else {
-                        f4_to(Mf[u], m);
-                        f4_to(Vf[u], v);
+                        bf8_to(Mp[u], Mf[u]);
+                        bf8_to(Vp[u], Vf[u]);
                     }
-                    adam_quad<M == kBF16x2>(w, g, m, v, pm, pv, s, f);
-                    st_f4(r.w + 4 * q, f4_of(w));
+                    adam8<M == kBF16x2>(W[u], Gf[u], Mf[u], Vf[u], pm, pv, s, f);
+                    st8(r.w + kOct * o, W[u]);
                     if constexpr (M == kBF16x2) {
-                        st_u2(static_cast<uint32_t*>(r.m) + 2 * q, make_uint2(pm[0], pm[1]));
-                        st_u2(static_cast<uint32_t*>(r.v) + 2 * q, make_uint2(pv[0], pv[1]));
+                        st16(static_cast<uint32_t*>(r.m) + 4 * o, make_uint4(pm[0], pm[1], pm[2], pm[3]));
+                        st16(static_cast<uint32_t*>(r.v) + 4 * o, make_uint4(pv[0], pv[1], pv[2], pv[3]));
                     } else {
-                        st_f4(static_cast<float*>(r.m) + 4 * q, f4_of(m));
-                        st_f4(static_cast<float*>(r.v) + 4 * q, f4_of(v));
+                        st8(static_cast<float*>(r.m) + kOct * o, Mf[u]);
+                        st8(static_cast<float*>(r.v) + kOct * o, Vf[u]);
                     }
                     if (s.zero_grad) {
-                        if constexpr (G == kF16) st_u2(static_cast<__half*>(r.g) + 4 * q, make_uint2(0u, 0u));
-                        else st_f4(static_cast<float*>(r.g) + 4 * q, make_float4(0.f, 0.f, 0.f, 0.f));
+                        if constexpr (G == kF16) {
+                            st16(static_cast<__half*>(r.g) + kOct * o, make_uint4(0u, 0u, 0u, 0u));
+                        } else {
+                            const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                            st8(static_cast<float*>(r.g) + kOct * o, z);
+                        }
                     }
                 }
             }
         }
-        // the last, partial quad (n % 4 != 0), when it lies in this range
-        if (full < qe && full >= qb && lane == (int)((full - qb) % stride)) adam_quad_elements<G, M>(r, full, s, f);
+        // the last, partial octet (n % 8 != 0), when it lies in this range
+        if (full < oe && full >= ob && lane == (int)((full - ob) % stride)) adam_oct_elements<G, M>(r, full, s, fac);
     } else {
-        for (int64_t q = qb + lane; q < qe; q += stride) adam_quad_elements<G, M>(r, q, s, f);
+        for (int64_t o = ob + lane; o < oe; o += stride) adam_oct_elements<G, M>(r, o, s, fac);
     }
 }
 
+// One CTA per work item, items taken in reverse order (the norm reads them forwards, so the gradient it read last
+// may still be in L2 when this kernel starts).
 template <Dtype G, Dtype M>
-__global__ void __launch_bounds__(kThreads, 2) adamw_kernel(const TensorRec* __restrict__ recs,
-                                                         const WorkItem* __restrict__ items, int32_t num_items,
-                                                         int32_t item_quads, StepScalars s,
-                                                         const float* __restrict__ d_factor) {
-    const float f = d_factor ? __ldg(d_factor) : 1.0f;
+__global__ void __launch_bounds__(kThreads, 3) adamw_kernel(const TensorRec* __restrict__ recs,
+                                                            const WorkItem* __restrict__ items, int32_t num_items,
+                                                            int32_t item_octs, StepScalars s,
+                                                            const float* __restrict__ d_factor) {
+    Factor fac{d_factor, 1.0f, false};
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int32_t it = blockIdx.x; it < num_items; it += gridDim.x) {
-        const WorkItem item = items[it];
+    for (int32_t k = blockIdx.x; k < num_items; k += gridDim.x) {
+        const WorkItem item = items[num_items - 1 - k];
         if (item.count == 1) {
             const TensorRec r = recs[item.t];
-            const int64_t nq = (r.n + 3) >> 2;
-            adam_range<G, M>(r, item.q0, min(item.q0 + (int64_t)item_quads, nq), threadIdx.x, kThreads, s, f);
+            const int64_t no = (r.n + kOct - 1) / kOct;
+            const int64_t oe = item.o0 + item_octs < no ? item.o0 + item_octs : no;
+            adam_range<G, M>(r, item.o0, oe, threadIdx.x, kThreads, s, fac);
         } else {
-            for (int k = warp; k < item.count; k += kWarps) {
-                const TensorRec r = recs[item.t + k];
-                adam_range<G, M>(r, 0, (r.n + 3) >> 2, lane, 32, s, f);
+            for (int j = warp; j < item.count; j += kWarps) {
+                const TensorRec r = recs[item.t + j];
+                adam_range<G, M>(r, 0, (r.n + kOct - 1) / kOct, lane, 32, s, fac);
             }
         }
     }
 }
 
 // ------------------------------------------------------------------------------------------------------------------
-// joint norm: per-item partial square sums, then one fixed-order finalize
+// the joint norm: per-item partial square sums, finalized by the CTA that finishes last
 // ------------------------------------------------------------------------------------------------------------------
 
-// Adds x^2 to the pair (hi, lo) without loss: the product's rounding error comes from an FMA and the sum's from
-// Knuth's two-sum, so hi + lo carries the running sum to about twice float32's precision. This holds while
-// 2^-50 <= |x| < 2^50 (the product error then stays a normal float32 and sums cannot overflow); a zero adds nothing;
-// anything else (tiny, huge, infinite, NaN) is squared and summed in double in `ext`.
-__device__ __forceinline__ void add_square(float x, float& hi, float& lo, double& ext) {
-    const uint32_t ex = (__float_as_uint(x) >> 23) & 0xFFu;
-    if ((ex - 77u) < 100u) {
+// x^2 summed to about twice float32's precision: each square is split exactly into p + e (p = x*x rounded, e its
+// rounding error from an FMA) and p is added to the running hi by Knuth's two-sum, whose exact error joins e in lo.
+// Four independent (hi, lo) chains keep consecutive squares from waiting on one another. This is exact up to the
+// float32 rounding of lo while every |x| lies in [2^-50, 2^50): squares then stay below 2^100 (no overflow) and
+// every e is a normal float32. Elements below 2^-50 in a range whose largest |x| is at least 2^-50 lose at most
+// 2^-150 each, a relative 2^-44 of that range's sum; any other range (a value at or above 2^50, an infinity or
+// NaN, or nothing but values below 2^-50) is summed again in double by the caller.
+struct SumSq {
+    float hi[4], lo[4];
+    float mx;  // the largest |x| seen (NaNs are ignored here and show up in hi instead)
+    __device__ __forceinline__ void add(float x, int c) {
+        mx = fmaxf(mx, fabsf(x));
         const float p = __fmul_rn(x, x);
         const float e = __fmaf_rn(x, x, -p);
-        const float s = __fadd_rn(hi, p);
-        const float bp = __fsub_rn(s, hi);
-        const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(p, bp));
-        hi = s;
-        lo = __fadd_rn(lo, __fadd_rn(err, e));
-    } else if (x != 0.0f) {
-        const double xd = (double)x;
-        ext = __fma_rn(xd, xd, ext);
+        const float s = __fadd_rn(hi[c], p);
+        const float bp = __fsub_rn(s, hi[c]);
+        const float err = __fadd_rn(__fsub_rn(hi[c], __fsub_rn(s, bp)), __fsub_rn(p, bp));
+        hi[c] = s;
+        lo[c] = __fadd_rn(lo[c], __fadd_rn(err, e));
     }
-}
+    __device__ __forceinline__ double total() const {
+        double t = 0.0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) t += (double)hi[c] + (double)lo[c];
+        return t;
+    }
+    __device__ __forceinline__ bool exact(double t) const {
+        return mx < 0x1p50f && !(mx < 0x1p-50f && mx > 0.0f) && t < 0x1p100;
+    }
+};
 
+// Asynchronous 16-byte copies global -> shared (cached in L2 only), in commit groups each thread waits on itself.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Follows the list's octet space forwards: which tensor holds octet o, where that tensor's octets start, and its
+// gradient base, length and vector flag. Octets only move forwards, so each tensor boundary is crossed once.
+struct Cursor {
+    int32_t k;
+    int64_t lo, hi;
+    const char* base;
+    int64_t n;
+    int32_t vec;
+    __device__ __forceinline__ void load(const ChunkTable& ct) {
+        const TensorRec& r = ct.recs[k];
+        base = static_cast<const char*>(r.g);
+        n = r.n;
+        vec = r.vec;
+    }
+    __device__ __forceinline__ void init(const ChunkTable& ct, int32_t k0) {
+        k = k0;
+        if (ct.T > 0) {
+            lo = __ldg(ct.prefix + k0);
+            hi = __ldg(ct.prefix + k0 + 1);
+            load(ct);
+        } else {  // an empty list: no octet is ever asked for
+            lo = hi = 0;
+            base = nullptr;
+            n = 0;
+            vec = 0;
+        }
+    }
+    __device__ __forceinline__ void advance(const ChunkTable& ct, int64_t o) {
+        if (o < hi) return;
+        do {
+            ++k;
+            lo = hi;
+            hi = __ldg(ct.prefix + k + 1);
+        } while (o >= hi);
+        load(ct);
+    }
+};
+
+// Each thread streams its octets through its own slots of a shared-memory ring: kNormStages - 1 octets are always
+// on their way while one is summed, so the bytes in flight cost shared memory, not registers. Slot s of thread t is
+// ring[(2 s + h) * kThreads + t] for the two 16-byte halves h of a float32 octet (h = 0 only for binary16), which
+// keeps every warp's shared-memory reads conflict-free.
+constexpr int kNormStages = 5;
+
+// The elements of octet `local` of the cursor's tensor one by one (zeros past its end).
 template <Dtype G>
-__device__ __forceinline__ void sumsq_range(const TensorRec& r, int64_t qb, int64_t qe, int lane, int stride,
-                                            float inv_scale, float& hi, float& lo, double& ext) {
-    const int64_t full = r.n >> 2;
-    if (r.vec) {
-        const int64_t vend = min(qe, full);
-        for (int64_t q0 = qb + lane; q0 < vend; q0 += (int64_t)stride * kUnrollNorm) {
-            float4 Gf[kUnrollNorm];
-            uint2 Gh[kUnrollNorm];
+__device__ __forceinline__ void load_elements(const Cursor& c, int64_t local, float (&x)[8]) {
+    const int64_t i0 = local * kOct;
 #pragma unroll
-            for (int u = 0; u < kUnrollNorm; ++u) {
-                const int64_t q = q0 + (int64_t)u * stride;
-                if (q < vend) {
-                    if constexpr (G == kF16) Gh[u] = ld_u2(static_cast<const __half*>(r.g) + 4 * q);
-                    else Gf[u] = ld_f4(static_cast<const float*>(r.g) + 4 * q);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < kUnrollNorm; ++u) {
-                const int64_t q = q0 + (int64_t)u * stride;
-                if (q < vend) {
-                    float g[4];
-                    if constexpr (G == kF16) h4_to(Gh[u], g);
-                    else f4_to(Gf[u], g);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) add_square(__fmul_rn(g[j], inv_scale), hi, lo, ext);
-                }
-            }
-        }
-        if (full < qe && full >= qb && lane == (int)((full - qb) % stride)) {
-            for (int64_t i = full * 4; i < r.n; ++i) {
-                const float g = (G == kF16) ? __half2float(static_cast<const __half*>(r.g)[i])
-                                            : static_cast<const float*>(r.g)[i];
-                add_square(__fmul_rn(g, inv_scale), hi, lo, ext);
-            }
-        }
-    } else {
-        for (int64_t q = qb + lane; q < qe; q += stride) {
-            const int64_t end = min(r.n, 4 * q + 4);
-            for (int64_t i = 4 * q; i < end; ++i) {
-                const float g = (G == kF16) ? __half2float(static_cast<const __half*>(r.g)[i])
-                                            : static_cast<const float*>(r.g)[i];
-                add_square(__fmul_rn(g, inv_scale), hi, lo, ext);
-            }
+    for (int j = 0; j < 8; ++j) {
+        if (i0 + j < c.n) {
+            x[j] = (G == kF16) ? __half2float(reinterpret_cast<const __half*>(c.base)[i0 + j])
+                               : reinterpret_cast<const float*>(c.base)[i0 + j];
+        } else {
+            x[j] = 0.0f;
         }
     }
 }
@@ -328,44 +434,13 @@ __device__ __forceinline__ double block_sum(double x, double* red) {
     return t;
 }
 
-template <Dtype G>
-__global__ void __launch_bounds__(kThreads) norm_partials_kernel(const TensorRec* __restrict__ recs,
-                                                                 const WorkItem* __restrict__ items,
-                                                                 int32_t num_items, int32_t item_quads,
-                                                                 float inv_scale, double* __restrict__ partials) {
-    __shared__ double red[kWarps];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int32_t it = blockIdx.x; it < num_items; it += gridDim.x) {
-        const WorkItem item = items[it];
-        float hi = 0.f, lo = 0.f;
-        double ext = 0.0;
-        if (item.count == 1) {
-            const TensorRec r = recs[item.t];
-            const int64_t nq = (r.n + 3) >> 2;
-            sumsq_range<G>(r, item.q0, min(item.q0 + (int64_t)item_quads, nq), threadIdx.x, kThreads, inv_scale,
-                           hi, lo, ext);
-        } else {
-            for (int k = warp; k < item.count; k += kWarps) {
-                const TensorRec r = recs[item.t + k];
-                sumsq_range<G>(r, 0, (r.n + 3) >> 2, lane, 32, inv_scale, hi, lo, ext);
-            }
-        }
-        const double t = block_sum(((double)hi + (double)lo) + ext, red);
-        if (threadIdx.x == 0) partials[it] = t;
-    }
-}
-
-constexpr int kFinalizeThreads = 1024;
-
-// S = the partials summed in a fixed order; norm = f32(sqrt(S)); factor = inv_scale * min(1, max_norm / (norm +
-// 1e-6)) with PyTorch's clip_grad_norm_ rounding (every step in float32) and a NaN passed through.
-__global__ void __launch_bounds__(kFinalizeThreads) norm_finalize_kernel(const double* __restrict__ partials,
-                                                                         int32_t num, float max_norm,
-                                                                         float inv_scale, float* d_norm,
-                                                                         float* d_factor) {
-    __shared__ double red[kFinalizeThreads / 32];
+// S = the partials summed in a fixed order (thread i takes i, i + 256, ... then block_sum); norm = f32(sqrt(S));
+// factor = inv_scale * min(1, max_norm / (norm + 1e-6)) with PyTorch's clip_grad_norm_ rounding (every step in
+// float32) and a NaN passed through.
+__device__ void finalize_norm(const double* partials, int32_t num, float max_norm, float inv_scale, float* d_norm,
+                              float* d_factor, double* red) {
     double acc = 0.0;
-    for (int32_t i = threadIdx.x; i < num; i += kFinalizeThreads) acc += partials[i];
+    for (int32_t i = threadIdx.x; i < num; i += blockDim.x) acc += __ldcg(partials + i);
     const double S = block_sum(acc, red);
     if (threadIdx.x == 0) {
         const float norm = __double2float_rn(__dsqrt_rn(S));
@@ -376,47 +451,153 @@ __global__ void __launch_bounds__(kFinalizeThreads) norm_finalize_kernel(const d
     }
 }
 
+// This thread's octets c0 + t, c0 + t + 256, ... below c1, squared and summed in double: the rare chunks the
+// float32 pairs cannot hold exactly.
+template <Dtype G>
+__device__ __noinline__ double sumsq_chunk_double(const ChunkTable& ct, int32_t k0, int64_t c0, int64_t c1,
+                                                  float inv_scale) {
+    Cursor c;
+    c.init(ct, k0);
+    double t = 0.0;
+    for (int64_t o = c0 + threadIdx.x; o < c1; o += kThreads) {
+        c.advance(ct, o);
+        float x[8];
+        load_elements<G>(c, o - c.lo, x);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const double xd = (double)__fmul_rn(x[j], inv_scale);
+            t = __fma_rn(xd, xd, t);
+        }
+    }
+    return t;
+}
+
+// The joint norm. CTA b streams its equal, contiguous chunk of the list's octets (crossing tensor boundaries),
+// each thread keeping one running sum over the whole chunk; one block reduction gives the CTA's partial; the CTA
+// that finishes last sums every partial in a fixed order and writes norm and factor.
+template <Dtype G>
+__global__ void __launch_bounds__(kThreads, kNormCtasPerSm) norm_kernel(ChunkTable ct, float inv_scale,
+                                                                        double* __restrict__ partials,
+                                                                        unsigned int* ticket, float max_norm,
+                                                                        float* d_norm, float* d_factor) {
+    constexpr int S = kNormStages;
+    constexpr int kOctBytes = (G == kF16) ? 16 : 32;
+    __shared__ double red[kWarps];
+    __shared__ int last;
+    __shared__ float4 ring[2 * S * kThreads];
+    allow_dependents();
+    const bool scaled = inv_scale != 1.0f;
+    const int t = threadIdx.x;
+    const int64_t c0 = ct.total_octs * blockIdx.x / ct.grid;
+    const int64_t c1 = ct.total_octs * (blockIdx.x + 1) / ct.grid;
+    const int32_t k0 = ct.first[blockIdx.x];
+
+    SumSq acc{{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}, 0.f};
+    Cursor ci, cc;  // the issuing side runs S - 1 octets ahead of the consuming side
+    ci.init(ct, k0);
+    cc.init(ct, k0);
+    int64_t o_issue = c0 + t;
+    auto issue = [&](int slot) {
+        if (o_issue < c1) {
+            ci.advance(ct, o_issue);
+            const int64_t local = o_issue - ci.lo;
+            if (ci.vec && local < ci.n / kOct) {
+                const char* src = ci.base + local * kOctBytes;
+                cp_async16(&ring[(2 * slot) * kThreads + t], src);
+                if constexpr (G != kF16) cp_async16(&ring[(2 * slot + 1) * kThreads + t], src + 16);
+            }
+        }
+        cp_async_commit();  // one group per octet, empty where nothing was copied, so the count stays in step
+        o_issue += kThreads;
+    };
+#pragma unroll
+    for (int s = 0; s < S - 1; ++s) issue(s);
+    int slot = 0;
+    for (int64_t o = c0 + t; o < c1; o += kThreads) {
+        cp_async_wait<S - 2>();  // this octet's group has landed
+        cc.advance(ct, o);
+        const int64_t local = o - cc.lo;
+        float x[8];
+        if (cc.vec && local < cc.n / kOct) {
+            const float4 a = ring[(2 * slot) * kThreads + t];
+            if constexpr (G == kF16) {
+                h8_to(*reinterpret_cast<const uint4*>(&a), x);
+            } else {
+                const float4 b = ring[(2 * slot + 1) * kThreads + t];
+                x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+                x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+            }
+        } else {  // a tensor's partial last octet, or an unaligned tensor
+            load_elements<G>(cc, local, x);
+        }
+        issue(slot == 0 ? S - 1 : slot - 1);  // refill the slot emptied one octet ago
+        slot = (slot + 1 == S) ? 0 : slot + 1;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc.add(scaled ? __fmul_rn(x[j], inv_scale) : x[j], j & 3);
+    }
+    cp_async_wait_all();
+    double mine = acc.total();
+    if (!acc.exact(mine)) mine = sumsq_chunk_double<G>(ct, k0, c0, c1, scaled ? inv_scale : 1.0f);
+
+    const double part = block_sum(mine, red);
+    if (t == 0) {
+        partials[blockIdx.x] = part;
+        __threadfence();  // the partial is visible before the ticket says so
+        last = (atomicAdd(ticket, 1u) == (unsigned int)(ct.grid - 1));
+    }
+    __syncthreads();
+    if (last) {  // every other CTA's partial is written: sum them all, in order
+        __threadfence();
+        finalize_norm(partials, ct.grid, max_norm, inv_scale, d_norm, d_factor, red);
+        if (t == 0) *ticket = 0u;  // ready for the next launch on this list
+    }
+}
+
 // ------------------------------------------------------------------------------------------------------------------
 // ScaleTensors
 // ------------------------------------------------------------------------------------------------------------------
 
 template <Dtype T>
-__device__ __forceinline__ void scale_range(const TensorRec& r, int64_t qb, int64_t qe, int lane, int stride,
+__device__ __forceinline__ void scale_range(const TensorRec& r, int64_t ob, int64_t oe, int lane, int stride,
                                             float f) {
-    const int64_t full = r.n >> 2;
-    const int64_t vend = r.vec ? min(qe, full) : qb;
-    for (int64_t q0 = qb + lane; q0 < vend; q0 += (int64_t)stride * kUnrollScale) {
-        float4 X[kUnrollScale];
-        uint2 H[kUnrollScale];
+    constexpr int U = kUnrollScale;
+    const int64_t full = r.n / kOct;
+    const int64_t vend = r.vec ? (oe < full ? oe : full) : ob;
+    for (int64_t o0 = ob + lane; o0 < vend; o0 += (int64_t)stride * U) {
+        float X[U][8];
+        uint4 H[U];
 #pragma unroll
-        for (int u = 0; u < kUnrollScale; ++u) {
-            const int64_t q = q0 + (int64_t)u * stride;
-            if (q < vend) {
-                if constexpr (T == kF16) H[u] = ld_u2(reinterpret_cast<const __half*>(r.w) + 4 * q);
-                else X[u] = ld_f4(r.w + 4 * q);
+        for (int u = 0; u < U; ++u) {
+            const int64_t o = o0 + (int64_t)u * stride;
+            if (o < vend) {
+                if constexpr (T == kF16) H[u] = ld16_stream(reinterpret_cast<const __half*>(r.w) + kOct * o);
+                else ld8_stream(r.w + kOct * o, X[u]);
             }
         }
 #pragma unroll
-        for (int u = 0; u < kUnrollScale; ++u) {
-            const int64_t q = q0 + (int64_t)u * stride;
-            if (q < vend) {
-                float a[4];
-                if constexpr (T == kF16) h4_to(H[u], a);
-                else f4_to(X[u], a);
+        for (int u = 0; u < U; ++u) {
+            const int64_t o = o0 + (int64_t)u * stride;
+            if (o < vend) {
+                if constexpr (T == kF16) h8_to(H[u], X[u]);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) a[j] = __fmul_rn(a[j], f);
+                for (int j = 0; j < 8; ++j) X[u][j] = __fmul_rn(X[u][j], f);
                 if constexpr (T == kF16) {
-                    __half2 lo = __floats2half2_rn(a[0], a[1]), hi = __floats2half2_rn(a[2], a[3]);
-                    st_u2(reinterpret_cast<__half*>(r.w) + 4 * q,
-                          make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi)));
+                    uint32_t h[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const __half2 p = __floats2half2_rn(X[u][2 * k], X[u][2 * k + 1]);
+                        h[k] = *reinterpret_cast<const uint32_t*>(&p);
+                    }
+                    st16(reinterpret_cast<__half*>(r.w) + kOct * o, make_uint4(h[0], h[1], h[2], h[3]));
                 } else {
-                    st_f4(r.w + 4 * q, f4_of(a));
+                    st8(r.w + kOct * o, X[u]);
                 }
             }
         }
     }
-    // elements not covered by vectors: the partial last quad, or everything when unaligned
-    const int64_t eb = (vend > qb ? vend : qb) * 4, ee = min(r.n, qe * 4);
+    // elements not covered by vectors: the partial last octet, or everything when unaligned
+    const int64_t eb = (vend > ob ? vend : ob) * kOct;
+    const int64_t ee = r.n < oe * kOct ? r.n : oe * kOct;
     for (int64_t i = eb + lane; i < ee; i += stride) {
         if constexpr (T == kF16) {
             __half* p = reinterpret_cast<__half*>(r.w) + i;
@@ -430,26 +611,41 @@ __device__ __forceinline__ void scale_range(const TensorRec& r, int64_t qb, int6
 template <Dtype T>
 __global__ void __launch_bounds__(kThreads) scale_kernel(const TensorRec* __restrict__ recs,
                                                          const WorkItem* __restrict__ items, int32_t num_items,
-                                                         int32_t item_quads, float factor,
+                                                         int32_t item_octs, float factor,
                                                          const float* __restrict__ d_factor) {
-    const float f = d_factor ? __ldg(d_factor) : factor;
+    const float f = d_factor ? __ldcg(d_factor) : factor;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int32_t it = blockIdx.x; it < num_items; it += gridDim.x) {
         const WorkItem item = items[it];
         if (item.count == 1) {
             const TensorRec r = recs[item.t];
-            const int64_t nq = (r.n + 3) >> 2;
-            scale_range<T>(r, item.q0, min(item.q0 + (int64_t)item_quads, nq), threadIdx.x, kThreads, f);
+            const int64_t no = (r.n + kOct - 1) / kOct;
+            scale_range<T>(r, item.o0, item.o0 + item_octs < no ? item.o0 + item_octs : no, threadIdx.x, kThreads,
+                           f);
         } else {
-            for (int k = warp; k < item.count; k += kWarps) {
-                const TensorRec r = recs[item.t + k];
-                scale_range<T>(r, 0, (r.n + 3) >> 2, lane, 32, f);
+            for (int j = warp; j < item.count; j += kWarps) {
+                const TensorRec r = recs[item.t + j];
+                scale_range<T>(r, 0, (r.n + kOct - 1) / kOct, lane, 32, f);
             }
         }
     }
 }
 
-int grid_for(int32_t num_items) { return num_items; }
+template <Dtype G, Dtype M>
+cudaError_t launch_adamw_t(dim3 grid, cudaStream_t st, const TensorRec* recs, const WorkItem* items,
+                           int32_t num_items, int32_t item_octs, const StepScalars& s, const float* d_factor) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, adamw_kernel<G, M>, recs, items, num_items, item_octs, s, d_factor);
+}
 
 }  // namespace
 
@@ -457,52 +653,45 @@ int grid_for(int32_t num_items) { return num_items; }
 // launchers
 // ------------------------------------------------------------------------------------------------------------------
 
-int launch_adamw(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_quads, Dtype gdt,
+int launch_adamw(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_octs, Dtype gdt,
                  Dtype mdt, const StepScalars& s, const float* d_factor, void* stream) {
     if (num_items <= 0) return (int)cudaSuccess;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const dim3 grid(grid_for(num_items)), block(kThreads);
+    const dim3 grid(num_items);
+    cudaError_t e;
     if (gdt == kF32 && mdt == kF32)
-        adamw_kernel<kF32, kF32><<<grid, block, 0, st>>>(recs, items, num_items, item_quads, s, d_factor);
+        e = launch_adamw_t<kF32, kF32>(grid, st, recs, items, num_items, item_octs, s, d_factor);
     else if (gdt == kF32 && mdt == kBF16x2)
-        adamw_kernel<kF32, kBF16x2><<<grid, block, 0, st>>>(recs, items, num_items, item_quads, s, d_factor);
+        e = launch_adamw_t<kF32, kBF16x2>(grid, st, recs, items, num_items, item_octs, s, d_factor);
     else if (gdt == kF16 && mdt == kF32)
-        adamw_kernel<kF16, kF32><<<grid, block, 0, st>>>(recs, items, num_items, item_quads, s, d_factor);
+        e = launch_adamw_t<kF16, kF32>(grid, st, recs, items, num_items, item_octs, s, d_factor);
     else
-        adamw_kernel<kF16, kBF16x2><<<grid, block, 0, st>>>(recs, items, num_items, item_quads, s, d_factor);
+        e = launch_adamw_t<kF16, kBF16x2>(grid, st, recs, items, num_items, item_octs, s, d_factor);
     count_launches(1);
-    return (int)cudaGetLastError();
+    return (int)(e != cudaSuccess ? e : cudaGetLastError());
 }
 
-int launch_norm(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_quads, Dtype gdt,
-                float inv_scale, double* partials, float max_norm, float* d_norm, float* d_factor, void* stream) {
+int launch_norm(const ChunkTable& ct, Dtype gdt, float inv_scale, double* partials, unsigned int* ticket,
+                float max_norm, float* d_norm, float* d_factor, void* stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (num_items > 0) {
-        const dim3 grid(grid_for(num_items)), block(kThreads);
-        if (gdt == kF16)
-            norm_partials_kernel<kF16><<<grid, block, 0, st>>>(recs, items, num_items, item_quads, inv_scale,
-                                                               partials);
-        else
-            norm_partials_kernel<kF32><<<grid, block, 0, st>>>(recs, items, num_items, item_quads, inv_scale,
-                                                               partials);
-        count_launches(1);
-        const cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return (int)e;
-    }
-    norm_finalize_kernel<<<1, kFinalizeThreads, 0, st>>>(partials, num_items, max_norm, inv_scale, d_norm, d_factor);
+    const dim3 grid(ct.grid > 0 ? ct.grid : 1), block(kThreads);
+    if (gdt == kF16)
+        norm_kernel<kF16><<<grid, block, 0, st>>>(ct, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
+    else
+        norm_kernel<kF32><<<grid, block, 0, st>>>(ct, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
     count_launches(1);
     return (int)cudaGetLastError();
 }
 
-int launch_scale(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_quads, Dtype dt,
+int launch_scale(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_octs, Dtype dt,
                  float factor, const float* d_factor, void* stream) {
     if (num_items <= 0) return (int)cudaSuccess;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const dim3 grid(grid_for(num_items)), block(kThreads);
+    const dim3 grid(num_items), block(kThreads);
     if (dt == kF16)
-        scale_kernel<kF16><<<grid, block, 0, st>>>(recs, items, num_items, item_quads, factor, d_factor);
+        scale_kernel<kF16><<<grid, block, 0, st>>>(recs, items, num_items, item_octs, factor, d_factor);
     else
-        scale_kernel<kF32><<<grid, block, 0, st>>>(recs, items, num_items, item_quads, factor, d_factor);
+        scale_kernel<kF32><<<grid, block, 0, st>>>(recs, items, num_items, item_octs, factor, d_factor);
     count_launches(1);
     return (int)cudaGetLastError();
 }

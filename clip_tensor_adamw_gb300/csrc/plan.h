@@ -1,14 +1,17 @@
-// Internal layout shared by the host plan builder (plan.cpp) and the kernels (kernels.cu).
+// Internal layout shared by the host side (api.cpp: validation, tables, launches) and the kernels (kernels.cu).
 //
 // A call's tensor list becomes one device table:
 //   TensorRec[T]   the four base pointers and the element count of every tensor;
 //   WorkItem[I]    the units of work one CTA takes at a time;
-//   double[I]      (norm plans only) one partial square sum per work item.
+// and a norm's list instead becomes
+//   TensorRec[T], int64 prefix[T + 1], int32 first[G], double partials[G] and a 32-bit ticket counter
+// (see ChunkTable).
 //
-// Work items are counted in quads (4 consecutive elements, one 16-byte float32 vector). A large tensor is cut into
-// slices of `item_quads` quads; runs of consecutive small tensors (each at most item_quads / 2 quads) are packed
-// into one item whose tensors the CTA's warps share out. Every element belongs to exactly one item, so each element
-// is read and written by exactly one thread per launch and the results do not depend on how items are scheduled.
+// Work items are counted in octets (8 consecutive elements: one 32-byte float32 vector, one 16-byte vector of
+// binary16 values or of 4 packed BF16 words). A large tensor is cut into slices of `item_octs` octets; runs of
+// consecutive small tensors (each at most item_octs / 2 octets) are packed into one item whose tensors the CTA's
+// warps share out. Every element belongs to exactly one item, so each element is read and written by exactly one
+// thread per launch and the results do not depend on how items are scheduled.
 #pragma once
 
 #include <cstdint>
@@ -17,6 +20,8 @@ namespace mica {
 
 constexpr int kThreads = 256;  // threads per CTA of every streaming kernel
 constexpr int kWarps = kThreads / 32;
+constexpr int kOct = 8;        // elements per vector unit
+constexpr int kNormCtasPerSm = 4;  // resident CTAs per SM of the norm kernel (its grid is this times the SM count)
 
 struct TensorRec {
     float* w;      // weights (AdamW) / the tensor itself (scale) / unused (norm)
@@ -24,17 +29,30 @@ struct TensorRec {
     void* m;       // first moment
     void* v;       // second moment
     int64_t n;     // elements
-    int32_t vec;   // 1 when every base pointer is 16-byte aligned (the quad-vector path); 0: element path
+    int32_t vec;   // 1 when every base pointer is aligned for its octet vector (32 B for float32 streams, 16 B for
+                   // binary16 and packed streams): the vector path; 0: the element path
     int32_t pad;
 };
 static_assert(sizeof(TensorRec) == 48, "TensorRec layout");
 
 struct WorkItem {
     int32_t t;      // first tensor
-    int32_t count;  // 1: quads [q0, min(q0 + item_quads, ceil(n/4))) of tensor t; > 1: tensors t .. t+count-1 whole
-    int64_t q0;     // first quad of a slice (0 for a pack)
+    int32_t count;  // 1: octets [o0, min(o0 + item_octs, ceil(n/8))) of tensor t; > 1: tensors t .. t+count-1 whole
+    int64_t o0;     // first octet of a slice (0 for a pack)
 };
 static_assert(sizeof(WorkItem) == 16, "WorkItem layout");
+
+// A list walked as contiguous chunks of its octet space (the norm's layout): tensor k holds the list's octets
+// [prefix[k], prefix[k+1]); CTA b of `grid` takes octets [total*b/grid, total*(b+1)/grid), starting in tensor
+// first[b]. Every CTA gets the same number of octets whatever the tensors' sizes.
+struct ChunkTable {
+    const TensorRec* recs;
+    const int64_t* prefix;  // T + 1 entries
+    const int32_t* first;   // grid entries
+    int32_t T;
+    int32_t grid;
+    int64_t total_octs;
+};
 
 // The step's float32 scalars, each computed in double on the host and rounded once.
 struct StepScalars {
@@ -51,14 +69,22 @@ struct StepScalars {
 enum Dtype : int32_t { kF32 = 0, kF16 = 1, kBF16x2 = 2 };
 
 // Kernel launchers (kernels.cu). Each returns the cudaError_t of its launch as an int.
-int launch_adamw(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_quads, Dtype gdt,
+// AdamW over every item. It is launched as a programmatic dependent of the kernel queued before it: it may start
+// and load its tensors while that kernel finishes, and reads d_factor only once that kernel has completed.
+int launch_adamw(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_octs, Dtype gdt,
                  Dtype mdt, const StepScalars& s, const float* d_factor, void* stream);
-int launch_norm(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_quads, Dtype gdt,
-                float inv_scale, double* partials, float max_norm, float* d_norm, float* d_factor, void* stream);
-int launch_scale(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_quads, Dtype dt,
+// The joint norm in one launch of ct.grid CTAs: one partial square sum per CTA into `partials` (ct.grid doubles),
+// and the CTA that finishes last sums them in a fixed order and writes norm and factor. `ticket` must be 0 before
+// the launch; the kernel leaves it 0.
+int launch_norm(const ChunkTable& ct, Dtype gdt, float inv_scale, double* partials, unsigned int* ticket,
+                float max_norm, float* d_norm, float* d_factor, void* stream);
+int launch_scale(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_octs, Dtype dt,
                  float factor, const float* d_factor, void* stream);
 
 // kernels queued so far (incremented by the launchers)
 void count_launches(uint64_t k);
+
+// sets the calling thread's one-line error detail (what mica_last_error_detail returns)
+void set_error_detail(const char* msg);
 
 }  // namespace mica

@@ -14,7 +14,8 @@ from typing import Sequence
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libmica_optim.so")
+# the library this package builds; MICA_LIB names another build of the same ABI instead
+LIB_PATH = os.environ.get("MICA_LIB") or os.path.join(_PKG, "libmica_optim.so")
 
 MICA_F32, MICA_F16, MICA_BF16X2 = 0, 1, 2
 STATUS = ["MICA_OK", "MICA_ERR_NULL", "MICA_ERR_COUNT", "MICA_ERR_DTYPE", "MICA_ERR_HYPER", "MICA_ERR_BETA",
