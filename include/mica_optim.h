@@ -131,6 +131,28 @@ MICA_API mica_status mica_adamw_steps(float* const* w, void* const* g, void* con
                              int32_t T, mica_dtype gdt, mica_dtype mdt, const mica_adamw_hp* hp,
                              const float* d_factor, void* stream);
 
+/*
+ * ClipGradNorms for callers that cannot let a library allocate device memory: a runtime that reserves its whole
+ * device-memory budget at start-up and treats any later cudaMalloc as a failure, a caller whose memory is all held
+ * by another allocator, or a loop that cannot afford cudaMalloc's implicit synchronisation. The method's pages have
+ * no counterpart to this entry point; it is an addition of this library.
+ *
+ * Arguments, results and errors are those of mica_clip_grad_norms (same kernel, same arithmetic). The difference is
+ * where the scratch lives: instead of a per-list table allocated on first use, every call copies its tables into
+ * one fixed device array of this library (930,304 bytes, held by every GPU that loads the library until the
+ * process exits) and launches on `stream`. Limits: at most 16,384 tensors (MICA_ERR_COUNT beyond, with a detail
+ * naming the limit). The call allocates nothing: no cudaMalloc, no cudaFree, no host heap.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with that device
+ *     current; make that first call before any stream capture.
+ *   - The array is shared by every call and keeps the last call's contents; each call rewrites what it reads, so
+ *     calls ordered on one stream are safe, while calls that overlap on the GPU (other streams, other threads'
+ *     streams) race on it.
+ *   - The table copies come from a static host buffer, so the host side of concurrent calls is serialised.
+ */
+MICA_API mica_status mica_clip_grad_norms_noalloc(const void* const* g, const int64_t* n, int32_t T, mica_dtype gdt,
+                                                  float max_norm, float inv_scale, float* d_norm, float* d_factor,
+                                                  void* stream);
+
 /* Waits for `stream` and reports a fault of any work queued on it (MICA_OK or MICA_ERR_CUDA). */
 MICA_API mica_status mica_sync(void* stream);
 
