@@ -321,13 +321,13 @@ __global__ void __launch_bounds__(kThreads, 3) adamw_kernel(const TensorRec* __r
 
 // x^2 summed to about twice float32's precision: each square is split exactly into p + e (p = x*x rounded, e its
 // rounding error from an FMA) and p is added to the running hi by Knuth's two-sum, whose exact error joins e in lo.
-// Four independent (hi, lo) chains keep consecutive squares from waiting on one another. This is exact up to the
+// Two independent (hi, lo) chains keep consecutive squares from waiting on one another. This is exact up to the
 // float32 rounding of lo while every |x| lies in [2^-50, 2^50): squares then stay below 2^100 (no overflow) and
 // every e is a normal float32. Elements below 2^-50 in a range whose largest |x| is at least 2^-50 lose at most
 // 2^-150 each, a relative 2^-44 of that range's sum; any other range (a value at or above 2^50, an infinity or
 // NaN, or nothing but values below 2^-50) is summed again in double by the caller.
 struct SumSq {
-    float hi[4], lo[4];
+    float hi[2], lo[2];
     float mx;  // the largest |x| seen (NaNs are ignored here and show up in hi instead)
     __device__ __forceinline__ void add(float x, int c) {
         mx = fmaxf(mx, fabsf(x));
@@ -342,23 +342,13 @@ struct SumSq {
     __device__ __forceinline__ double total() const {
         double t = 0.0;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) t += (double)hi[c] + (double)lo[c];
+        for (int c = 0; c < 2; ++c) t += (double)hi[c] + (double)lo[c];
         return t;
     }
     __device__ __forceinline__ bool exact(double t) const {
         return mx < 0x1p50f && !(mx < 0x1p-50f && mx > 0.0f) && t < 0x1p100;
     }
 };
-
-// Asynchronous 16-byte copies global -> shared (cached in L2 only), in commit groups each thread waits on itself.
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-    const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Follows the list's octet space forwards: which tensor holds octet o, where that tensor's octets start, and its
 // gradient base, length and vector flag. Octets only move forwards, so each tensor boundary is crossed once.
@@ -367,11 +357,13 @@ struct Cursor {
     int64_t lo, hi;
     const char* base;
     int64_t n;
+    int64_t full;  // octets of the tensor with all eight elements
     int32_t vec;
     __device__ __forceinline__ void load(const ChunkTable& ct) {
         const TensorRec& r = ct.recs[k];
         base = static_cast<const char*>(r.g);
         n = r.n;
+        full = r.n / kOct;
         vec = r.vec;
     }
     __device__ __forceinline__ void init(const ChunkTable& ct, int32_t k0) {
@@ -384,6 +376,7 @@ struct Cursor {
             lo = hi = 0;
             base = nullptr;
             n = 0;
+            full = 0;
             vec = 0;
         }
     }
@@ -397,12 +390,6 @@ struct Cursor {
         load(ct);
     }
 };
-
-// Each thread streams its octets through its own slots of a shared-memory ring: kNormStages - 1 octets are always
-// on their way while one is summed, so the bytes in flight cost shared memory, not registers. Slot s of thread t is
-// ring[(2 s + h) * kThreads + t] for the two 16-byte halves h of a float32 octet (h = 0 only for binary16), which
-// keeps every warp's shared-memory reads conflict-free.
-constexpr int kNormStages = 5;
 
 // The elements of octet `local` of the cursor's tensor one by one (zeros past its end).
 template <Dtype G>
@@ -472,72 +459,80 @@ __device__ __noinline__ double sumsq_chunk_double(const ChunkTable& ct, int32_t 
     return t;
 }
 
-// The joint norm. CTA b streams its equal, contiguous chunk of the list's octets (crossing tensor boundaries),
-// each thread keeping one running sum over the whole chunk; one block reduction gives the CTA's partial; the CTA
-// that finishes last sums every partial in a fixed order and writes norm and factor.
+// Gradient octet `o` of the list (zeros past the chunk's end or the tensor's end): one 32-byte load (16 for
+// binary16) when the octet is whole and its tensor aligned, else element by element. Normal L2 priority, so the
+// part of the gradient read last may still be in L2 when the AdamW kernel, which walks backwards, reads it again.
 template <Dtype G>
+__device__ __forceinline__ void load_grad_octet(const ChunkTable& ct, Cursor& c, int64_t o, int64_t c1,
+                                                float (&x)[8]) {
+    if (o >= c1) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[j] = 0.0f;
+        return;
+    }
+    c.advance(ct, o);
+    const int64_t local = o - c.lo;
+    if (c.vec && local < c.full) {
+        if constexpr (G == kF16) {
+            uint4 h;
+            asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(h.x), "=r"(h.y), "=r"(h.z), "=r"(h.w)
+                         : "l"(c.base + local * 16));
+            h8_to(h, x);
+        } else {
+            asm volatile("ld.global.L1::no_allocate.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                         : "=f"(x[0]), "=f"(x[1]), "=f"(x[2]), "=f"(x[3]), "=f"(x[4]), "=f"(x[5]), "=f"(x[6]),
+                           "=f"(x[7])
+                         : "l"(c.base + local * 32));
+        }
+    } else {  // a tensor's partial last octet, or an unaligned tensor
+        load_elements<G>(c, local, x);
+    }
+}
+
+// The joint norm. CTA b streams its equal, contiguous chunk of the list's octets (crossing tensor boundaries):
+// thread t takes octets c0 + t, c0 + t + 256, ..., two at a time, the next two always loading while the current
+// two are summed; each thread keeps one running sum over its whole share, one block reduction gives the CTA's
+// partial, and the CTA that finishes last sums every partial in a fixed order and writes norm and factor.
+template <Dtype G, bool kScaled>
 __global__ void __launch_bounds__(kThreads, kNormCtasPerSm) norm_kernel(ChunkTable ct, float inv_scale,
                                                                         double* __restrict__ partials,
                                                                         unsigned int* ticket, float max_norm,
                                                                         float* d_norm, float* d_factor) {
-    constexpr int S = kNormStages;
-    constexpr int kOctBytes = (G == kF16) ? 16 : 32;
     __shared__ double red[kWarps];
     __shared__ int last;
-    __shared__ float4 ring[2 * S * kThreads];
     allow_dependents();
-    const bool scaled = inv_scale != 1.0f;
     const int t = threadIdx.x;
     const int64_t c0 = ct.total_octs * blockIdx.x / ct.grid;
     const int64_t c1 = ct.total_octs * (blockIdx.x + 1) / ct.grid;
     const int32_t k0 = ct.first[blockIdx.x];
 
-    SumSq acc{{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}, 0.f};
-    Cursor ci, cc;  // the issuing side runs S - 1 octets ahead of the consuming side
-    ci.init(ct, k0);
-    cc.init(ct, k0);
-    int64_t o_issue = c0 + t;
-    auto issue = [&](int slot) {
-        if (o_issue < c1) {
-            ci.advance(ct, o_issue);
-            const int64_t local = o_issue - ci.lo;
-            if (ci.vec && local < ci.n / kOct) {
-                const char* src = ci.base + local * kOctBytes;
-                cp_async16(&ring[(2 * slot) * kThreads + t], src);
-                if constexpr (G != kF16) cp_async16(&ring[(2 * slot + 1) * kThreads + t], src + 16);
-            }
-        }
-        cp_async_commit();  // one group per octet, empty where nothing was copied, so the count stays in step
-        o_issue += kThreads;
+    SumSq acc{{0.f, 0.f}, {0.f, 0.f}, 0.f};
+    Cursor cur;
+    cur.init(ct, k0);
+    auto sum2 = [&](const float (&a)[8], const float (&b)[8]) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc.add(kScaled ? __fmul_rn(a[j], inv_scale) : a[j], j & 1);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc.add(kScaled ? __fmul_rn(b[j], inv_scale) : b[j], j & 1);
     };
-#pragma unroll
-    for (int s = 0; s < S - 1; ++s) issue(s);
-    int slot = 0;
-    for (int64_t o = c0 + t; o < c1; o += kThreads) {
-        cp_async_wait<S - 2>();  // this octet's group has landed
-        cc.advance(ct, o);
-        const int64_t local = o - cc.lo;
-        float x[8];
-        if (cc.vec && local < cc.n / kOct) {
-            const float4 a = ring[(2 * slot) * kThreads + t];
-            if constexpr (G == kF16) {
-                h8_to(*reinterpret_cast<const uint4*>(&a), x);
-            } else {
-                const float4 b = ring[(2 * slot + 1) * kThreads + t];
-                x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-                x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-            }
-        } else {  // a tensor's partial last octet, or an unaligned tensor
-            load_elements<G>(cc, local, x);
-        }
-        issue(slot == 0 ? S - 1 : slot - 1);  // refill the slot emptied one octet ago
-        slot = (slot + 1 == S) ? 0 : slot + 1;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc.add(scaled ? __fmul_rn(x[j], inv_scale) : x[j], j & 3);
+    float A0[8], A1[8], B0[8], B1[8];
+    int64_t o = c0 + t;
+    load_grad_octet<G>(ct, cur, o, c1, A0);
+    load_grad_octet<G>(ct, cur, o + kThreads, c1, A1);
+    while (o < c1) {
+        const int64_t ob = o + 2 * kThreads;
+        load_grad_octet<G>(ct, cur, ob, c1, B0);
+        load_grad_octet<G>(ct, cur, ob + kThreads, c1, B1);
+        sum2(A0, A1);
+        if (ob >= c1) break;
+        o = ob + 2 * kThreads;
+        load_grad_octet<G>(ct, cur, o, c1, A0);
+        load_grad_octet<G>(ct, cur, o + kThreads, c1, A1);
+        sum2(B0, B1);
     }
-    cp_async_wait_all();
     double mine = acc.total();
-    if (!acc.exact(mine)) mine = sumsq_chunk_double<G>(ct, k0, c0, c1, scaled ? inv_scale : 1.0f);
+    if (!acc.exact(mine)) mine = sumsq_chunk_double<G>(ct, k0, c0, c1, kScaled ? inv_scale : 1.0f);
 
     const double part = block_sum(mine, red);
     if (t == 0) {
@@ -675,10 +670,15 @@ int launch_norm(const ChunkTable& ct, Dtype gdt, float inv_scale, double* partia
                 float max_norm, float* d_norm, float* d_factor, void* stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const dim3 grid(ct.grid > 0 ? ct.grid : 1), block(kThreads);
-    if (gdt == kF16)
-        norm_kernel<kF16><<<grid, block, 0, st>>>(ct, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
+    const bool scaled = inv_scale != 1.0f;  // an unscaled list skips the multiply (x * 1 is x)
+    if (gdt == kF16 && scaled)
+        norm_kernel<kF16, true><<<grid, block, 0, st>>>(ct, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
+    else if (gdt == kF16)
+        norm_kernel<kF16, false><<<grid, block, 0, st>>>(ct, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
+    else if (scaled)
+        norm_kernel<kF32, true><<<grid, block, 0, st>>>(ct, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
     else
-        norm_kernel<kF32><<<grid, block, 0, st>>>(ct, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
+        norm_kernel<kF32, false><<<grid, block, 0, st>>>(ct, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
     count_launches(1);
     return (int)cudaGetLastError();
 }
