@@ -246,27 +246,39 @@ def measure(wl: workloads.Workload, steps: int, warmup: int, zero_grad: bool, di
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    # the timed region: K steps back to back, events only at its two ends
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches0 = mica.mica_launch_count()
     t_wall0 = time.time()
+    start.record(stream)
     for i in range(steps):
-        ev[i][0].record(stream)
-        step(warmup + 1 + i, ev[i][1])
-        ev[i][2].record(stream)
+        step(warmup + 1 + i)
+    end.record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.time()
     launches = mica.mica_launch_count() - launches0
-    total_ms = ev[0][0].elapsed_time(ev[-1][2])
+    total_ms = start.elapsed_time(end)
+    if dist is not None:
+        dist.barrier()
+        tt = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    # each kernel's own duration, from events around each launch (a separate loop: events between the two
+    # launches of a step keep them from overlapping)
+    k2 = min(steps, 50)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(k2)]
+    for i in range(k2):
+        ev[i][0].record(stream)
+        step(warmup + steps + 1 + i, ev[i][1])
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
     adamw_ms = [e[1].elapsed_time(e[2]) for e in ev]
     clip_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    if dist is not None:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
     out = {"total_ms": total_ms, "ms_per_step": total_ms / steps, "adamw_ms": statistics.mean(adamw_ms),
            "clip_ms": statistics.mean(clip_ms), "launches": launches, "t_wall": (t_wall0, t_wall1),
            "norm": float(norm.item())}
+    mica.mica_sync()
     del st
     return out, (W, G, M, V, norm, factor, kw)
 

@@ -58,11 +58,23 @@ static bool sync_debug() {
     return on;
 }
 
+// After a stream has drained: a kernel whose bounded pipeline wait gave up leaves a nonzero device status word.
+static mica_status check_device_status(const char* what) {
+    unsigned int st = 0;
+    const int e = read_device_status(&st);
+    if (e != (int)cudaSuccess) return cuda_fail((cudaError_t)e, what);
+    if (st) return fail(MICA_ERR_CUDA, "%s: a kernel's wait on its shared-memory pipeline gave up (status 0x%x); "
+                        "its results are not valid", what, st);
+    return MICA_OK;
+}
+
 static mica_status after_launch(int err, void* stream, const char* what) {
     if (err != (int)cudaSuccess) return cuda_fail((cudaError_t)err, what);
     if (sync_debug()) {
         const cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return cuda_fail(e, what);
+        const mica_status s = check_device_status(what);
+        if (s != MICA_OK) return s;
     }
     return ok();
 }
@@ -325,13 +337,17 @@ static mica_status build_plan(const ListDesc& L, int device, std::vector<uint64_
     std::vector<WorkItem> items;
     std::vector<int64_t> prefix;
     std::vector<int32_t> first;
-    if (L.kind == kNorm) {
-        // contiguous equal chunks, four CTAs per SM (at least one octet per thread)
+    int64_t nonempty = 0;
+    for (int32_t k = 0; k < L.T; ++k) nonempty += L.n[k] > 0;
+    const bool chunked = L.kind == kNorm;
+    if (chunked) {
+        // contiguous equal chunks (see choose_norm_shape)
         prefix.resize((size_t)L.T + 1);
         prefix[0] = 0;
         for (int32_t k = 0; k < L.T; ++k) prefix[k + 1] = prefix[k] + (L.n[k] + kOct - 1) / kOct;
-        const int64_t want = std::max<int64_t>(1, (total_octs + kThreads - 1) / kThreads);
-        const int32_t grid = (int32_t)std::min<int64_t>((int64_t)kNormCtasPerSm * sms, want);
+        int32_t grid = 1, direct = 0;
+        choose_norm_shape(total_octs, nonempty, sms, INT32_MAX, &grid, &direct);
+        plan->chunks.direct = direct;
         first.resize((size_t)grid);
         for (int32_t b = 0; b < grid; ++b) {
             const int64_t c0 = total_octs * b / grid;
@@ -358,7 +374,7 @@ static mica_status build_plan(const ListDesc& L, int device, std::vector<uint64_
     const size_t first_off = up(prefix_off + prefix_b);
     const size_t first_b = first.size() * sizeof(int32_t);
     const size_t part_off = up(first_off + first_b);
-    const size_t part_b = first.size() * sizeof(double);
+    const size_t part_b = (L.kind == kNorm) ? first.size() * sizeof(double) : 0;
     const size_t ticket_off = up(part_off + part_b);
     const size_t total = ticket_off + ((L.kind == kNorm) ? 256 : 0);
     cudaError_t e = cudaMalloc(&plan->dev, std::max<size_t>(total, 256));
@@ -371,10 +387,12 @@ static mica_status build_plan(const ListDesc& L, int device, std::vector<uint64_
     char* base = static_cast<char*>(plan->dev);
     plan->recs = reinterpret_cast<TensorRec*>(base);
     plan->items = reinterpret_cast<WorkItem*>(base + item_off);
-    if (L.kind == kNorm) {
+    if (chunked) {
         plan->chunks.recs = plan->recs;
         plan->chunks.prefix = reinterpret_cast<const int64_t*>(base + prefix_off);
         plan->chunks.first = reinterpret_cast<const int32_t*>(base + first_off);
+    }
+    if (L.kind == kNorm) {
         plan->partials = reinterpret_cast<double*>(base + part_off);
         plan->ticket = reinterpret_cast<unsigned int*>(base + ticket_off);
     }
@@ -580,6 +598,8 @@ extern "C" mica_status mica_adamw_steps(float* const* w, void* const* g, void* c
 extern "C" mica_status mica_sync(void* stream) {
     const cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "mica_sync");
+    const mica_status s = check_device_status("mica_sync");
+    if (s != MICA_OK) return s;
     return ok();
 }
 

@@ -225,15 +225,38 @@ __device__ __noinline__ void adam_oct_elements(const TensorRec& r, int64_t o, co
     }
 }
 
-// Octets [ob, oe) of one tensor: octet ob + lane first, then every `stride`-th.
+// Asks L2 to fetch `bytes` (a multiple of 16) from `p` (16-byte aligned), without waiting for them.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// The four streams of octets [a, b) of tensor r into L2 (a < b, whole octets of an aligned tensor).
+template <Dtype G, Dtype M>
+__device__ __forceinline__ void prefetch_octets(const TensorRec& r, int64_t a, int64_t b) {
+    constexpr int kGb = (G == kF16) ? 16 : 32, kMb = (M == kBF16x2) ? 16 : 32;
+    const uint32_t n = (uint32_t)(b - a);
+    prefetch_l2(reinterpret_cast<const char*>(r.w) + a * 32, n * 32);
+    prefetch_l2(static_cast<const char*>(r.g) + a * kGb, n * kGb);
+    prefetch_l2(static_cast<const char*>(r.m) + a * kMb, n * kMb);
+    prefetch_l2(static_cast<const char*>(r.v) + a * kMb, n * kMb);
+}
+
+// Octets [ob, oe) of one tensor: octet ob + lane first, then every `stride`-th. With `prefetch` (a whole CTA on
+// one slice: lane is the thread index and stride the CTA size) thread 0 asks L2 for the rounds one and two ahead,
+// so that the other threads' loads of those rounds find their data in L2 rather than waiting on DRAM.
 template <Dtype G, Dtype M>
 __device__ __forceinline__ void adam_range(const TensorRec& r, int64_t ob, int64_t oe, int lane, int stride,
-                                           const StepScalars& s, Factor& fac) {
+                                           const StepScalars& s, Factor& fac, bool prefetch = false) {
     constexpr int U = AdamUnroll<M>::value;
     const int64_t full = r.n / kOct;  // octets with all eight elements
     if (r.vec) {
         const int64_t vend = oe < full ? oe : full;
-        for (int64_t o0 = ob + lane; o0 < vend; o0 += (int64_t)stride * U) {
+        const int64_t round = (int64_t)stride * U;
+        if (prefetch && lane == 0 && ob + round < vend)
+            prefetch_octets<G, M>(r, ob + round, ob + 2 * round < vend ? ob + 2 * round : vend);
+        for (int64_t o0 = ob + lane; o0 < vend; o0 += round) {
+            if (prefetch && lane == 0 && o0 + 2 * round < vend)
+                prefetch_octets<G, M>(r, o0 + 2 * round, o0 + 3 * round < vend ? o0 + 3 * round : vend);
             float W[U][8], Gf[U][8], Mf[U][8], Vf[U][8];
             uint4 Gh[U], Mp[U], Vp[U];
 #pragma unroll
@@ -305,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 3) adamw_kernel(const TensorRec* __r
             const TensorRec r = recs[item.t];
             const int64_t no = (r.n + kOct - 1) / kOct;
             const int64_t oe = item.o0 + item_octs < no ? item.o0 + item_octs : no;
-            adam_range<G, M>(r, item.o0, oe, threadIdx.x, kThreads, s, fac);
+            adam_range<G, M>(r, item.o0, oe, threadIdx.x, kThreads, s, fac, true);
         } else {
             for (int j = warp; j < item.count; j += kWarps) {
                 const TensorRec r = recs[item.t + j];
@@ -321,29 +344,38 @@ __global__ void __launch_bounds__(kThreads, 3) adamw_kernel(const TensorRec* __r
 
 // x^2 summed to about twice float32's precision: each square is split exactly into p + e (p = x*x rounded, e its
 // rounding error from an FMA) and p is added to the running hi by Knuth's two-sum, whose exact error joins e in lo.
-// Two independent (hi, lo) chains keep consecutive squares from waiting on one another. This is exact up to the
-// float32 rounding of lo while every |x| lies in [2^-50, 2^50): squares then stay below 2^100 (no overflow) and
-// every e is a normal float32. Elements below 2^-50 in a range whose largest |x| is at least 2^-50 lose at most
-// 2^-150 each, a relative 2^-44 of that range's sum; any other range (a value at or above 2^50, an infinity or
-// NaN, or nothing but values below 2^-50) is summed again in double by the caller.
+// The two halves of a float2 are two independent (hi, lo) chains (even and odd elements), advanced together by
+// sm_100's packed float32x2 instructions, each half rounded exactly as the scalar operation would be. This is exact
+// up to the float32 rounding of lo while every |x| lies in [2^-50, 2^50): squares then stay below 2^100 (no
+// overflow) and every e is a normal float32. Elements below 2^-50 in a share whose largest |x| is at least 2^-50
+// lose at most 2^-150 each, a relative 2^-44 of that share's sum; any other share (a value at or above 2^50, an
+// infinity or NaN, or nothing but values below 2^-50) is summed again in double by the caller.
+__device__ __forceinline__ float2 neg2(float2 v) { return make_float2(-v.x, -v.y); }
+
 struct SumSq {
-    float hi[2], lo[2];
+    float2 hi, lo;
     float mx;  // the largest |x| seen (NaNs are ignored here and show up in hi instead)
-    __device__ __forceinline__ void add(float x, int c) {
-        mx = fmaxf(mx, fabsf(x));
-        const float p = __fmul_rn(x, x);
-        const float e = __fmaf_rn(x, x, -p);
-        const float s = __fadd_rn(hi[c], p);
-        const float bp = __fsub_rn(s, hi[c]);
-        const float err = __fadd_rn(__fsub_rn(hi[c], __fsub_rn(s, bp)), __fsub_rn(p, bp));
-        hi[c] = s;
-        lo[c] = __fadd_rn(lo[c], __fadd_rn(err, e));
+    __device__ __forceinline__ void add2(float2 x) {
+        mx = fmaxf(mx, fmaxf(fabsf(x.x), fabsf(x.y)));
+        const float2 p = __fmul2_rn(x, x);
+        const float2 e = __ffma2_rn(x, x, neg2(p));
+        const float2 s = __fadd2_rn(hi, p);
+        const float2 bp = __fadd2_rn(s, neg2(hi));
+        const float2 err = __fadd2_rn(__fadd2_rn(hi, neg2(__fadd2_rn(s, neg2(bp)))), __fadd2_rn(p, neg2(bp)));
+        hi = s;
+        lo = __fadd2_rn(lo, __fadd2_rn(err, e));
+    }
+    template <bool kScaled>
+    __device__ __forceinline__ void add8(const float (&x)[8], float inv_scale) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float2 v = make_float2(x[2 * j], x[2 * j + 1]);
+            if constexpr (kScaled) v = __fmul2_rn(v, make_float2(inv_scale, inv_scale));
+            add2(v);
+        }
     }
     __device__ __forceinline__ double total() const {
-        double t = 0.0;
-#pragma unroll
-        for (int c = 0; c < 2; ++c) t += (double)hi[c] + (double)lo[c];
-        return t;
+        return ((double)hi.x + (double)lo.x) + ((double)hi.y + (double)lo.y);
     }
     __device__ __forceinline__ bool exact(double t) const {
         return mx < 0x1p50f && !(mx < 0x1p-50f && mx > 0.0f) && t < 0x1p100;
@@ -490,12 +522,12 @@ __device__ __forceinline__ void load_grad_octet(const ChunkTable& ct, Cursor& c,
     }
 }
 
-// The joint norm. CTA b streams its equal, contiguous chunk of the list's octets (crossing tensor boundaries):
-// thread t takes octets c0 + t, c0 + t + 256, ..., two at a time, the next two always loading while the current
-// two are summed; each thread keeps one running sum over its whole share, one block reduction gives the CTA's
-// partial, and the CTA that finishes last sums every partial in a fixed order and writes norm and factor.
+// The joint norm for lists of many small tensors, where a stage of the TMA pipeline would cross several tensors:
+// CTA b streams its equal, contiguous chunk of the list's octets straight into registers. Thread t takes octets
+// c0 + t, c0 + t + 256, ..., two at a time, the next two always loading while the current two are summed, each
+// thread following the tensor boundaries with its own cursor; the rest is as in norm_tma_kernel.
 template <Dtype G, bool kScaled>
-__global__ void __launch_bounds__(kThreads, kNormCtasPerSm) norm_kernel(ChunkTable ct, float inv_scale,
+__global__ void __launch_bounds__(kThreads, kNormDirectCtasPerSm) norm_direct_kernel(ChunkTable ct, float inv_scale,
                                                                         double* __restrict__ partials,
                                                                         unsigned int* ticket, float max_norm,
                                                                         float* d_norm, float* d_factor) {
@@ -511,10 +543,8 @@ __global__ void __launch_bounds__(kThreads, kNormCtasPerSm) norm_kernel(ChunkTab
     Cursor cur;
     cur.init(ct, k0);
     auto sum2 = [&](const float (&a)[8], const float (&b)[8]) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc.add(kScaled ? __fmul_rn(a[j], inv_scale) : a[j], j & 1);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc.add(kScaled ? __fmul_rn(b[j], inv_scale) : b[j], j & 1);
+        acc.add8<kScaled>(a, inv_scale);
+        acc.add8<kScaled>(b, inv_scale);
     };
     float A0[8], A1[8], B0[8], B1[8];
     int64_t o = c0 + t;
@@ -533,6 +563,204 @@ __global__ void __launch_bounds__(kThreads, kNormCtasPerSm) norm_kernel(ChunkTab
     }
     double mine = acc.total();
     if (!acc.exact(mine)) mine = sumsq_chunk_double<G>(ct, k0, c0, c1, kScaled ? inv_scale : 1.0f);
+
+    const double part = block_sum(mine, red);
+    if (t == 0) {
+        partials[blockIdx.x] = part;
+        __threadfence();  // the partial is visible before the ticket says so
+        last = (atomicAdd(ticket, 1u) == (unsigned int)(ct.grid - 1));
+    }
+    __syncthreads();
+    if (last) {  // every other CTA's partial is written: sum them all, in order
+        __threadfence();
+        finalize_norm(partials, ct.grid, max_norm, inv_scale, d_norm, d_factor, red);
+        if (t == 0) *ticket = 0u;  // ready for the next launch on this list
+    }
+}
+
+// ------------------------------------------------------------------------------------------------------------------
+// TMA bulk copies and mbarriers
+// ------------------------------------------------------------------------------------------------------------------
+
+// Set (OR-ed) by a kernel whose pipeline wait gave up; read and cleared by the host (read_device_status).
+__device__ unsigned int g_mica_status;
+
+constexpr uint32_t kMaxPolls = 1u << 22;  // try_wait rounds before a wait gives up (each round may suspend a while)
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// Waits until the barrier's phase of parity `parity` has completed; false if it has not after kMaxPolls rounds.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    const uint32_t addr = smem_u32(bar);
+    for (uint32_t i = 0; i < kMaxPolls; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(addr), "r"(parity)
+            : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+// `bytes` (a multiple of 16) from global to shared memory, both 16-byte aligned, completing on `bar`.
+__device__ __forceinline__ void bulk_copy_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(smem_dst)),
+                 "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// ------------------------------------------------------------------------------------------------------------------
+// the joint norm: a TMA pipeline over equal contiguous chunks
+// ------------------------------------------------------------------------------------------------------------------
+
+// Each CTA streams its chunk of the list's octets through kNormStages shared-memory stages of 256 octets. One
+// producer warp (its lane 0) walks the chunk and, per stage, issues one bulk copy per run of whole octets of an
+// aligned tensor (a stage may cross tensor boundaries), completing on the stage's `full` barrier; the 8 consumer
+// warps wait on it, thread t takes the stage's octet t (from shared memory, or element by element from global
+// memory for a tensor's partial last octet or an unaligned tensor), then each warp arrives on the stage's `empty`
+// barrier so the producer may refill it. The bytes in flight (up to 8 stages x 8 KB per CTA, 3 CTAs per SM) cost
+// shared memory, not registers.
+constexpr int kNormStages = 8;
+constexpr int kNormThreads = kThreads + 32;
+
+template <Dtype G>
+__host__ __device__ constexpr int norm_stage_bytes() { return kThreads * ((G == kF16) ? 16 : 32); }
+
+template <Dtype G>
+size_t norm_smem_bytes() { return (size_t)kNormStages * norm_stage_bytes<G>(); }
+
+enum : unsigned int { kStatusNormProducer = 1u, kStatusNormConsumer = 2u };
+
+template <Dtype G, bool kScaled>
+__global__ void __launch_bounds__(kNormThreads, kNormTmaCtasPerSm) norm_tma_kernel(ChunkTable ct, float inv_scale,
+                                                                            double* __restrict__ partials,
+                                                                            unsigned int* ticket, float max_norm,
+                                                                            float* d_norm, float* d_factor) {
+    constexpr int S = kNormStages;
+    constexpr int kOctBytes = (G == kF16) ? 16 : 32;
+    constexpr int kStageBytes = norm_stage_bytes<G>();
+    extern __shared__ __align__(128) unsigned char stages[];
+    __shared__ __align__(8) uint64_t full[S];
+    __shared__ __align__(8) uint64_t empty[S];
+    __shared__ double red[kWarps + 1];
+    __shared__ int last;
+    allow_dependents();
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int64_t c0 = ct.total_octs * blockIdx.x / ct.grid;
+    const int64_t c1 = ct.total_octs * (blockIdx.x + 1) / ct.grid;
+    const int32_t k0 = ct.first[blockIdx.x];
+    const int64_t nstage = (c1 - c0 + kThreads - 1) / kThreads;
+    if (t == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);          // the producer's arrive (with the stage's byte count)
+            mbar_init(&empty[s], kWarps);    // one arrive per consumer warp
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    double mine = 0.0;
+    if (warp == kWarps) {
+        // ---- producer ----
+        if (lane == 0) {
+            Cursor pc;
+            pc.init(ct, k0);
+            bool ok = true;
+            int64_t i = 0;
+            for (; i < nstage; ++i) {
+                const int slot = (int)(i % S);
+                if (i >= S && !mbar_wait(&empty[slot], (uint32_t)((i / S - 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                const int64_t a = c0 + i * kThreads;
+                const int64_t b = a + kThreads < c1 ? a + kThreads : c1;
+                unsigned char* stage = stages + (size_t)slot * kStageBytes;
+                // the runs of whole octets of aligned tensors in [a, b): counted first, then copied
+                for (int pass = 0; pass < 2; ++pass) {
+                    Cursor c = pc;
+                    uint32_t bytes = 0;
+                    for (int64_t o = a; o < b;) {
+                        c.advance(ct, o);
+                        const int64_t seg_end = b < c.hi ? b : c.hi;
+                        const int64_t whole_end = c.lo + c.full < seg_end ? c.lo + c.full : seg_end;
+                        if (c.vec && whole_end > o) {
+                            const uint32_t nb = (uint32_t)(whole_end - o) * kOctBytes;
+                            if (pass == 1)
+                                bulk_copy_g2s(stage + (o - a) * kOctBytes, c.base + (o - c.lo) * kOctBytes, nb,
+                                              &full[slot]);
+                            bytes += nb;
+                        }
+                        o = seg_end;
+                    }
+                    if (pass == 0) {
+                        mbar_arrive_expect_tx(&full[slot], bytes);
+                    } else {
+                        pc = c;
+                    }
+                }
+            }
+            // every copy this CTA issued has landed before it may exit: wait for each slot's last use
+            const int64_t from = i > S ? i - S : 0;
+            for (int64_t j = from; j < i; ++j) mbar_wait(&full[j % S], (uint32_t)((j / S) & 1));
+            if (!ok) atomicOr(&g_mica_status, kStatusNormProducer);
+        }
+    } else {
+        // ---- consumers ----
+        SumSq acc{{0.f, 0.f}, {0.f, 0.f}, 0.f};
+        Cursor cc;
+        cc.init(ct, k0);
+        bool ok = true;
+        for (int64_t i = 0; i < nstage; ++i) {
+            const int slot = (int)(i % S);
+            if (!mbar_wait(&full[slot], (uint32_t)((i / S) & 1))) {
+                ok = false;
+                break;
+            }
+            const int64_t o = c0 + i * kThreads + t;
+            float x[8];
+            if (o < c1) {
+                cc.advance(ct, o);
+                const int64_t local = o - cc.lo;
+                if (cc.vec && local < cc.full) {
+                    const unsigned char* src = stages + (size_t)slot * kStageBytes + (size_t)t * kOctBytes;
+                    const float4 p0 = *reinterpret_cast<const float4*>(src);
+                    if constexpr (G == kF16) {
+                        h8_to(*reinterpret_cast<const uint4*>(&p0), x);
+                    } else {
+                        const float4 p1 = *reinterpret_cast<const float4*>(src + 16);
+                        x[0] = p0.x; x[1] = p0.y; x[2] = p0.z; x[3] = p0.w;
+                        x[4] = p1.x; x[5] = p1.y; x[6] = p1.z; x[7] = p1.w;
+                    }
+                } else {  // a tensor's partial last octet, or an unaligned tensor
+                    load_elements<G>(cc, local, x);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) x[j] = 0.0f;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);  // this warp is done reading the stage
+            acc.add8<kScaled>(x, inv_scale);
+        }
+        mine = acc.total();
+        if (!acc.exact(mine)) mine = sumsq_chunk_double<G>(ct, k0, c0, c1, kScaled ? inv_scale : 1.0f);
+        if (!ok) atomicOr(&g_mica_status, kStatusNormConsumer);
+    }
 
     const double part = block_sum(mine, red);
     if (t == 0) {
@@ -627,10 +855,10 @@ __global__ void __launch_bounds__(kThreads) scale_kernel(const TensorRec* __rest
 }
 
 template <Dtype G, Dtype M>
-cudaError_t launch_adamw_t(dim3 grid, cudaStream_t st, const TensorRec* recs, const WorkItem* items,
-                           int32_t num_items, int32_t item_octs, const StepScalars& s, const float* d_factor) {
+cudaError_t launch_adamw_t(const WorkItem* items, const TensorRec* recs, int32_t num_items, int32_t item_octs,
+                           cudaStream_t st, const StepScalars& s, const float* d_factor) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
+    cfg.gridDim = dim3(num_items);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
@@ -652,35 +880,64 @@ int launch_adamw(const TensorRec* recs, const WorkItem* items, int32_t num_items
                  Dtype mdt, const StepScalars& s, const float* d_factor, void* stream) {
     if (num_items <= 0) return (int)cudaSuccess;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const dim3 grid(num_items);
     cudaError_t e;
     if (gdt == kF32 && mdt == kF32)
-        e = launch_adamw_t<kF32, kF32>(grid, st, recs, items, num_items, item_octs, s, d_factor);
+        e = launch_adamw_t<kF32, kF32>(items, recs, num_items, item_octs, st, s, d_factor);
     else if (gdt == kF32 && mdt == kBF16x2)
-        e = launch_adamw_t<kF32, kBF16x2>(grid, st, recs, items, num_items, item_octs, s, d_factor);
+        e = launch_adamw_t<kF32, kBF16x2>(items, recs, num_items, item_octs, st, s, d_factor);
     else if (gdt == kF16 && mdt == kF32)
-        e = launch_adamw_t<kF16, kF32>(grid, st, recs, items, num_items, item_octs, s, d_factor);
+        e = launch_adamw_t<kF16, kF32>(items, recs, num_items, item_octs, st, s, d_factor);
     else
-        e = launch_adamw_t<kF16, kBF16x2>(grid, st, recs, items, num_items, item_octs, s, d_factor);
+        e = launch_adamw_t<kF16, kBF16x2>(items, recs, num_items, item_octs, st, s, d_factor);
     count_launches(1);
     return (int)(e != cudaSuccess ? e : cudaGetLastError());
+}
+
+template <Dtype G, bool kScaled>
+cudaError_t launch_norm_t(const ChunkTable& ct, cudaStream_t st, float inv_scale, double* partials,
+                          unsigned int* ticket, float max_norm, float* d_norm, float* d_factor) {
+    const dim3 grid(ct.grid > 0 ? ct.grid : 1);
+    if (ct.direct) {
+        norm_direct_kernel<G, kScaled><<<grid, dim3(kThreads), 0, st>>>(ct, inv_scale, partials, ticket, max_norm,
+                                                                         d_norm, d_factor);
+        return cudaGetLastError();
+    }
+    const size_t smem = norm_smem_bytes<G>();
+    cudaError_t e = cudaFuncSetAttribute(norm_tma_kernel<G, kScaled>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    norm_tma_kernel<G, kScaled><<<grid, dim3(kNormThreads), smem, st>>>(ct, inv_scale, partials, ticket, max_norm,
+                                                                        d_norm, d_factor);
+    return cudaGetLastError();
 }
 
 int launch_norm(const ChunkTable& ct, Dtype gdt, float inv_scale, double* partials, unsigned int* ticket,
                 float max_norm, float* d_norm, float* d_factor, void* stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const dim3 grid(ct.grid > 0 ? ct.grid : 1), block(kThreads);
     const bool scaled = inv_scale != 1.0f;  // an unscaled list skips the multiply (x * 1 is x)
+    cudaError_t e;
     if (gdt == kF16 && scaled)
-        norm_kernel<kF16, true><<<grid, block, 0, st>>>(ct, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
+        e = launch_norm_t<kF16, true>(ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
     else if (gdt == kF16)
-        norm_kernel<kF16, false><<<grid, block, 0, st>>>(ct, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
+        e = launch_norm_t<kF16, false>(ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
     else if (scaled)
-        norm_kernel<kF32, true><<<grid, block, 0, st>>>(ct, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
+        e = launch_norm_t<kF32, true>(ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
     else
-        norm_kernel<kF32, false><<<grid, block, 0, st>>>(ct, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
+        e = launch_norm_t<kF32, false>(ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
     count_launches(1);
-    return (int)cudaGetLastError();
+    return (int)e;
+}
+
+int read_device_status(unsigned int* status) {
+    unsigned int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_mica_status, sizeof v);
+    if (e != cudaSuccess) return (int)e;
+    if (v) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_mica_status, &zero, sizeof zero);
+    }
+    *status = v;
+    return (int)e;
 }
 
 int launch_scale(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_octs, Dtype dt,

@@ -114,8 +114,8 @@ extern "C" mica_status mica_clip_grad_norms_noalloc(const void* const* g, const 
     mica_status s = scratch_address(dev, &scratch);
     if (s != MICA_OK) return s;
 
-    // The chunk layout the allocating entry point uses: the octet prefix of the list, equal contiguous chunks,
-    // four CTAs per SM (capped by this scratch), each chunk's first tensor.
+    // The chunk layout the allocating entry point uses: the octet prefix of the list, equal contiguous chunks (as
+    // many as the allocating entry point's, capped by this scratch), each chunk's first tensor.
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
         cudaGetLastError();
@@ -131,11 +131,11 @@ extern "C" mica_status mica_clip_grad_norms_noalloc(const void* const* g, const 
         recs[k].vec = (reinterpret_cast<uintptr_t>(gp) % (gdt == MICA_F16 ? 16 : 32)) == 0;
         prefix[k + 1] = prefix[k] + (n[k] + kOct - 1) / kOct;
     }
-    const int64_t want = total_octs > kThreads ? (total_octs + kThreads - 1) / kThreads : 1;
-    int64_t grid = (int64_t)kNormCtasPerSm * sms;
-    if (grid > kNoallocMaxGrid) grid = kNoallocMaxGrid;
-    if (grid > want) grid = want;
-    for (int64_t b = 0; b < grid; ++b) {
+    int64_t nonempty = 0;
+    for (int32_t k = 0; k < T; ++k) nonempty += n[k] > 0;
+    int32_t grid = 1, direct = 0;
+    choose_norm_shape(total_octs, nonempty, sms, kNoallocMaxGrid, &grid, &direct);
+    for (int32_t b = 0; b < grid; ++b) {
         const int64_t c0 = total_octs * b / grid;
         int32_t lo = 0, hi = T;  // the last tensor whose octets start at or before c0
         while (hi - lo > 1) {
@@ -153,8 +153,9 @@ extern "C" mica_status mica_clip_grad_norms_noalloc(const void* const* g, const 
     ct.prefix = reinterpret_cast<const int64_t*>(scratch + kRecBytes);
     ct.first = reinterpret_cast<const int32_t*>(scratch + kRecBytes + kPrefixBytes);
     ct.T = T;
-    ct.grid = (int32_t)grid;
+    ct.grid = grid;
     ct.total_octs = total_octs;
+    ct.direct = direct;
     double* d_part = reinterpret_cast<double*>(scratch + kTableBytes);
     unsigned int* d_ticket = reinterpret_cast<unsigned int*>(scratch + kTableBytes + kPartialBytes);
     cudaError_t e = cudaSuccess;

@@ -21,7 +21,6 @@ namespace mica {
 constexpr int kThreads = 256;  // threads per CTA of every streaming kernel
 constexpr int kWarps = kThreads / 32;
 constexpr int kOct = 8;        // elements per vector unit
-constexpr int kNormCtasPerSm = 4;  // resident CTAs per SM of the norm kernel (its grid is this times the SM count)
 
 struct TensorRec {
     float* w;      // weights (AdamW) / the tensor itself (scale) / unused (norm)
@@ -52,7 +51,24 @@ struct ChunkTable {
     int32_t T;
     int32_t grid;
     int64_t total_octs;
+    int32_t direct;         // 1: the register-streaming kernel (many small tensors); 0: the TMA pipeline
+    int32_t pad;
 };
+
+// The norm's launch shape. Lists whose tensors average under 512 octets (4,096 elements) are streamed straight into
+// registers, 4 CTAs of 256 threads per SM; others go through the TMA pipeline, 3 CTAs of 288 threads per SM. Either
+// way the grid is that many CTAs per SM, but no more than one per 256 octets (and at least one).
+constexpr int kNormDirectCtasPerSm = 4;
+constexpr int kNormTmaCtasPerSm = 3;
+inline void choose_norm_shape(int64_t total_octs, int64_t nonempty_tensors, int sms, int32_t max_grid,
+                              int32_t* grid, int32_t* direct) {
+    *direct = (nonempty_tensors > 0 && total_octs < 512 * nonempty_tensors) ? 1 : 0;
+    int64_t g = (int64_t)(*direct ? kNormDirectCtasPerSm : kNormTmaCtasPerSm) * sms;
+    const int64_t want = total_octs > 256 ? (total_octs + 255) / 256 : 1;
+    if (g > want) g = want;
+    if (g > max_grid) g = max_grid;
+    *grid = (int32_t)(g > 0 ? g : 1);
+}
 
 // The step's float32 scalars, each computed in double on the host and rounded once.
 struct StepScalars {
@@ -69,8 +85,9 @@ struct StepScalars {
 enum Dtype : int32_t { kF32 = 0, kF16 = 1, kBF16x2 = 2 };
 
 // Kernel launchers (kernels.cu). Each returns the cudaError_t of its launch as an int.
-// AdamW over every item. It is launched as a programmatic dependent of the kernel queued before it: it may start
-// and load its tensors while that kernel finishes, and reads d_factor only once that kernel has completed.
+// AdamW over every item, one CTA per item. It is launched as a programmatic dependent of the kernel queued before
+// it: it may start and load its tensors while that kernel finishes, and reads d_factor only once that kernel has
+// completed.
 int launch_adamw(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_octs, Dtype gdt,
                  Dtype mdt, const StepScalars& s, const float* d_factor, void* stream);
 // The joint norm in one launch of ct.grid CTAs: one partial square sum per CTA into `partials` (ct.grid doubles),
@@ -80,6 +97,10 @@ int launch_norm(const ChunkTable& ct, Dtype gdt, float inv_scale, double* partia
                 float max_norm, float* d_norm, float* d_factor, void* stream);
 int launch_scale(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_octs, Dtype dt,
                  float factor, const float* d_factor, void* stream);
+
+// The device's pipeline status word: nonzero when a kernel's bounded wait on a shared-memory barrier gave up (the
+// kernel then stopped early and its results are not valid). Reads it (synchronously) and clears it.
+int read_device_status(unsigned int* status);
 
 // kernels queued so far (incremented by the launchers)
 void count_launches(uint64_t k);

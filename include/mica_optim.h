@@ -153,7 +153,10 @@ MICA_API mica_status mica_clip_grad_norms_noalloc(const void* const* g, const in
                                                   float max_norm, float inv_scale, float* d_norm, float* d_factor,
                                                   void* stream);
 
-/* Waits for `stream` and reports a fault of any work queued on it (MICA_OK or MICA_ERR_CUDA). */
+/* Waits for `stream` and reports a fault of any work queued on it (MICA_OK or MICA_ERR_CUDA). It also reads and clears
+ * the device's pipeline status word: every wait of a kernel on its shared-memory barriers is bounded, and a wait
+ * that gives up (which only a broken memory system could cause) stops that kernel early and is reported here as
+ * MICA_ERR_CUDA, with its results not valid. */
 MICA_API mica_status mica_sync(void* stream);
 
 /* Waits for the current device, then frees every cached per-list device table. Returns MICA_OK or MICA_ERR_CUDA. */

@@ -141,4 +141,5 @@ def run_parity(wl: workloads.Workload, sizes=None, steps: int | None = None, zer
         norms.append((float(g_norm), float(o_norm), float(g_factor), float(o_factor)))
         if check_every_step or t == steps:
             compare_state(st, host, bool(same), f"{wl.name} step {t}")
+    mica.mica_sync()  # raises if a kernel's bounded pipeline wait gave up
     return {"norms": norms, "same_factor_every_step": same_all, "state": st}
