@@ -284,41 +284,58 @@ def measure(wl: workloads.Workload, steps: int, warmup: int, zero_grad: bool, di
 
 
 def measure_e2e(wl: workloads.Workload, steps: int, warmup: int):
-    """The same step through the public API with the step's gradient arriving from pinned host memory and the norm
-    read back to the host, both inside the timed region."""
+    """The same step through the public API, fed from the host: every step copies its whole gradient from pinned host
+    memory into one of two device gradient buffers (on a copy stream, so that step t+1's copy overlaps step t's
+    kernels, as a training loop's input pipeline would) and reads the step's norm back into pinned host memory.
+    Both copies of every step are inside the timed region. Returns (ms per step, H2D bytes, D2H bytes)."""
     import clip_tensor_adamw_gb300 as mica
     st = workloads.make_state(wl, "cuda")
     workloads.fill_grad(st, 1)
     g_host = torch.empty(st.g_flat.shape, dtype=st.g_flat.dtype, pin_memory=True)
     g_host.copy_(st.g_flat)
-    norm_host = torch.empty(1, dtype=torch.float32, pin_memory=True)
+    g_flat = [st.g_flat, torch.empty_like(st.g_flat)]
+    g_lists = [mica.TensorList(st.g)]
+    views = [g_flat[1][(x.data_ptr() - st.g_flat.data_ptr()) // x.element_size():][:x.numel()] for x in st.g]
+    g_lists.append(mica.TensorList(views))
+    norm_host = torch.empty(2, dtype=torch.float32, pin_memory=True)
     W = mica.TensorList(st.w)
-    G = mica.TensorList(st.g)
     M = mica.TensorList(st.m, W.counts)
     V = mica.TensorList(st.v, W.counts)
     norm = torch.empty(1, device="cuda")
     factor = torch.empty(1, device="cuda")
     kw = dict(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps, weight_decay=wl.weight_decay, factor=factor)
-    stream = torch.cuda.current_stream()
+    compute = torch.cuda.current_stream()
+    copier = torch.cuda.Stream()
+    copied = [torch.cuda.Event(), torch.cuda.Event()]
+    released = [torch.cuda.Event(), torch.cuda.Event()]
+    for e in released:
+        e.record(compute)
 
     def step(t):
-        st.g_flat.copy_(g_host, non_blocking=True)
-        mica.mica_clip_grad_norms(G, wl.max_norm, wl.inv_scale, norm_out=norm, factor_out=factor)
-        mica.mica_adamw_steps(W, G, M, V, step=t, **kw)
-        norm_host.copy_(norm, non_blocking=True)
+        x = t % 2
+        with torch.cuda.stream(copier):
+            copier.wait_event(released[x])              # the buffer's previous step has read it
+            g_flat[x].copy_(g_host, non_blocking=True)
+            copied[x].record(copier)
+        compute.wait_event(copied[x])
+        mica.mica_clip_grad_norms(g_lists[x], wl.max_norm, wl.inv_scale, norm_out=norm, factor_out=factor)
+        mica.mica_adamw_steps(W, g_lists[x], M, V, step=t, **kw)
+        released[x].record(compute)
+        norm_host[x:x + 1].copy_(norm, non_blocking=True)
 
     for t in range(1, warmup + 1):
         step(t)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    e0.record(compute)
+    copier.wait_event(e0)
     for i in range(steps):
         step(warmup + 1 + i)
-    e1.record(stream)
+    e1.record(compute)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
     h2d = st.g_flat.numel() * st.g_flat.element_size()
-    del st
+    del st, g_flat, views
     return ms, h2d, 4
 
 

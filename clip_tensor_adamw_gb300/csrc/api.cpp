@@ -168,8 +168,15 @@ static bool overlaps_any(const std::vector<Span>& sorted, const void* p, size_t 
 enum Kind : uint64_t { kAdamW = 1, kNorm = 2, kScale = 3 };
 
 struct Plan {
+    // the list it was built for (compared in full on every lookup)
+    Kind kind = kAdamW;
     int device = 0;
-    std::vector<uint64_t> key;
+    Dtype gdt = kF32, mdt = kF32;
+    int32_t T = 0;
+    std::vector<int64_t> n;
+    std::vector<const void*> ptrs[4];  // the pointer arrays the kind uses, in ListDesc order
+    int64_t total = 0;                 // elements
+    const void* checked_scalar[2] = {nullptr, nullptr};  // the last scalar outputs found valid for this list
     void* dev = nullptr;  // one allocation: TensorRec[T] | WorkItem[I] | double[I] (norm)
     TensorRec* recs = nullptr;
     WorkItem* items = nullptr;
@@ -196,13 +203,9 @@ static std::unordered_map<uint64_t, std::vector<std::unique_ptr<Plan>>> g_plans;
 static size_t g_plan_count = 0;
 constexpr size_t kMaxPlans = 1024;
 
-static uint64_t hash_key(const std::vector<uint64_t>& k) {
-    uint64_t h = 0x243F6A8885A308D3ull;
-    for (uint64_t x : k) {
-        h ^= x + 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
-        h *= 0xFF51AFD7ED558CCDull;
-    }
-    return h;
+static uint64_t mix(uint64_t h, uint64_t x) {
+    h ^= x + 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
+    return h * 0xFF51AFD7ED558CCDull;
 }
 
 static int sm_count(int device) {
@@ -278,11 +281,68 @@ struct ListDesc {
 
 static size_t elem_bytes(Dtype d) { return d == kF16 ? 2 : 4; }
 
-static mica_status build_plan(const ListDesc& L, int device, std::vector<uint64_t>&& key, Plan** out,
-                              void* stream) {
+static int list_arrays(const ListDesc& L, const void* const* out[4]) {
+    if (L.kind == kScale) {
+        out[0] = reinterpret_cast<const void* const*>(L.w);
+        return 1;
+    }
+    if (L.kind == kNorm) {
+        out[0] = L.g;
+        return 1;
+    }
+    out[0] = reinterpret_cast<const void* const*>(L.w);
+    out[1] = L.g;
+    out[2] = L.m;
+    out[3] = L.v;
+    return 4;
+}
+
+// A hash of the list from its header and a sample of its entries (at most ~64): cheap for lists of any length.
+// Lookups compare the whole list, so a shared hash only costs a comparison.
+static uint64_t list_hash(const ListDesc& L, int device) {
+    uint64_t h = 0x243F6A8885A308D3ull;
+    h = mix(h, (uint64_t)L.kind);
+    h = mix(h, (uint64_t)device);
+    h = mix(h, ((uint64_t)L.gdt << 8) | (uint64_t)L.mdt);
+    h = mix(h, (uint64_t)L.T);
+    if (L.T == 0) return h;
+    const void* const* arr[4];
+    const int na = list_arrays(L, arr);
+    const int32_t step = L.T > 64 ? L.T / 64 : 1;
+    for (int32_t k = 0; k < L.T; k += step) {
+        h = mix(h, (uint64_t)L.n[k]);
+        for (int a = 0; a < na; ++a) h = mix(h, ptr_u(arr[a][k]));
+    }
+    h = mix(h, (uint64_t)L.n[L.T - 1]);
+    for (int a = 0; a < na; ++a) h = mix(h, ptr_u(arr[a][L.T - 1]));
+    return h;
+}
+
+static bool same_list(const Plan& p, const ListDesc& L, int device) {
+    if (p.kind != L.kind || p.device != device || p.gdt != L.gdt || p.mdt != L.mdt || p.T != L.T) return false;
+    if (L.T == 0) return true;
+    if (std::memcmp(p.n.data(), L.n, (size_t)L.T * sizeof(int64_t)) != 0) return false;
+    const void* const* arr[4];
+    const int na = list_arrays(L, arr);
+    for (int a = 0; a < na; ++a)
+        if (std::memcmp(p.ptrs[a].data(), arr[a], (size_t)L.T * sizeof(void*)) != 0) return false;
+    return true;
+}
+
+static mica_status build_plan(const ListDesc& L, int device, uint64_t h, Plan** out, void* stream) {
     auto plan = std::make_unique<Plan>();
+    plan->kind = L.kind;
     plan->device = device;
-    plan->key = std::move(key);
+    plan->gdt = L.gdt;
+    plan->mdt = L.mdt;
+    plan->T = L.T;
+    if (L.T > 0) {
+        plan->n.assign(L.n, L.n + L.T);
+        const void* const* arr[4];
+        const int na = list_arrays(L, arr);
+        for (int a = 0; a < na; ++a) plan->ptrs[a].assign(arr[a], arr[a] + L.T);
+    }
+    for (int32_t k = 0; k < L.T; ++k) plan->total += L.n[k];
 
     // pointer checks and the overlap check, over every non-empty buffer of the list
     std::vector<Span> spans;
@@ -412,7 +472,6 @@ static mica_status build_plan(const ListDesc& L, int device, std::vector<uint64_
     if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cuda_fail(e, "waiting for the table upload");
     *out = plan.get();
 
-    uint64_t h = hash_key(plan->key);
     if (g_plan_count >= kMaxPlans) {
         cudaDeviceSynchronize();
         g_plans.clear();
@@ -423,37 +482,54 @@ static mica_status build_plan(const ListDesc& L, int device, std::vector<uint64_
     return MICA_OK;
 }
 
-static mica_status get_plan(const ListDesc& L, int device, Plan** out, void* stream) {
-    std::vector<uint64_t> key;
-    key.reserve(5 + (size_t)L.T * 5);
-    key.push_back((uint64_t)L.kind);
-    key.push_back((uint64_t)device);
-    key.push_back((uint64_t)L.gdt);
-    key.push_back((uint64_t)L.mdt);
-    key.push_back((uint64_t)L.T);
-    for (int32_t k = 0; k < L.T; ++k) {
-        key.push_back((uint64_t)L.n[k]);
-        if (L.kind == kScale) {
-            key.push_back(ptr_u(L.w[k]));
-        } else if (L.kind == kNorm) {
-            key.push_back(ptr_u(L.g[k]));
-        } else {
-            key.push_back(ptr_u(L.w[k]));
-            key.push_back(ptr_u(L.g[k]));
-            key.push_back(ptr_u(L.m[k]));
-            key.push_back(ptr_u(L.v[k]));
-        }
-    }
-    const uint64_t h = hash_key(key);
-    std::lock_guard<std::mutex> lock(g_mu);
+// The cached table of a list, or nullptr.
+static Plan* find_plan(const ListDesc& L, int device, uint64_t h) {
     auto it = g_plans.find(h);
-    if (it != g_plans.end())
-        for (auto& p : it->second)
-            if (p->key == key) {
-                *out = p.get();
-                return MICA_OK;
-            }
-    return build_plan(L, device, std::move(key), out, stream);
+    if (it == g_plans.end()) return nullptr;
+    for (auto& p : it->second)
+        if (same_list(*p, L, device)) return p.get();
+    return nullptr;
+}
+
+// The table of an already validated list: the cached one, or a new one (which checks every pointer).
+static mica_status get_plan(const ListDesc& L, int device, Plan** out, void* stream) {
+    const uint64_t h = list_hash(L, device);
+    std::lock_guard<std::mutex> lock(g_mu);
+    if ((*out = find_plan(L, device, h)) != nullptr) return MICA_OK;
+    return build_plan(L, device, h, out, stream);
+}
+
+// A list seen before needs none of the per-tensor checks again: its counts and pointers equal those of a list that
+// passed them when its table was built.
+static Plan* cached_plan(const ListDesc& L, int device) {
+    if (L.T <= 0) return nullptr;
+    const uint64_t h = list_hash(L, device);
+    std::lock_guard<std::mutex> lock(g_mu);
+    return find_plan(L, device, h);
+}
+
+// The device scalars of a call (d_factor, d_norm): device memory of the current device, aligned, outside the list's
+// buffers. The last pair found valid for a table is remembered, so a repeated call skips the driver queries.
+static mica_status check_scalars(Plan* p, int dev, const float* a, const float* b, const char* what) {
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (p->checked_scalar[0] == a && p->checked_scalar[1] == b) return MICA_OK;
+    }
+    const float* outs[2] = {a, b};
+    const char* names[2] = {"d_factor", "d_norm"};
+    for (int i = 0; i < 2; ++i) {
+        if (!outs[i]) continue;
+        mica_status s = check_device_span(outs[i], 4, 4, dev, names[i], 0);
+        if (s != MICA_OK) return s;
+        if (overlaps_any(p->spans, outs[i], 4)) return fail(MICA_ERR_OVERLAP, "%s lies inside %s", names[i], what);
+    }
+    if (a && b && reinterpret_cast<uintptr_t>(a) + 4 > reinterpret_cast<uintptr_t>(b) &&
+        reinterpret_cast<uintptr_t>(b) + 4 > reinterpret_cast<uintptr_t>(a))
+        return fail(MICA_ERR_OVERLAP, "d_norm and d_factor overlap");
+    std::lock_guard<std::mutex> lock(g_mu);
+    p->checked_scalar[0] = a;
+    p->checked_scalar[1] = b;
+    return MICA_OK;
 }
 
 // ------------------------------------------------------------------------------------------------------------------
@@ -505,18 +581,21 @@ extern "C" mica_status mica_scale_tensors(void* const* t, const int64_t* n, int3
                                           const float* d_factor, void* stream) {
     if (dt != MICA_F32 && dt != MICA_F16) return fail(MICA_ERR_DTYPE, "ScaleTensors takes float32 or float16 tensors");
     if (!d_factor && !std::isfinite(factor)) return fail(MICA_ERR_HYPER, "factor %g is not finite", (double)factor);
-    int64_t total = 0;
-    mica_status s = check_list(T, n, {t}, &total);
-    if (s != MICA_OK) return s;
-    if (total == 0) return ok();
+    if (T < 0 || T > MICA_MAX_TENSORS) return fail(MICA_ERR_COUNT, "T = %d is outside [0, %d]", T, MICA_MAX_TENSORS);
+    if (T > 0 && (!t || !n)) return fail(MICA_ERR_NULL, "a pointer array is NULL");
+    mica_status s;
     int dev = 0;
-    if ((s = current_device(&dev)) != MICA_OK) return s;
-    if (d_factor && (s = check_device_span(d_factor, 4, 4, dev, "d_factor", 0)) != MICA_OK) return s;
     ListDesc L{kScale, T, n, reinterpret_cast<float* const*>(t), nullptr, nullptr, nullptr, (Dtype)dt, kF32};
     Plan* p = nullptr;
-    if ((s = get_plan(L, dev, &p, stream)) != MICA_OK) return s;
-    if (d_factor && overlaps_any(p->spans, d_factor, 4))
-        return fail(MICA_ERR_OVERLAP, "d_factor lies inside one of the tensors");
+    if (T > 0 && current_device(&dev) == MICA_OK) p = cached_plan(L, dev);
+    if (!p) {
+        int64_t total = 0;
+        if ((s = check_list(T, n, {t}, &total)) != MICA_OK) return s;
+        if (total == 0) return ok();
+        if ((s = current_device(&dev)) != MICA_OK) return s;
+        if ((s = get_plan(L, dev, &p, stream)) != MICA_OK) return s;
+    }
+    if ((s = check_scalars(p, dev, d_factor, nullptr, "one of the tensors")) != MICA_OK) return s;
     return after_launch(launch_scale(p->recs, p->items, p->num_items, p->item_octs, (Dtype)dt, factor, d_factor,
                                      stream),
                         stream, "ScaleTensors launch");
@@ -530,23 +609,23 @@ extern "C" mica_status mica_clip_grad_norms(const void* const* g, const int64_t*
     if (std::isnan(max_norm) || !(max_norm > 0.0f)) return fail(MICA_ERR_HYPER, "max_norm %g is not > 0", (double)max_norm);
     if (!std::isfinite(inv_scale) || !(inv_scale > 0.0f))
         return fail(MICA_ERR_HYPER, "inv_scale %g is not finite and > 0", (double)inv_scale);
-    int64_t total = 0;
-    mica_status s = check_list(T, n, {g}, &total);
-    if (s != MICA_OK) return s;
+    if (T < 0 || T > MICA_MAX_TENSORS) return fail(MICA_ERR_COUNT, "T = %d is outside [0, %d]", T, MICA_MAX_TENSORS);
+    if (T > 0 && (!g || !n)) return fail(MICA_ERR_NULL, "a pointer array is NULL");
+    mica_status s;
     int dev = 0;
-    if ((s = current_device(&dev)) != MICA_OK) return s;
-    if ((s = check_device_span(d_factor, 4, 4, dev, "d_factor", 0)) != MICA_OK) return s;
-    if (d_norm && (s = check_device_span(d_norm, 4, 4, dev, "d_norm", 0)) != MICA_OK) return s;
-    if (d_norm && reinterpret_cast<uintptr_t>(d_norm) + 4 > reinterpret_cast<uintptr_t>(d_factor) &&
-        reinterpret_cast<uintptr_t>(d_factor) + 4 > reinterpret_cast<uintptr_t>(d_norm))
-        return fail(MICA_ERR_OVERLAP, "d_norm and d_factor overlap");
-    // An empty list still gets its norm (0) and factor written: the table then holds no tensors and no items.
-    ListDesc L{kNorm, total ? T : 0, n, nullptr, const_cast<void* const*>(reinterpret_cast<const void* const*>(g)),
-               nullptr, nullptr, (Dtype)gdt, kF32};
+    ListDesc L{kNorm, T, n, nullptr, const_cast<void* const*>(reinterpret_cast<const void* const*>(g)), nullptr,
+               nullptr, (Dtype)gdt, kF32};
     Plan* p = nullptr;
-    if ((s = get_plan(L, dev, &p, stream)) != MICA_OK) return s;
-    if (overlaps_any(p->spans, d_factor, 4) || (d_norm && overlaps_any(p->spans, d_norm, 4)))
-        return fail(MICA_ERR_OVERLAP, "d_norm or d_factor lies inside a gradient");
+    if (T > 0 && current_device(&dev) == MICA_OK) p = cached_plan(L, dev);
+    if (!p) {
+        int64_t total = 0;
+        if ((s = check_list(T, n, {g}, &total)) != MICA_OK) return s;
+        if ((s = current_device(&dev)) != MICA_OK) return s;
+        // An empty list still gets its norm (0) and factor written: its table holds no tensors.
+        if (total == 0) L.T = 0;
+        if ((s = get_plan(L, dev, &p, stream)) != MICA_OK) return s;
+    }
+    if ((s = check_scalars(p, dev, d_factor, d_norm, "a gradient")) != MICA_OK) return s;
     return after_launch(launch_norm(p->chunks, (Dtype)gdt, inv_scale, p->partials, p->ticket, max_norm, d_norm,
                                     d_factor, stream),
                         stream, "ClipGradNorms launch");
@@ -566,18 +645,22 @@ extern "C" mica_status mica_adamw_steps(float* const* w, void* const* g, void* c
     if (hp->reserved != 0) return fail(MICA_ERR_HYPER, "hp->reserved must be 0");
     if (!(hp->beta1 >= 0.0 && hp->beta1 < 1.0)) return fail(MICA_ERR_BETA, "beta1 %g is outside [0, 1)", hp->beta1);
     if (!(hp->beta2 >= 0.0 && hp->beta2 < 1.0)) return fail(MICA_ERR_BETA, "beta2 %g is outside [0, 1)", hp->beta2);
-    int64_t total = 0;
-    mica_status s = check_list(T, n, {reinterpret_cast<const void* const*>(w), g, m, v}, &total);
-    if (s != MICA_OK) return s;
-    if (total == 0) return ok();
+    if (T < 0 || T > MICA_MAX_TENSORS) return fail(MICA_ERR_COUNT, "T = %d is outside [0, %d]", T, MICA_MAX_TENSORS);
+    if (T > 0 && (!w || !g || !m || !v || !n)) return fail(MICA_ERR_NULL, "a pointer array is NULL");
+    mica_status s;
     int dev = 0;
-    if ((s = current_device(&dev)) != MICA_OK) return s;
-    if (d_factor && (s = check_device_span(d_factor, 4, 4, dev, "d_factor", 0)) != MICA_OK) return s;
     ListDesc L{kAdamW, T, n, w, g, m, v, (Dtype)gdt, (Dtype)mdt};
     Plan* p = nullptr;
-    if ((s = get_plan(L, dev, &p, stream)) != MICA_OK) return s;
-    if (d_factor && overlaps_any(p->spans, d_factor, 4))
-        return fail(MICA_ERR_OVERLAP, "d_factor lies inside one of the step's buffers");
+    if (T > 0 && current_device(&dev) == MICA_OK) p = cached_plan(L, dev);
+    if (!p) {
+        int64_t total = 0;
+        if ((s = check_list(T, n, {reinterpret_cast<const void* const*>(w), g, m, v}, &total)) != MICA_OK) return s;
+        if (total == 0) return ok();
+        if ((s = current_device(&dev)) != MICA_OK) return s;
+        if ((s = get_plan(L, dev, &p, stream)) != MICA_OK) return s;
+    }
+    if (p->total == 0) return ok();
+    if ((s = check_scalars(p, dev, d_factor, nullptr, "one of the step's buffers")) != MICA_OK) return s;
 
     // the step's scalars: PyTorch's, each in double and rounded once to float32
     const double t = (double)hp->step;
