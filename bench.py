@@ -45,10 +45,10 @@ PROFILE = os.path.join(ROOT, "profiles", "adamw_gpt2_small.md")
 # ----------------------------------------------------------------------------------------------------------------
 
 def adamw_bytes_per_param(wl: workloads.Workload, zero_grad: bool = False) -> float:
-    """AdamW kernel: w read + write (8), g read (4 or 2), m and v read + write (16 float32, 4 packed BF16); the
-    gradient's zero write (4 or 2) only with zero_grad."""
+    """AdamW kernel: w read + write (8), g read (4 or 2), m and v read + write (16 float32, 8 packed BF16); the
+    gradient's zero write (4 or 2) only with zero_grad. 28 B/param with float32 moments, 20 with packed ones."""
     g = 2.0 if wl.grad_dtype == "f16" else 4.0
-    mv = 4.0 if wl.moments == "bf16x2" else 16.0
+    mv = 8.0 if wl.moments == "bf16x2" else 16.0
     return 8.0 + g + mv + (g if zero_grad else 0.0)
 
 

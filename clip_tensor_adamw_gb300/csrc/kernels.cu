@@ -320,6 +320,7 @@ __global__ void __launch_bounds__(kThreads, 3) adamw_kernel(const TensorRec* __r
                                                             const WorkItem* __restrict__ items, int32_t num_items,
                                                             int32_t item_octs, StepScalars s,
                                                             const float* __restrict__ d_factor) {
+    allow_dependents();  // the next step's norm may launch and set up while this kernel's last CTAs run
     Factor fac{d_factor, 1.0f, false};
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int32_t k = blockIdx.x; k < num_items; k += gridDim.x) {
@@ -542,6 +543,7 @@ __global__ void __launch_bounds__(kThreads, kNormDirectCtasPerSm) norm_direct_ke
     SumSq acc{{0.f, 0.f}, {0.f, 0.f}, 0.f};
     Cursor cur;
     cur.init(ct, k0);
+    wait_prerequisite();  // the kernel queued before may still be writing the gradients (zero_grad)
     auto sum2 = [&](const float (&a)[8], const float (&b)[8]) {
         acc.add8<kScaled>(a, inv_scale);
         acc.add8<kScaled>(b, inv_scale);
@@ -672,6 +674,7 @@ __global__ void __launch_bounds__(kNormThreads, kNormTmaCtasPerSm) norm_tma_kern
         mbar_fence_init();
     }
     __syncthreads();
+    wait_prerequisite();  // the kernel queued before may still be writing the gradients (zero_grad)
 
     double mine = 0.0;
     if (warp == kWarps) {
@@ -893,22 +896,33 @@ int launch_adamw(const TensorRec* recs, const WorkItem* items, int32_t num_items
     return (int)(e != cudaSuccess ? e : cudaGetLastError());
 }
 
+// Both norm kernels are launched as programmatic dependents of the kernel queued before them: they may start and
+// set up while it finishes, and wait for it (griddepcontrol.wait) before reading any gradient.
 template <Dtype G, bool kScaled>
 cudaError_t launch_norm_t(const ChunkTable& ct, cudaStream_t st, float inv_scale, double* partials,
                           unsigned int* ticket, float max_norm, float* d_norm, float* d_factor) {
-    const dim3 grid(ct.grid > 0 ? ct.grid : 1);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ct.grid > 0 ? ct.grid : 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (ct.direct) {
-        norm_direct_kernel<G, kScaled><<<grid, dim3(kThreads), 0, st>>>(ct, inv_scale, partials, ticket, max_norm,
-                                                                         d_norm, d_factor);
-        return cudaGetLastError();
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = 0;
+        return cudaLaunchKernelEx(&cfg, norm_direct_kernel<G, kScaled>, ct, inv_scale, partials, ticket, max_norm,
+                                  d_norm, d_factor);
     }
     const size_t smem = norm_smem_bytes<G>();
     cudaError_t e = cudaFuncSetAttribute(norm_tma_kernel<G, kScaled>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    norm_tma_kernel<G, kScaled><<<grid, dim3(kNormThreads), smem, st>>>(ct, inv_scale, partials, ticket, max_norm,
-                                                                        d_norm, d_factor);
-    return cudaGetLastError();
+    cfg.blockDim = dim3(kNormThreads);
+    cfg.dynamicSmemBytes = smem;
+    return cudaLaunchKernelEx(&cfg, norm_tma_kernel<G, kScaled>, ct, inv_scale, partials, ticket, max_norm, d_norm,
+                              d_factor);
 }
 
 int launch_norm(const ChunkTable& ct, Dtype gdt, float inv_scale, double* partials, unsigned int* ticket,
