@@ -219,6 +219,18 @@ def run_reference(args, wl: workloads.Workload) -> None:
 # the GPU step
 # ----------------------------------------------------------------------------------------------------------------
 
+def slowest_rank_ms(ms: float, dist, device) -> float:
+    """The timed region of the slowest rank: every rank's time, reduced by MAX over the process group."""
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world: int, params: int, steps: int, total_ms: float) -> float:
+    """Parameters stepped per second by the whole job: every rank steps its own full list (weak scaling)."""
+    return world * params * steps / (total_ms / 1e3)
+
+
 def measure(wl: workloads.Workload, steps: int, warmup: int, zero_grad: bool, dist=None, sampler=None):
     """Times `steps` steps of the whole hot path on the device (inputs resident). Returns a dict of figures."""
     import clip_tensor_adamw_gb300 as mica
@@ -260,9 +272,7 @@ def measure(wl: workloads.Workload, steps: int, warmup: int, zero_grad: bool, di
     total_ms = start.elapsed_time(end)
     if dist is not None:
         dist.barrier()
-        tt = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+        total_ms = slowest_rank_ms(total_ms, dist, "cuda")
     # each kernel's own duration, from events around each launch (a separate loop: events between the two
     # launches of a step keep them from overlapping)
     k2 = min(steps, 50)
@@ -392,7 +402,7 @@ def main():
 
     P = wl.params
     sec = main_fig["total_ms"] / 1e3
-    value = world * P * args.steps / sec
+    value = job_value(world, P, args.steps, main_fig["total_ms"])
     step_bpp = step_bytes_per_param(wl)
     step_gbs = P * step_bpp * args.steps / sec / 1e9
     a_bpp = adamw_bytes_per_param(wl)

@@ -1,0 +1,58 @@
+"""The benchmark's multi-process path on the CPU: two gloo ranks, as torchrun would start them.
+
+Every rank steps its own full parameter list (replicas), the job's time is the slowest rank's (a MAX all-reduce),
+and the job's value counts every rank's parameters. The reference arm prints only on rank 0."""
+import io
+import os
+import socket
+import sys
+from contextlib import redirect_stdout
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank: int, world: int, port: int, times, out):
+    sys.path.insert(0, ROOT)
+    import bench
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        slow = bench.slowest_rank_ms(times[rank], dist, "cpu")
+        out[rank] = (slow, bench.job_value(world, 1000, 10, slow))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_slowest_rank_and_job_value():
+    world, port = 2, _free_port()
+    out = mp.Manager().dict()
+    mp.spawn(_rank_main, args=(world, port, [1.5, 4.0], out), nprocs=world, join=True)
+    assert out[0][0] == out[1][0] == 4.0
+    assert out[0][1] == pytest.approx(world * 1000 * 10 / 4.0e-3)
+
+
+def test_reference_arm_prints_on_rank_zero_only(monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads
+    wl = workloads.WORKLOADS["tiny"]
+
+    class Args:
+        steps, warmup, gpus = 1, 3, 2
+    for rank, expect in (("1", ""), ("0", '"impl": "reference"')):
+        monkeypatch.setenv("RANK", rank)
+        buf = io.StringIO()
+        with redirect_stdout(buf):
+            bench.run_reference(Args(), wl)
+        assert (expect in buf.getvalue()) if expect else buf.getvalue() == ""
