@@ -25,7 +25,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
-F32, F16, BF16X2 = 0, 1, 2
+F32, F16, BF16X2, BF16X2_M = 0, 1, 2, 3
+SKIP_NONFINITE, COUPLED_L2 = 1, 2
 CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11", "-shared", "-fPIC"]
 
 
@@ -74,6 +75,9 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         fn.argtypes = [_P, _P, _P, _P, _I64P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                        ctypes.POINTER(_Scalars), ctypes.c_float, ctypes.c_int32]
         fn.restype = None
+    lib.ora_adam_steps_flags.argtypes = [_P, _P, _P, _P, _I64P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                         ctypes.POINTER(_Scalars), ctypes.c_float, ctypes.c_int32, ctypes.c_uint32]
+    lib.ora_adam_steps_flags.restype = None
     lib.ora_clip_grad_norms.argtypes = [_P, _I64P, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, ctypes.c_float,
                                         ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float),
                                         ctypes.POINTER(ctypes.c_double)]
@@ -128,11 +132,11 @@ def _gdt(g: np.ndarray) -> int:
     raise TypeError(f"gradient dtype {g.dtype} is neither float32 nor float16")
 
 
-def _mdt(m: np.ndarray) -> int:
+def _mdt(m: np.ndarray, v: np.ndarray | None = None) -> int:
     if m.dtype == np.float32:
         return F32
     if m.dtype == np.uint32:
-        return BF16X2
+        return BF16X2_M if v is not None and v.dtype == np.float32 else BF16X2
     raise TypeError(f"moment dtype {m.dtype} is neither float32 nor packed uint32")
 
 
@@ -192,17 +196,24 @@ class Oracle:
 
     # ---- AdamWSteps ----
     def adamw_steps(self, ws, gs, ms, vs, hp: Hyper, factor: float = 1.0, zero_grad: bool = False,
-                    decoupled: bool = True) -> None:
-        """In place over the lists; ``decoupled=False`` is Adam with the coupled L2 term."""
+                    decoupled: bool = True, skip_nonfinite: bool = False) -> None:
+        """In place over the lists; ``decoupled=False`` is Adam with the coupled L2 term; ``skip_nonfinite`` leaves
+        w, m, v as they are when the factor is not > 0. Packed m with float32 v is the BF16X2_M moment type."""
         T = len(ws)
         if T == 0:
             return
-        gdt, mdt = _gdt(gs[0]), _mdt(ms[0])
+        gdt, mdt = _gdt(gs[0]), _mdt(ms[0], vs[0])
         for w, g, m, v in zip(ws, gs, ms, vs):
             assert w.dtype == np.float32 and w.flags.c_contiguous and g.size == w.size
-            words = (w.size + 1) // 2 if mdt == BF16X2 else w.size
-            assert m.size == words and v.size == words and m.dtype == v.dtype
+            half = (w.size + 1) // 2
+            assert m.size == (half if mdt in (BF16X2, BF16X2_M) else w.size)
+            assert v.size == (half if mdt == BF16X2 else w.size)
         s = self._scalars_struct(hp)
+        if skip_nonfinite:
+            flags = SKIP_NONFINITE | (0 if decoupled else COUPLED_L2)
+            self.lib.ora_adam_steps_flags(_ptrs(ws), _ptrs(gs), _ptrs(ms), _ptrs(vs), _sizes([w.size for w in ws]), T,
+                                          gdt, mdt, ctypes.byref(s), np.float32(factor), int(bool(zero_grad)), flags)
+            return
         fn = self.lib.ora_adamw_steps if decoupled else self.lib.ora_adam_l2_steps
         fn(_ptrs(ws), _ptrs(gs), _ptrs(ms), _ptrs(vs), _sizes([w.size for w in ws]), T, gdt, mdt, ctypes.byref(s),
            np.float32(factor), int(bool(zero_grad)))
@@ -216,10 +227,11 @@ class Oracle:
 
     # ---- the whole hot path ----
     def clip_adamw_step(self, ws, gs, ms, vs, hp: Hyper, max_norm: float, inv_scale: float = 1.0,
-                        zero_grad: bool = False):
-        """Norm, clip factor, then AdamW over every group. Returns ``(norm, factor)``."""
+                        zero_grad: bool = False, decoupled: bool = True, skip_nonfinite: bool = False):
+        """Norm, clip factor, then the Adam-family update over every group. Returns ``(norm, factor)``."""
         norm, factor, _ = self.clip_grad_norms(gs, max_norm, inv_scale)
-        self.adamw_steps(ws, gs, ms, vs, hp, factor=factor, zero_grad=zero_grad)
+        self.adamw_steps(ws, gs, ms, vs, hp, factor=factor, zero_grad=zero_grad, decoupled=decoupled,
+                         skip_nonfinite=skip_nonfinite)
         return norm, factor
 
 

@@ -38,8 +38,8 @@
 #include <stdint.h>
 #include <string.h>
 
-/* element types, the oracle's own codes */
-enum { ORA_F32 = 0, ORA_F16 = 1, ORA_BF16X2 = 2 };
+/* element types, the oracle's own codes; ORA_BF16X2_M (moments only): m packed, v float32 */
+enum { ORA_F32 = 0, ORA_F16 = 1, ORA_BF16X2 = 2, ORA_BF16X2_M = 3 };
 
 /* ------------------------------------------------------------------------------------------------------------ */
 /* bit casts                                                                                                    */
@@ -221,7 +221,8 @@ static uint32_t with_half(uint32_t word, int64_t i, uint16_t h) {
 }
 
 /* One group: n elements of the float32 weight w, its gradient g (float32 or binary16), and the two moments m and
- * v (float32, or packed BF16 words, ceil(n/2) of them). decoupled != 0 is AdamW (w *= 1 - lr*wd); decoupled == 0
+ * v (float32, or packed BF16 words, ceil(n/2) of them; or, for ORA_BF16X2_M, m packed and v float32 - the page's
+ * CAdamWBF16 with v16 false). decoupled != 0 is AdamW (w *= 1 - lr*wd); decoupled == 0
  * is Adam's coupled L2 (g += wd * w), the other case the page's Adam family holds. Element by element, each float
  * operation rounded on its own, in this order:
  *   gh = g * factor                        (unscale and clip, folded)
@@ -243,27 +244,27 @@ void ora_adam_group(float* w, void* g, void* m, void* v, int64_t n, int32_t gdt,
         if (!decoupled) gh = gh + wi * s->wd;
         float wdec = decoupled ? wi * s->dec : wi;
 
-        float mi, vi;
-        if (mdt == ORA_BF16X2) {
-            mi = ora_f32_from_bf16(half_of(((uint32_t*)m)[i >> 1], i));
-            vi = ora_f32_from_bf16(half_of(((uint32_t*)v)[i >> 1], i));
-        } else {
-            mi = ((float*)m)[i];
-            vi = ((float*)v)[i];
-        }
+        const int m_packed = (mdt == ORA_BF16X2 || mdt == ORA_BF16X2_M);
+        const int v_packed = (mdt == ORA_BF16X2);
+        float mi = m_packed ? ora_f32_from_bf16(half_of(((uint32_t*)m)[i >> 1], i)) : ((float*)m)[i];
+        float vi = v_packed ? ora_f32_from_bf16(half_of(((uint32_t*)v)[i >> 1], i)) : ((float*)v)[i];
 
         float m_new = mi + s->c1 * (gh - mi);
         float v_new = vi * s->b2 + (s->c2 * gh) * gh;
 
-        if (mdt == ORA_BF16X2) {
+        /* a packed moment is rounded to BF16 and stored; the weight reads the stored, rounded value */
+        if (m_packed) {
             uint16_t hm = ora_bf16_from_f32(m_new);
-            uint16_t hv = ora_bf16_from_f32(v_new);
             ((uint32_t*)m)[i >> 1] = with_half(((uint32_t*)m)[i >> 1], i, hm);
-            ((uint32_t*)v)[i >> 1] = with_half(((uint32_t*)v)[i >> 1], i, hv);
-            m_new = ora_f32_from_bf16(hm);  /* the weight reads the stored, rounded moments */
-            v_new = ora_f32_from_bf16(hv);
+            m_new = ora_f32_from_bf16(hm);
         } else {
             ((float*)m)[i] = m_new;
+        }
+        if (v_packed) {
+            uint16_t hv = ora_bf16_from_f32(v_new);
+            ((uint32_t*)v)[i >> 1] = with_half(((uint32_t*)v)[i >> 1], i, hv);
+            v_new = ora_f32_from_bf16(hv);
+        } else {
             ((float*)v)[i] = v_new;
         }
 
@@ -293,6 +294,27 @@ void ora_adam_l2_steps(float* const* w, void* const* g, void* const* m, void* co
                        int32_t gdt, int32_t mdt, const ora_scalars* s, float factor, int32_t zero_grad) {
     for (int32_t k = 0; k < T; ++k)
         ora_adam_group(w[k], g[k], m[k], v[k], n[k], gdt, mdt, s, factor, zero_grad, 0);
+}
+
+/* The Adam family over a list with the step's options: bit 1 of `flags` picks Adam's coupled L2 form over AdamW's
+ * decoupled decay; bit 0 skips the update when the factor is not > 0 - the joint norm was NaN (factor NaN) or
+ * infinite (factor 0), the overflow a loss-scaled float16 step checks for before stepping - in which case only the
+ * gradient is zeroed (when zero_grad). */
+void ora_adam_steps_flags(float* const* w, void* const* g, void* const* m, void* const* v, const int64_t* n,
+                          int32_t T, int32_t gdt, int32_t mdt, const ora_scalars* s, float factor, int32_t zero_grad,
+                          uint32_t flags) {
+    const int skip = (flags & 1u) && !(factor > 0.0f);
+    const int decoupled = !(flags & 2u);
+    for (int32_t k = 0; k < T; ++k) {
+        if (!skip) {
+            ora_adam_group(w[k], g[k], m[k], v[k], n[k], gdt, mdt, s, factor, zero_grad, decoupled);
+        } else if (zero_grad) {
+            for (int64_t i = 0; i < n[k]; ++i) {
+                if (gdt == ORA_F16) ((uint16_t*)g[k])[i] = 0;
+                else ((float*)g[k])[i] = 0.0f;
+            }
+        }
+    }
 }
 
 /* ClipGradNorms: the joint norm and the folded factor of one list. */

@@ -420,6 +420,80 @@ def pin_scale_tensors(o: oracle.Oracle) -> None:
         np.testing.assert_array_equal(a.view(np.uint16), b.view(np.uint16))
 
 
+def pin_packed_m_float_v(o: oracle.Oracle) -> None:
+    """m packed, v float32 (the page's CAdamWBF16 with v16 false). With b1 = b2 = eps = 0 and t = 1, m = bf16(g)
+    and v = g*g unrounded, so the weight moves by exactly lr * bf16(g) / sqrt(g*g) (PyTorch's bfloat16 rounding
+    for m). Rounding v too, or leaving m unrounded, moves it by up to 2^-8 relative more. From zero moments with the
+    usual betas, the first step's moments are (1-b1) g within BF16 and (1-b2) g^2 within float32 rounding."""
+    rng = _rng(13)
+    g = rng.uniform(0.5, 2.0, size=301).astype(np.float32) * rng.choice([-1, 1], size=301).astype(np.float32)
+    w = np.zeros(g.size, np.float32)
+    m = np.zeros((g.size + 1) // 2, np.uint32)
+    v = np.zeros(g.size, np.float32)
+    o.adamw_steps([w], [g.copy()], [m], [v], Hyper(lr=1e-3, beta1=0.0, beta2=0.0, eps=0.0, weight_decay=0.0, step=1))
+    tg = torch.from_numpy(g)
+    mr = tg.to(torch.bfloat16).to(torch.float64)
+    vv = (tg * tg).to(torch.float64)
+    _close(w, (-1e-3 * mr / vv.sqrt()).numpy(), 4 * 2.0 ** -24, 0)
+    _close(v, vv.numpy(), 2.0 ** -24, 0)
+    g2 = rng.normal(0, 1e-3, size=257).astype(np.float32)
+    w0 = rng.normal(0, 0.02, size=g2.size).astype(np.float32)
+    w = w0.copy()
+    m = np.zeros((g2.size + 1) // 2, np.uint32)
+    v = np.zeros(g2.size, np.float32)
+    o.adamw_steps([w], [g2.copy()], [m], [v], Hyper(step=1, **HP0))
+    gd = g2.astype(np.float64)
+    _close(unpack_bf16(m, g2.size), 0.1 * gd, 2.0 ** -8, 1e-30)
+    _close(v, 0.05 * gd * gd, 4 * 2.0 ** -24, 1e-30)
+    upd = HP0["lr"] * gd / (np.abs(gd) + HP0["eps"])
+    _close(w, w0.astype(np.float64) * (1 - HP0["lr"] * HP0["weight_decay"]) - upd, 0,
+           2 * f32_ulp(w0) + 2.0 ** -7 * np.abs(upd) + 1e-12)
+
+
+def pin_skip_nonfinite_vs_gradscaler(o: oracle.Oracle) -> None:
+    """A loss-scaled step whose gradient overflowed is skipped, as PyTorch's GradScaler skips optimizer.step(): the
+    parameters and moments stay as they were; the next, finite step is the normal AdamW step on the unscaled
+    gradient. (GradScaler does not clip, so max_norm is infinite here; t counts only the steps taken.)"""
+    rng = _rng(14)
+    n = 64
+    w0 = rng.normal(0, 0.02, size=n).astype(np.float32)
+    grads = [rng.normal(0, 1e-2, size=n).astype(np.float32) for _ in range(2)]
+    grads[0][5] = np.inf
+    scale = 1024.0
+    p = torch.nn.Parameter(torch.from_numpy(w0.copy()))
+    opt = torch.optim.AdamW([p], lr=HP0["lr"], betas=(HP0["beta1"], HP0["beta2"]), eps=HP0["eps"],
+                            weight_decay=HP0["weight_decay"], foreach=False, fused=False)
+    scaler = torch.amp.GradScaler("cpu", init_scale=scale, growth_interval=1000)
+    scales = []
+    for gnp in grads:
+        scales.append(scaler.get_scale())
+        opt.zero_grad()
+        scaler.scale((p * torch.from_numpy(gnp)).sum()).backward()  # the gradient is g * scale
+        scaler.step(opt)
+        scaler.update()
+    w = w0.copy()
+    m = np.zeros(n, np.float32)
+    v = np.zeros(n, np.float32)
+    t = 0
+    for gnp, sc in zip(grads, scales):
+        g_scaled = (gnp.astype(np.float64) * sc).astype(np.float32)
+        inv = 1.0 / sc
+        norm, factor, _ = o.clip_grad_norms([g_scaled], np.inf, inv)
+        taken = bool(factor > 0)
+        o.adamw_steps([w], [g_scaled.copy()], [m], [v], Hyper(step=t + 1, **HP0), factor=factor, zero_grad=True,
+                      skip_nonfinite=True)
+        if taken:
+            t += 1
+        else:
+            np.testing.assert_array_equal(w, w0)
+            assert not m.any() and not v.any()
+    assert t == 1
+    _close(w, p.detach().numpy(), 1e-6, 1e-7)
+    st = opt.state[p]
+    _close(m, st["exp_avg"].numpy(), 2e-5, 1e-12)
+    _close(v, st["exp_avg_sq"].numpy(), 2e-5, 1e-16)
+
+
 def read_golden(name: str) -> dict:
     out = {}
     with open(os.path.join(GOLDEN, name)) as f:
@@ -450,5 +524,5 @@ ALL_PINS = [
     pin_bf16_rounding, pin_bf16_printed, pin_f16, pin_norm_fsum, pin_norm_closed_forms, pin_clip_factor,
     pin_torch_adamw, pin_torch_adam_l2, pin_first_step_closed_form, pin_constant_gradient,
     pin_packed_reads_rounded_moments, pin_odd_tail_untouched, pin_zero_grad, pin_list_equals_groups,
-    pin_scale_tensors, pin_printed_beta_rounding,
+    pin_scale_tensors, pin_printed_beta_rounding, pin_packed_m_float_v, pin_skip_nonfinite_vs_gradscaler,
 ]

@@ -1,7 +1,8 @@
 """Plant one plausible mistake at a time in a copy of the oracle (on the CPU) and require the pins to catch it.
 
 Each mutation is a textual replacement in a temporary copy of ``oracle/oracle.c``; the copy is compiled with the
-oracle's own flags and every pin is run against it. A mutation that no pin catches would mean the pins cannot tell
+oracle's own flags and every pin is run against it. Every mutation keeps the oracle's memory accesses in bounds
+(a mistake that wrote past an array would corrupt this test process instead of being caught by a pin). A mutation that no pin catches would mean the pins cannot tell
 that mistake from the page's arithmetic.
 """
 import os
@@ -41,6 +42,10 @@ MUTATIONS = {
     "f16_exponent_bias": ("mag = ldexpf((float)(f | 0x400), e - 25);", "mag = ldexpf((float)(f | 0x400), e - 24);"),
     "f16_round_down": ("if (rem > half || (rem == half && (kept & 1u))) kept += 1u;", ";"),
     "scale_ignores_factor": ("p[i] = p[i] * factor;", "p[i] = p[i];"),
+    "packed_m_rounds_v_too": ("const int v_packed = (mdt == ORA_BF16X2);",
+                              "const int v_packed = (mdt == ORA_BF16X2 || mdt == ORA_BF16X2_M);"),
+    "skip_ignored": ("const int skip = (flags & 1u) && !(factor > 0.0f);", "const int skip = 0;"),
+    "skip_on_finite": ("const int skip = (flags & 1u) && !(factor > 0.0f);", "const int skip = (flags & 1u);"),
     "odd_tail_clobbered": ("if (i & 1) return (word & 0x0000FFFFu) | ((uint32_t)h << 16);\n    return (word & 0xFFFF0000u) | (uint32_t)h;",
                            "if (i & 1) return (word & 0x0000FFFFu) | ((uint32_t)h << 16);\n    return (uint32_t)h;"),
 }
