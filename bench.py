@@ -48,7 +48,7 @@ def adamw_bytes_per_param(wl: workloads.Workload, zero_grad: bool = False) -> fl
     """AdamW kernel: w read + write (8), g read (4 or 2), m and v read + write (16 float32, 8 packed BF16); the
     gradient's zero write (4 or 2) only with zero_grad. 28 B/param with float32 moments, 20 with packed ones."""
     g = 2.0 if wl.grad_dtype == "f16" else 4.0
-    mv = 8.0 if wl.moments == "bf16x2" else 16.0
+    mv = {"bf16x2": 8.0, "bf16x2_m": 12.0}.get(wl.moments, 16.0)
     return 8.0 + g + mv + (g if zero_grad else 0.0)
 
 
@@ -231,7 +231,8 @@ def job_value(world: int, params: int, steps: int, total_ms: float) -> float:
     return world * params * steps / (total_ms / 1e3)
 
 
-def measure(wl: workloads.Workload, steps: int, warmup: int, zero_grad: bool, dist=None, sampler=None):
+def measure(wl: workloads.Workload, steps: int, warmup: int, zero_grad: bool, dist=None, sampler=None,
+            coupled_l2: bool = False):
     """Times `steps` steps of the whole hot path on the device (inputs resident). Returns a dict of figures."""
     import clip_tensor_adamw_gb300 as mica
     st = workloads.make_state(wl, "cuda")
@@ -243,7 +244,7 @@ def measure(wl: workloads.Workload, steps: int, warmup: int, zero_grad: bool, di
     norm = torch.empty(1, device="cuda")
     factor = torch.empty(1, device="cuda")
     kw = dict(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps, weight_decay=wl.weight_decay,
-              zero_grad=zero_grad, factor=factor)
+              zero_grad=zero_grad, factor=factor, coupled_l2=coupled_l2)
     stream = torch.cuda.current_stream()
 
     def step(t, ev_mid=None):
@@ -418,12 +419,15 @@ def main():
                                "hbm_gbs_model": P * step_bytes_per_param(wl) / (zg["ms_per_step"] / 1e3) / 1e9,
                                "hbm_gbs_actual": P * step_bytes_per_param(wl, True) / (zg["ms_per_step"] / 1e3) / 1e9,
                                "bytes_per_param_actual": step_bytes_per_param(wl, True)}
-        for other in ("gpt2_small_bf16", "gpt2_xl", "fp16_scaled", "tiny"):
+        others = [(n, workloads.WORKLOADS[n], False) for n in ("gpt2_small_bf16", "gpt2_xl", "fp16_scaled", "tiny")]
+        others += [("gpt2_small_bf16_m", dataclasses.replace(workloads.WORKLOADS["gpt2_small"],
+                                                             name="gpt2_small_bf16_m", moments="bf16x2_m"), False),
+                   ("gpt2_small_adam_l2", workloads.WORKLOADS["gpt2_small"], True)]
+        for other, owl, coupled in others:
             if other == wl.name:
                 continue
-            owl = workloads.WORKLOADS[other]
             k = 40 if other == "gpt2_xl" else max(20, args.steps // 4)
-            f, _ = measure(owl, k, args.warmup, zero_grad=False)
+            f, _ = measure(owl, k, args.warmup, zero_grad=False, coupled_l2=coupled)
             torch.cuda.empty_cache()
             extras[other] = {"params": owl.params, "ms_per_step": f["ms_per_step"],
                              "params_per_s": owl.params / (f["ms_per_step"] / 1e3),

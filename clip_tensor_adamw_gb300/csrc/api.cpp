@@ -371,18 +371,21 @@ static mica_status build_plan(const ListDesc& L, int device, uint64_t h, Plan** 
         bool vec = (ptr_u(r.g) % (L.gdt == kF16 ? 16 : 32)) == 0;
         if (L.kind == kAdamW) {
             const size_t wb = (size_t)n * 4;
-            const size_t mb = (L.mdt == kBF16x2) ? (size_t)((n + 1) / 2) * 4 : (size_t)n * 4;
+            const size_t packed_b = (size_t)((n + 1) / 2) * 4, f32_b = (size_t)n * 4;
+            const size_t mb = (L.mdt == kBF16x2 || L.mdt == kBF16x2M) ? packed_b : f32_b;
+            const size_t vb = (L.mdt == kBF16x2) ? packed_b : f32_b;
             if ((s = check_device_span(L.w[k], wb, 4, device, "w", k)) != MICA_OK) return s;
             if ((s = check_device_span(L.m[k], mb, 4, device, "m", k)) != MICA_OK) return s;
-            if ((s = check_device_span(L.v[k], mb, 4, device, "v", k)) != MICA_OK) return s;
+            if ((s = check_device_span(L.v[k], vb, 4, device, "v", k)) != MICA_OK) return s;
             r.w = L.w[k];
             r.m = L.m[k];
             r.v = L.v[k];
             spans.push_back({(uintptr_t)ptr_u(r.w), (uintptr_t)(ptr_u(r.w) + wb), 0, k});
             spans.push_back({(uintptr_t)ptr_u(r.m), (uintptr_t)(ptr_u(r.m) + mb), 2, k});
-            spans.push_back({(uintptr_t)ptr_u(r.v), (uintptr_t)(ptr_u(r.v) + mb), 3, k});
-            const uint64_t ma = (L.mdt == kBF16x2) ? 16 : 32;
-            vec = vec && ptr_u(r.w) % 32 == 0 && ptr_u(r.m) % ma == 0 && ptr_u(r.v) % ma == 0;
+            spans.push_back({(uintptr_t)ptr_u(r.v), (uintptr_t)(ptr_u(r.v) + vb), 3, k});
+            const uint64_t ma = (L.mdt == kBF16x2 || L.mdt == kBF16x2M) ? 16 : 32;  // packed: 4 words an octet
+            const uint64_t va = (L.mdt == kBF16x2) ? 16 : 32;
+            vec = vec && ptr_u(r.w) % 32 == 0 && ptr_u(r.m) % ma == 0 && ptr_u(r.v) % va == 0;
         }
         r.vec = vec ? 1 : 0;
     }
@@ -637,13 +640,15 @@ extern "C" mica_status mica_adamw_steps(float* const* w, void* const* g, void* c
                                         const mica_adamw_hp* hp, const float* d_factor, void* stream) {
     if (!hp) return fail(MICA_ERR_NULL, "hp is NULL");
     if (gdt != MICA_F32 && gdt != MICA_F16) return fail(MICA_ERR_DTYPE, "gradients must be float32 or float16");
-    if (mdt != MICA_F32 && mdt != MICA_BF16X2) return fail(MICA_ERR_DTYPE, "moments must be float32 or packed BF16");
+    if (mdt != MICA_F32 && mdt != MICA_BF16X2 && mdt != MICA_BF16X2_M)
+        return fail(MICA_ERR_DTYPE, "moments must be float32, packed BF16, or packed m with float32 v");
     if (!finite_nonneg(hp->lr)) return fail(MICA_ERR_HYPER, "lr %g is not finite and >= 0", hp->lr);
     if (!finite_nonneg(hp->eps)) return fail(MICA_ERR_HYPER, "eps %g is not finite and >= 0", hp->eps);
     if (!finite_nonneg(hp->weight_decay))
         return fail(MICA_ERR_HYPER, "weight_decay %g is not finite and >= 0", hp->weight_decay);
     if (hp->step < 1) return fail(MICA_ERR_HYPER, "step %lld is not >= 1", (long long)hp->step);
-    if (hp->reserved != 0) return fail(MICA_ERR_HYPER, "hp->reserved must be 0");
+    if (hp->flags & ~(MICA_STEP_SKIP_NONFINITE | MICA_STEP_COUPLED_L2))
+        return fail(MICA_ERR_HYPER, "hp->flags has unknown bits (0x%x)", hp->flags);
     if (!(hp->beta1 >= 0.0 && hp->beta1 < 1.0)) return fail(MICA_ERR_BETA, "beta1 %g is outside [0, 1)", hp->beta1);
     if (!(hp->beta2 >= 0.0 && hp->beta2 < 1.0)) return fail(MICA_ERR_BETA, "beta2 %g is outside [0, 1)", hp->beta2);
     if (T < 0 || T > MICA_MAX_TENSORS) return fail(MICA_ERR_COUNT, "T = %d is outside [0, %d]", T, MICA_MAX_TENSORS);
@@ -673,9 +678,12 @@ extern "C" mica_status mica_adamw_steps(float* const* w, void* const* g, void* c
     sc.bc2 = (float)std::sqrt(1.0 - std::pow(hp->beta2, t));
     sc.dec = (float)(1.0 - hp->lr * hp->weight_decay);
     sc.eps = (float)hp->eps;
+    sc.wd = (float)hp->weight_decay;
     sc.zero_grad = hp->zero_grad ? 1 : 0;
-    return after_launch(launch_adamw(p->recs, p->items, p->num_items, p->item_octs, (Dtype)gdt, (Dtype)mdt, sc,
-                                     d_factor, stream),
+    sc.skip_nonfinite = (hp->flags & MICA_STEP_SKIP_NONFINITE) ? 1 : 0;
+    const bool coupled = (hp->flags & MICA_STEP_COUPLED_L2) != 0;
+    return after_launch(launch_adamw(p->recs, p->items, p->num_items, p->item_octs, (Dtype)gdt, (Dtype)mdt, coupled,
+                                     sc, d_factor, stream),
                         stream, "AdamWSteps launch");
 }
 

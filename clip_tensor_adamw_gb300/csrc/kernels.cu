@@ -19,10 +19,6 @@ namespace {
 
 constexpr int kUnrollScale = 2;  // octets in flight per thread and round in ScaleTensors
 
-// AdamW: octets per thread and round; float32 moments move 128 B per octet, packed ones 96 B
-template <Dtype M>
-struct AdamUnroll { static constexpr int value = 1; };
-
 // ------------------------------------------------------------------------------------------------------------------
 // memory access
 // ------------------------------------------------------------------------------------------------------------------
@@ -116,26 +112,44 @@ struct Factor {
 // AdamW on one octet, in registers
 // ------------------------------------------------------------------------------------------------------------------
 
+// Which moments a moment type stores as packed BF16 words, and the bytes of one octet of each.
+template <Dtype M>
+struct MomentLayout {
+    static constexpr bool kMPacked = (M == kBF16x2 || M == kBF16x2M);
+    static constexpr bool kVPacked = (M == kBF16x2);
+    static constexpr int kMb = kMPacked ? 16 : 32;
+    static constexpr int kVb = kVPacked ? 16 : 32;
+};
+
 // m, v hold the moments read (float32, or the exact widening of the stored BF16); on return they hold the new
-// moments as the weight update reads them (rounded through BF16 when kPacked), and pm, pv the packed words to store.
-template <bool kPacked>
+// moments as the weight update reads them (rounded through BF16 where stored packed), and pm, pv the packed words to
+// store. kCoupled is Adam's coupled L2 form (g + w * wd, no decoupled decay).
+template <Dtype M, bool kCoupled>
 __device__ __forceinline__ void adam8(float (&w)[8], const float (&g)[8], float (&m)[8], float (&v)[8],
                                       uint32_t (&pm)[4], uint32_t (&pv)[4], const StepScalars& s, float f) {
+    using L = MomentLayout<M>;
     float wdec[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        const float gh = __fmul_rn(g[j], f);
-        wdec[j] = __fmul_rn(w[j], s.dec);
+        float gh = __fmul_rn(g[j], f);
+        if constexpr (kCoupled) {
+            gh = __fadd_rn(gh, __fmul_rn(w[j], s.wd));
+            wdec[j] = w[j];
+        } else {
+            wdec[j] = __fmul_rn(w[j], s.dec);
+        }
         m[j] = __fadd_rn(m[j], __fmul_rn(s.c1, __fsub_rn(gh, m[j])));
         v[j] = __fadd_rn(__fmul_rn(v[j], s.b2), __fmul_rn(__fmul_rn(s.c2, gh), gh));
     }
-    if constexpr (kPacked) {
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
+    for (int p = 0; p < 4; ++p) {
+        if constexpr (L::kMPacked) {
             pm[p] = pack_bf16x2(m[2 * p], m[2 * p + 1]);
-            pv[p] = pack_bf16x2(v[2 * p], v[2 * p + 1]);
             m[2 * p] = bf16_lo(pm[p]);
             m[2 * p + 1] = bf16_hi(pm[p]);
+        }
+        if constexpr (L::kVPacked) {
+            pv[p] = pack_bf16x2(v[2 * p], v[2 * p + 1]);
             v[2 * p] = bf16_lo(pv[p]);
             v[2 * p + 1] = bf16_hi(pv[p]);
         }
@@ -147,10 +161,41 @@ __device__ __forceinline__ void adam8(float (&w)[8], const float (&g)[8], float 
     }
 }
 
+// A step to skip: the caller asked to skip steps whose norm was not finite, and the factor is not > 0 (a NaN norm
+// gives a NaN factor, an infinite one a zero factor).
+__device__ __forceinline__ bool skip_step(const StepScalars& s, float f) { return s.skip_nonfinite && !(f > 0.0f); }
+
+// One packed-moment octet's 4 words, element by element (words past the tensor's last element are not read).
+__device__ __forceinline__ void load_words(const void* base, int64_t o, int cnt, uint32_t (&word)[4],
+                                           float (&x)[8]) {
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        if (2 * p < cnt) {
+            word[p] = static_cast<const uint32_t*>(base)[4 * o + p];
+            x[2 * p] = bf16_lo(word[p]);
+            x[2 * p + 1] = bf16_hi(word[p]);
+        }
+    }
+}
+
+// ... and back: the high half of a word that holds no element keeps what it held.
+__device__ __forceinline__ void store_words(void* base, int64_t o, int cnt, const uint32_t (&old)[4],
+                                            const uint32_t (&word)[4]) {
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        if (2 * p < cnt) {
+            uint32_t x = word[p];
+            if (2 * p + 1 >= cnt) x = (x & 0x0000FFFFu) | (old[p] & 0xFFFF0000u);
+            static_cast<uint32_t*>(base)[4 * o + p] = x;
+        }
+    }
+}
+
 // One octet element by element: for bases not aligned for the vectors, and for a tensor's last, partial octet.
 // Elements past n are neither read nor written, nor is the high half of a last packed word that holds no element.
-template <Dtype G, Dtype M>
+template <Dtype G, Dtype M, bool kCoupled>
 __device__ __noinline__ void adam_oct_elements(const TensorRec& r, int64_t o, const StepScalars& s, Factor& fac) {
+    using L = MomentLayout<M>;
     const int64_t i0 = o * kOct;
     const int64_t left = r.n - i0;
     const int cnt = left < kOct ? (int)left : kOct;
@@ -159,69 +204,39 @@ __device__ __noinline__ void adam_oct_elements(const TensorRec& r, int64_t o, co
 #pragma unroll
     for (int j = 0; j < 8; ++j) w[j] = g[j] = m[j] = v[j] = 0.f;
 #pragma unroll
-    for (int p = 0; p < 4; ++p) om[p] = ov[p] = 0u;
+    for (int p = 0; p < 4; ++p) om[p] = ov[p] = pm[p] = pv[p] = 0u;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         if (j < cnt) {
             w[j] = r.w[i0 + j];
             g[j] = (G == kF16) ? __half2float(static_cast<const __half*>(r.g)[i0 + j])
                                : static_cast<const float*>(r.g)[i0 + j];
+            if constexpr (!L::kMPacked) m[j] = static_cast<const float*>(r.m)[i0 + j];
+            if constexpr (!L::kVPacked) v[j] = static_cast<const float*>(r.v)[i0 + j];
         }
     }
-    if constexpr (M == kBF16x2) {
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            if (2 * p < cnt) {
-                om[p] = static_cast<const uint32_t*>(r.m)[4 * o + p];
-                ov[p] = static_cast<const uint32_t*>(r.v)[4 * o + p];
-                m[2 * p] = bf16_lo(om[p]);
-                m[2 * p + 1] = bf16_hi(om[p]);
-                v[2 * p] = bf16_lo(ov[p]);
-                v[2 * p + 1] = bf16_hi(ov[p]);
-            }
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            if (j < cnt) {
-                m[j] = static_cast<const float*>(r.m)[i0 + j];
-                v[j] = static_cast<const float*>(r.v)[i0 + j];
-            }
-        }
-    }
+    if constexpr (L::kMPacked) load_words(r.m, o, cnt, om, m);
+    if constexpr (L::kVPacked) load_words(r.v, o, cnt, ov, v);
     const float f = fac.get();
-    adam8<M == kBF16x2>(w, g, m, v, pm, pv, s, f);
+    const bool skip = skip_step(s, f);
+    if (!skip) adam8<M, kCoupled>(w, g, m, v, pm, pv, s, f);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         if (j < cnt) {
-            r.w[i0 + j] = w[j];
+            if (!skip) {
+                r.w[i0 + j] = w[j];
+                if constexpr (!L::kMPacked) static_cast<float*>(r.m)[i0 + j] = m[j];
+                if constexpr (!L::kVPacked) static_cast<float*>(r.v)[i0 + j] = v[j];
+            }
             if (s.zero_grad) {
                 if (G == kF16) static_cast<__half*>(r.g)[i0 + j] = __ushort_as_half(0);
                 else static_cast<float*>(r.g)[i0 + j] = 0.f;
             }
         }
     }
-    if constexpr (M == kBF16x2) {
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            if (2 * p < cnt) {
-                uint32_t nm = pm[p], nv = pv[p];
-                if (2 * p + 1 >= cnt) {  // the word's high half holds no element: keep it as it was
-                    nm = (nm & 0x0000FFFFu) | (om[p] & 0xFFFF0000u);
-                    nv = (nv & 0x0000FFFFu) | (ov[p] & 0xFFFF0000u);
-                }
-                static_cast<uint32_t*>(r.m)[4 * o + p] = nm;
-                static_cast<uint32_t*>(r.v)[4 * o + p] = nv;
-            }
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            if (j < cnt) {
-                static_cast<float*>(r.m)[i0 + j] = m[j];
-                static_cast<float*>(r.v)[i0 + j] = v[j];
-            }
-        }
+    if (!skip) {
+        if constexpr (L::kMPacked) store_words(r.m, o, cnt, om, pm);
+        if constexpr (L::kVPacked) store_words(r.v, o, cnt, ov, pv);
     }
 }
 
@@ -233,89 +248,73 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
 // The four streams of octets [a, b) of tensor r into L2 (a < b, whole octets of an aligned tensor).
 template <Dtype G, Dtype M>
 __device__ __forceinline__ void prefetch_octets(const TensorRec& r, int64_t a, int64_t b) {
-    constexpr int kGb = (G == kF16) ? 16 : 32, kMb = (M == kBF16x2) ? 16 : 32;
+    using L = MomentLayout<M>;
+    constexpr int kGb = (G == kF16) ? 16 : 32;
     const uint32_t n = (uint32_t)(b - a);
     prefetch_l2(reinterpret_cast<const char*>(r.w) + a * 32, n * 32);
     prefetch_l2(static_cast<const char*>(r.g) + a * kGb, n * kGb);
-    prefetch_l2(static_cast<const char*>(r.m) + a * kMb, n * kMb);
-    prefetch_l2(static_cast<const char*>(r.v) + a * kMb, n * kMb);
+    prefetch_l2(static_cast<const char*>(r.m) + a * L::kMb, n * L::kMb);
+    prefetch_l2(static_cast<const char*>(r.v) + a * L::kVb, n * L::kVb);
 }
 
 // Octets [ob, oe) of one tensor: octet ob + lane first, then every `stride`-th. With `prefetch` (a whole CTA on
 // one slice: lane is the thread index and stride the CTA size) thread 0 asks L2 for the rounds one and two ahead,
 // so that the other threads' loads of those rounds find their data in L2 rather than waiting on DRAM.
-template <Dtype G, Dtype M>
+template <Dtype G, Dtype M, bool kCoupled>
 __device__ __forceinline__ void adam_range(const TensorRec& r, int64_t ob, int64_t oe, int lane, int stride,
                                            const StepScalars& s, Factor& fac, bool prefetch = false) {
-    constexpr int U = AdamUnroll<M>::value;
+    using L = MomentLayout<M>;
     const int64_t full = r.n / kOct;  // octets with all eight elements
     if (r.vec) {
         const int64_t vend = oe < full ? oe : full;
-        const int64_t round = (int64_t)stride * U;
+        const int64_t round = stride;
         if (prefetch && lane == 0 && ob + round < vend)
             prefetch_octets<G, M>(r, ob + round, ob + 2 * round < vend ? ob + 2 * round : vend);
-        for (int64_t o0 = ob + lane; o0 < vend; o0 += round) {
-            if (prefetch && lane == 0 && o0 + 2 * round < vend)
-                prefetch_octets<G, M>(r, o0 + 2 * round, o0 + 3 * round < vend ? o0 + 3 * round : vend);
-            float W[U][8], Gf[U][8], Mf[U][8], Vf[U][8];
-            uint4 Gh[U], Mp[U], Vp[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t o = o0 + (int64_t)u * stride;
-                if (o < vend) {
-                    ld8_stream(r.w + kOct * o, W[u]);
-                    if constexpr (G == kF16) Gh[u] = ld16_stream(static_cast<const __half*>(r.g) + kOct * o);
-                    else ld8_stream(static_cast<const float*>(r.g) + kOct * o, Gf[u]);
-                    if constexpr (M == kBF16x2) {
-                        Mp[u] = ld16_stream(static_cast<const uint32_t*>(r.m) + 4 * o);
-                        Vp[u] = ld16_stream(static_cast<const uint32_t*>(r.v) + 4 * o);
-                    } else {
-                        ld8_stream(static_cast<const float*>(r.m) + kOct * o, Mf[u]);
-                        ld8_stream(static_cast<const float*>(r.v) + kOct * o, Vf[u]);
-                    }
-                }
-            }
+        for (int64_t o = ob + lane; o < vend; o += round) {
+            if (prefetch && lane == 0 && o + 2 * round < vend)
+                prefetch_octets<G, M>(r, o + 2 * round, o + 3 * round < vend ? o + 3 * round : vend);
+            float w[8], g[8], m[8], v[8];
+            uint4 gh, mp, vp;
+            ld8_stream(r.w + kOct * o, w);
+            if constexpr (G == kF16) gh = ld16_stream(static_cast<const __half*>(r.g) + kOct * o);
+            else ld8_stream(static_cast<const float*>(r.g) + kOct * o, g);
+            if constexpr (L::kMPacked) mp = ld16_stream(static_cast<const uint32_t*>(r.m) + 4 * o);
+            else ld8_stream(static_cast<const float*>(r.m) + kOct * o, m);
+            if constexpr (L::kVPacked) vp = ld16_stream(static_cast<const uint32_t*>(r.v) + 4 * o);
+            else ld8_stream(static_cast<const float*>(r.v) + kOct * o, v);
             const float f = fac.get();
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t o = o0 + (int64_t)u * stride;
-                if (o < vend) {
-                    uint32_t pm[4], pv[4];
-                    if constexpr (G == kF16) h8_to(Gh[u], Gf[u]);
-                    if constexpr (M == kBF16x2) {
-                        bf8_to(Mp[u], Mf[u]);
-                        bf8_to(Vp[u], Vf[u]);
-                    }
-                    adam8<M == kBF16x2>(W[u], Gf[u], Mf[u], Vf[u], pm, pv, s, f);
-                    st8(r.w + kOct * o, W[u]);
-                    if constexpr (M == kBF16x2) {
-                        st16(static_cast<uint32_t*>(r.m) + 4 * o, make_uint4(pm[0], pm[1], pm[2], pm[3]));
-                        st16(static_cast<uint32_t*>(r.v) + 4 * o, make_uint4(pv[0], pv[1], pv[2], pv[3]));
-                    } else {
-                        st8(static_cast<float*>(r.m) + kOct * o, Mf[u]);
-                        st8(static_cast<float*>(r.v) + kOct * o, Vf[u]);
-                    }
-                    if (s.zero_grad) {
-                        if constexpr (G == kF16) {
-                            st16(static_cast<__half*>(r.g) + kOct * o, make_uint4(0u, 0u, 0u, 0u));
-                        } else {
-                            const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                            st8(static_cast<float*>(r.g) + kOct * o, z);
-                        }
-                    }
+            if (!skip_step(s, f)) {
+                uint32_t pm[4], pv[4];
+                if constexpr (G == kF16) h8_to(gh, g);
+                if constexpr (L::kMPacked) bf8_to(mp, m);
+                if constexpr (L::kVPacked) bf8_to(vp, v);
+                adam8<M, kCoupled>(w, g, m, v, pm, pv, s, f);
+                st8(r.w + kOct * o, w);
+                if constexpr (L::kMPacked) st16(static_cast<uint32_t*>(r.m) + 4 * o, make_uint4(pm[0], pm[1], pm[2], pm[3]));
+                else st8(static_cast<float*>(r.m) + kOct * o, m);
+                if constexpr (L::kVPacked) st16(static_cast<uint32_t*>(r.v) + 4 * o, make_uint4(pv[0], pv[1], pv[2], pv[3]));
+                else st8(static_cast<float*>(r.v) + kOct * o, v);
+            }
+            if (s.zero_grad) {
+                if constexpr (G == kF16) {
+                    st16(static_cast<__half*>(r.g) + kOct * o, make_uint4(0u, 0u, 0u, 0u));
+                } else {
+                    const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                    st8(static_cast<float*>(r.g) + kOct * o, z);
                 }
             }
         }
         // the last, partial octet (n % 8 != 0), when it lies in this range
-        if (full < oe && full >= ob && lane == (int)((full - ob) % stride)) adam_oct_elements<G, M>(r, full, s, fac);
+        if (full < oe && full >= ob && lane == (int)((full - ob) % stride))
+            adam_oct_elements<G, M, kCoupled>(r, full, s, fac);
     } else {
-        for (int64_t o = ob + lane; o < oe; o += stride) adam_oct_elements<G, M>(r, o, s, fac);
+        for (int64_t o = ob + lane; o < oe; o += stride) adam_oct_elements<G, M, kCoupled>(r, o, s, fac);
     }
 }
 
 // One CTA per work item, items taken in reverse order (the norm reads them forwards, so the gradient it read last
 // may still be in L2 when this kernel starts).
-template <Dtype G, Dtype M>
+template <Dtype G, Dtype M, bool kCoupled>
 __global__ void __launch_bounds__(kThreads, 3) adamw_kernel(const TensorRec* __restrict__ recs,
                                                             const WorkItem* __restrict__ items, int32_t num_items,
                                                             int32_t item_octs, StepScalars s,
@@ -329,11 +328,11 @@ __global__ void __launch_bounds__(kThreads, 3) adamw_kernel(const TensorRec* __r
             const TensorRec r = recs[item.t];
             const int64_t no = (r.n + kOct - 1) / kOct;
             const int64_t oe = item.o0 + item_octs < no ? item.o0 + item_octs : no;
-            adam_range<G, M>(r, item.o0, oe, threadIdx.x, kThreads, s, fac, true);
+            adam_range<G, M, kCoupled>(r, item.o0, oe, threadIdx.x, kThreads, s, fac, true);
         } else {
             for (int j = warp; j < item.count; j += kWarps) {
                 const TensorRec r = recs[item.t + j];
-                adam_range<G, M>(r, 0, (r.n + kOct - 1) / kOct, lane, 32, s, fac);
+                adam_range<G, M, kCoupled>(r, 0, (r.n + kOct - 1) / kOct, lane, 32, s, fac);
             }
         }
     }
@@ -857,7 +856,7 @@ __global__ void __launch_bounds__(kThreads) scale_kernel(const TensorRec* __rest
     }
 }
 
-template <Dtype G, Dtype M>
+template <Dtype G, Dtype M, bool kCoupled>
 cudaError_t launch_adamw_t(const WorkItem* items, const TensorRec* recs, int32_t num_items, int32_t item_octs,
                            cudaStream_t st, const StepScalars& s, const float* d_factor) {
     cudaLaunchConfig_t cfg = {};
@@ -870,7 +869,23 @@ cudaError_t launch_adamw_t(const WorkItem* items, const TensorRec* recs, int32_t
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, adamw_kernel<G, M>, recs, items, num_items, item_octs, s, d_factor);
+    return cudaLaunchKernelEx(&cfg, adamw_kernel<G, M, kCoupled>, recs, items, num_items, item_octs, s, d_factor);
+}
+
+template <Dtype G, Dtype M>
+cudaError_t launch_adamw_c(bool coupled, const WorkItem* items, const TensorRec* recs, int32_t num_items,
+                           int32_t item_octs, cudaStream_t st, const StepScalars& s, const float* d_factor) {
+    return coupled ? launch_adamw_t<G, M, true>(items, recs, num_items, item_octs, st, s, d_factor)
+                   : launch_adamw_t<G, M, false>(items, recs, num_items, item_octs, st, s, d_factor);
+}
+
+template <Dtype G>
+cudaError_t launch_adamw_m(Dtype mdt, bool coupled, const WorkItem* items, const TensorRec* recs,
+                           int32_t num_items, int32_t item_octs, cudaStream_t st, const StepScalars& s,
+                           const float* d_factor) {
+    if (mdt == kBF16x2) return launch_adamw_c<G, kBF16x2>(coupled, items, recs, num_items, item_octs, st, s, d_factor);
+    if (mdt == kBF16x2M) return launch_adamw_c<G, kBF16x2M>(coupled, items, recs, num_items, item_octs, st, s, d_factor);
+    return launch_adamw_c<G, kF32>(coupled, items, recs, num_items, item_octs, st, s, d_factor);
 }
 
 }  // namespace
@@ -880,18 +895,12 @@ cudaError_t launch_adamw_t(const WorkItem* items, const TensorRec* recs, int32_t
 // ------------------------------------------------------------------------------------------------------------------
 
 int launch_adamw(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_octs, Dtype gdt,
-                 Dtype mdt, const StepScalars& s, const float* d_factor, void* stream) {
+                 Dtype mdt, bool coupled, const StepScalars& s, const float* d_factor, void* stream) {
     if (num_items <= 0) return (int)cudaSuccess;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e;
-    if (gdt == kF32 && mdt == kF32)
-        e = launch_adamw_t<kF32, kF32>(items, recs, num_items, item_octs, st, s, d_factor);
-    else if (gdt == kF32 && mdt == kBF16x2)
-        e = launch_adamw_t<kF32, kBF16x2>(items, recs, num_items, item_octs, st, s, d_factor);
-    else if (gdt == kF16 && mdt == kF32)
-        e = launch_adamw_t<kF16, kF32>(items, recs, num_items, item_octs, st, s, d_factor);
-    else
-        e = launch_adamw_t<kF16, kBF16x2>(items, recs, num_items, item_octs, st, s, d_factor);
+    const cudaError_t e =
+        (gdt == kF16) ? launch_adamw_m<kF16>(mdt, coupled, items, recs, num_items, item_octs, st, s, d_factor)
+                      : launch_adamw_m<kF32>(mdt, coupled, items, recs, num_items, item_octs, st, s, d_factor);
     count_launches(1);
     return (int)(e != cudaSuccess ? e : cudaGetLastError());
 }

@@ -77,19 +77,22 @@ struct StepScalars {
     float c2;        // 1 - beta2
     float neg_step;  // -(lr / (1 - beta1^t))
     float bc2;       // sqrt(1 - beta2^t)
-    float dec;       // 1 - lr * weight_decay
+    float dec;       // 1 - lr * weight_decay (AdamW's decoupled decay)
     float eps;       // eps
+    float wd;        // weight_decay (Adam's coupled L2 term)
     int32_t zero_grad;
+    int32_t skip_nonfinite;  // leave w, m, v as they are when the factor is not > 0
 };
 
-enum Dtype : int32_t { kF32 = 0, kF16 = 1, kBF16x2 = 2 };
+// kBF16x2M (moments only): m packed as kBF16x2, v float32
+enum Dtype : int32_t { kF32 = 0, kF16 = 1, kBF16x2 = 2, kBF16x2M = 3 };
 
 // Kernel launchers (kernels.cu). Each returns the cudaError_t of its launch as an int.
-// AdamW over every item, one CTA per item. It is launched as a programmatic dependent of the kernel queued before
+// AdamW (or, with `coupled`, Adam with the coupled L2 term) over every item, one CTA per item. It is launched as a programmatic dependent of the kernel queued before
 // it: it may start and load its tensors while that kernel finishes, and reads d_factor only once that kernel has
 // completed.
 int launch_adamw(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_octs, Dtype gdt,
-                 Dtype mdt, const StepScalars& s, const float* d_factor, void* stream);
+                 Dtype mdt, bool coupled, const StepScalars& s, const float* d_factor, void* stream);
 // The joint norm in one launch of ct.grid CTAs: one partial square sum per CTA into `partials` (ct.grid doubles),
 // and the CTA that finishes last sums them in a fixed order and writes norm and factor. `ticket` must be 0 before
 // the launch; the kernel leaves it 0.

@@ -17,7 +17,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 # the library this package builds; MICA_LIB names another build of the same ABI instead
 LIB_PATH = os.environ.get("MICA_LIB") or os.path.join(_PKG, "libmica_optim.so")
 
-MICA_F32, MICA_F16, MICA_BF16X2 = 0, 1, 2
+MICA_F32, MICA_F16, MICA_BF16X2, MICA_BF16X2_M = 0, 1, 2, 3
+MICA_STEP_SKIP_NONFINITE, MICA_STEP_COUPLED_L2 = 1, 2
 STATUS = ["MICA_OK", "MICA_ERR_NULL", "MICA_ERR_COUNT", "MICA_ERR_DTYPE", "MICA_ERR_HYPER", "MICA_ERR_BETA",
           "MICA_ERR_OVERLAP", "MICA_ERR_DEVICE", "MICA_ERR_ADDRESS", "MICA_ERR_CUDA", "MICA_ERR_NOMEM"]
 
@@ -33,7 +34,7 @@ class MicaError(RuntimeError):
 class _HP(ctypes.Structure):
     _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double), ("beta2", ctypes.c_double),
                 ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double), ("step", ctypes.c_int64),
-                ("zero_grad", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("zero_grad", ctypes.c_int32), ("flags", ctypes.c_uint32)]
 
 
 _P = ctypes.c_void_p
@@ -153,10 +154,12 @@ class AdamWHyper:
 
 
 def mica_adamw_steps(w, g, m, v, *, lr: float, beta1: float, beta2: float, eps: float, weight_decay: float,
-                     step: int, zero_grad: bool = False, factor: torch.Tensor | None = None, stream=None) -> None:
+                     step: int, zero_grad: bool = False, factor: torch.Tensor | None = None, stream=None,
+                     skip_nonfinite: bool = False, coupled_l2: bool = False) -> None:
     """AdamWSteps over every group in one launch, in place. ``m`` and ``v`` are float32 tensors of the weights'
-    shapes, or int32 tensors of ceil(n/2) packed BF16 words; ``factor`` is the device scalar from
-    mica_clip_grad_norms (None: 1)."""
+    shapes, or int32 tensors of ceil(n/2) packed BF16 words (packed m with float32 v is allowed); ``factor`` is the
+    device scalar from mica_clip_grad_norms (None: 1). ``skip_nonfinite`` leaves w, m, v as they are when the factor
+    is not > 0 (the norm was not finite); ``coupled_l2`` is Adam's coupled L2 form instead of AdamW's decay."""
     W = _as_list(w)
     sizes = W.counts
     G = _as_list(g)
@@ -166,8 +169,11 @@ def mica_adamw_steps(w, g, m, v, *, lr: float, beta1: float, beta2: float, eps: 
         raise ValueError("w, g, m and v must list the same number of tensors")
     gdt = _dtype_code(G.tensors[0] if G.T else None, "g")
     mdt = _dtype_code(M.tensors[0] if M.T else None, "m")
+    if mdt == MICA_BF16X2 and V.T and _dtype_code(V.tensors[0], "v") == MICA_F32:
+        mdt = MICA_BF16X2_M
+    flags = (MICA_STEP_SKIP_NONFINITE if skip_nonfinite else 0) | (MICA_STEP_COUPLED_L2 if coupled_l2 else 0)
     hp = _HP(float(lr), float(beta1), float(beta2), float(eps), float(weight_decay), int(step), int(bool(zero_grad)),
-             0)
+             flags)
     _check(lib().mica_adamw_steps(W.ptrs, G.ptrs, M.ptrs, V.ptrs, W.n, W.T, gdt, mdt, ctypes.byref(hp), _ptr(factor),
                                   _stream(stream)))
 

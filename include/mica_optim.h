@@ -61,13 +61,23 @@ typedef enum {
 } mica_status;
 
 /* Element types.
- *   MICA_F32     float32.
- *   MICA_F16     IEEE binary16 (gradients, and tensors of mica_scale_tensors).
- *   MICA_BF16X2  packed BF16 moments: a tensor of n elements is ceil(n/2) uint32 words; element 2k is the low 16 bits
- *                of word k and element 2k+1 the high 16 bits (BendTorch "main.bend", section "The layer protocol",
- *                the PTree comment). Rounding into it is to nearest, ties to even; a NaN is stored as 0xFFFF. For odd
- *                n the high half of the last word is never written. */
-typedef enum { MICA_F32 = 0, MICA_F16 = 1, MICA_BF16X2 = 2 } mica_dtype;
+ *   MICA_F32       float32.
+ *   MICA_F16       IEEE binary16 (gradients, and tensors of mica_scale_tensors).
+ *   MICA_BF16X2    packed BF16 moments: a tensor of n elements is ceil(n/2) uint32 words; element 2k is the low 16
+ *                  bits of word k and element 2k+1 the high 16 bits (BendTorch "main.bend", section "The layer
+ *                  protocol", the PTree comment). Rounding into it is to nearest, ties to even; a NaN is stored as
+ *                  0xFFFF. For odd n the high half of the last word is never written.
+ *   MICA_BF16X2_M  moments only: m packed as MICA_BF16X2, v float32 (the same page's CAdamWBF16 with v16 false). */
+typedef enum { MICA_F32 = 0, MICA_F16 = 1, MICA_BF16X2 = 2, MICA_BF16X2_M = 3 } mica_dtype;
+
+/* mica_adamw_hp.flags */
+#define MICA_STEP_SKIP_NONFINITE 1u /* leave w, m and v as they are when the factor read from d_factor is not > 0:
+                                       the norm of the unscaled gradient was NaN or infinite (a float16 step that
+                                       overflowed; the caller then lowers its loss scale). The gradient is still
+                                       zeroed when zero_grad asks for it. */
+#define MICA_STEP_COUPLED_L2 2u     /* Adam with the coupled L2 term instead of AdamW's decoupled decay: the
+                                       gradient becomes g * f + w * weight_decay and w is not decayed (BendTorch
+                                       "main.bend", section "Optimizers": the Adam case of its Adam family). */
 
 #define MICA_MAX_TENSORS (1 << 24)
 
@@ -81,7 +91,7 @@ typedef struct {
     int64_t step;         /* t, 1-based: the count of steps including this one (>= 1) */
     int32_t zero_grad;    /* nonzero: the gradient is written back as zeros (BendTorch "main.bend", section "The layer
                              protocol": a step hands the gradient back zeroed) */
-    int32_t reserved;     /* must be 0 */
+    uint32_t flags;       /* MICA_STEP_* bits; others must be 0 */
 } mica_adamw_hp;
 
 /*
@@ -121,7 +131,9 @@ MICA_API mica_status mica_clip_grad_norms(const void* const* g, const int64_t* n
  *   [mdt == MICA_BF16X2: m and v rounded to BF16, stored, and read back exactly]
  *   w  = w' + (-step * m) / (sqrt(v) / bc2 + eps)
  *   g  = 0                              when hp->zero_grad
- * w: float32 [n]; g: gdt (MICA_F32 or MICA_F16) [n]; m, v: float32 [n] or packed words [ceil(n/2)] (mdt).
+ * w: float32 [n]; g: gdt (MICA_F32 or MICA_F16) [n]; m, v: float32 [n] or packed words [ceil(n/2)] (mdt
+ * MICA_F32, MICA_BF16X2, or MICA_BF16X2_M for packed m and float32 v). hp->flags selects Adam's coupled L2 form and
+ * the skip of a step whose norm was not finite (MICA_STEP_*).
  * All in place. The results are bit-identical to stepping each group alone, and to the same step on the CPU.
  * Sources: "Mica 7.7 ...", section "The whole model in one call" (AdamWSteps); BendTorch "main.bend", section
  * "Optimizers" (the per-element order) and its part "AdamW over packed BF16 moments (CAdamWBF16)".

@@ -69,14 +69,15 @@ def hp_of(wl: workloads.Workload, t: int) -> oracle.Hyper:
 
 
 def gpu_step(st: workloads.State, lists, t: int, zero_grad: bool = False, max_norm: float | None = None,
-             norm_out=None, factor_out=None):
+             norm_out=None, factor_out=None, coupled_l2: bool = False, skip_nonfinite: bool = False):
     """One clip + AdamW step of the hot path on the device, through the binding (one C-ABI call each)."""
     wl = st.wl
     W, G, M, V = lists
     norm, factor = mica.mica_clip_grad_norms(G, wl.max_norm if max_norm is None else max_norm, wl.inv_scale,
                                              norm_out=norm_out, factor_out=factor_out)
     mica.mica_adamw_steps(W, G, M, V, lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps,
-                          weight_decay=wl.weight_decay, step=t, zero_grad=zero_grad, factor=factor)
+                          weight_decay=wl.weight_decay, step=t, zero_grad=zero_grad, factor=factor,
+                          coupled_l2=coupled_l2, skip_nonfinite=skip_nonfinite)
     return norm, factor
 
 
@@ -96,22 +97,20 @@ def compare_state(st: workloads.State, host, same_factor: bool, tag: str) -> Non
         if same_factor:
             exact(gw[k], ow[k], f"{tag} w[{k}] bits")
             exact(gg[k], og[k], f"{tag} g[{k}] bits")
-        if st.packed:
-            dm = bf16_within_one_ulp(gm[k], om[k], n, f"{tag} m[{k}]")
-            dv = bf16_within_one_ulp(gv[k], ov[k], n, f"{tag} v[{k}]")
-            if same_factor:
-                assert not dm.any() and not dv.any(), f"{tag}: packed moments differ with the same factor"
-        else:
-            f32_close(gm[k], om[k], f"{tag} m[{k}]")
-            f32_close(gv[k], ov[k], f"{tag} v[{k}]")
-            if same_factor:
-                exact(gm[k], om[k], f"{tag} m[{k}] bits")
-                exact(gv[k], ov[k], f"{tag} v[{k}] bits")
+        for name, gx, ox, packed in (("m", gm[k], om[k], st.m_packed), ("v", gv[k], ov[k], st.packed)):
+            if packed:
+                d = bf16_within_one_ulp(gx, ox, n, f"{tag} {name}[{k}]")
+                if same_factor:
+                    assert not d.any(), f"{tag}: packed {name}[{k}] differs with the same factor"
+            else:
+                f32_close(gx, ox, f"{tag} {name}[{k}]")
+                if same_factor:
+                    exact(gx, ox, f"{tag} {name}[{k}] bits")
 
 
 def run_parity(wl: workloads.Workload, sizes=None, steps: int | None = None, zero_grad: bool = False,
                seed: int | None = None, ora: oracle.Oracle | None = None, check_every_step: bool = True,
-               grad_hook=None) -> dict:
+               grad_hook=None, coupled_l2: bool = False, skip_nonfinite: bool = False) -> dict:
     """Both sides from the same initial state for ``steps`` steps, each step's gradient drawn on the device and
     copied to the oracle. Compares the norm every step and the state every step (or only at the end)."""
     ora = ora or oracle.Oracle()
@@ -127,8 +126,10 @@ def run_parity(wl: workloads.Workload, sizes=None, steps: int | None = None, zer
             grad_hook(st, t)
         host_g = [x.copy() for x in workloads.host_lists(st)[1]]
         host = (host[0], host_g, host[2], host[3])
-        d_norm, d_factor = gpu_step(st, lists, t, zero_grad=zero_grad)
-        o_norm, o_factor = ora.clip_adamw_step(*host, hp_of(wl, t), wl.max_norm, wl.inv_scale, zero_grad=zero_grad)
+        d_norm, d_factor = gpu_step(st, lists, t, zero_grad=zero_grad, coupled_l2=coupled_l2,
+                                    skip_nonfinite=skip_nonfinite)
+        o_norm, o_factor = ora.clip_adamw_step(*host, hp_of(wl, t), wl.max_norm, wl.inv_scale, zero_grad=zero_grad,
+                                               decoupled=not coupled_l2, skip_nonfinite=skip_nonfinite)
         torch.cuda.synchronize()
         g_norm = np.float32(d_norm.item())
         g_factor = np.float32(d_factor.item())

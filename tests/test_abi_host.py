@@ -43,7 +43,7 @@ def _arr(ctype, vals):
 
 
 def _hp(**kw):
-    d = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, step=1, zero_grad=0, reserved=0)
+    d = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, step=1, zero_grad=0, flags=0)
     d.update(kw)
     return _HP(**d)
 
@@ -61,8 +61,9 @@ def test_adamw_host_validation():
     assert adamw(hp=None) == NULL
     assert adamw(hp=_hp(), gdt=2) == DTYPE
     assert adamw(hp=_hp(), mdt=1) == DTYPE
+    assert adamw(hp=_hp(), mdt=4) == DTYPE
     for bad in (dict(lr=math.nan), dict(lr=-1.0), dict(lr=math.inf), dict(eps=-1e-8), dict(eps=math.inf),
-                dict(weight_decay=-0.1), dict(step=0), dict(step=-3), dict(reserved=1)):
+                dict(weight_decay=-0.1), dict(step=0), dict(step=-3), dict(flags=4), dict(flags=0x80000000)):
         assert adamw(hp=_hp(**bad)) == HYPER, bad
     for bad in (dict(beta1=1.0), dict(beta1=-0.1), dict(beta2=math.nan), dict(beta2=1.5)):
         assert adamw(hp=_hp(**bad)) == BETA, bad

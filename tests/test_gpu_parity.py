@@ -72,6 +72,33 @@ def test_empty_tensors_and_list(ora):
     mica.mica_adamw_steps([], [], [], [], lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, step=1)
 
 
+@pytest.mark.parametrize("grad", ["f32", "f16"])
+def test_packed_m_float_v(ora, grad):
+    """m packed, v float32 (the moment type of the page's CAdamWBF16 with v16 false)."""
+    base = W["fp16_scaled"] if grad == "f16" else W["gpt2_small_bf16"]
+    wl = dataclasses.replace(base, name=f"packed_m_{grad}", moments="bf16x2_m")
+    r = parity.run_parity(wl, sizes=small_gpt2_sizes() + RAGGED, ora=ora, zero_grad=True)
+    assert r["same_factor_every_step"]
+
+
+@pytest.mark.parametrize("name", ["gpt2_small", "gpt2_small_bf16", "fp16_scaled"])
+def test_adam_coupled_l2(ora, name):
+    """Adam with the coupled L2 term (the page's Adam case) instead of AdamW's decoupled decay."""
+    r = parity.run_parity(W[name], sizes=small_gpt2_sizes() + RAGGED, ora=ora, coupled_l2=True)
+    assert r["same_factor_every_step"]
+
+
+@pytest.mark.parametrize("bad", [float("inf"), float("nan")], ids=["inf", "nan"])
+@pytest.mark.parametrize("name", ["gpt2_small_bf16", "fp16_scaled"])
+def test_skip_step_with_nonfinite_gradient(ora, name, bad):
+    """A step whose gradient overflowed (its norm is not finite) leaves w, m and v as they were; the steps before
+    and after it are normal; zero_grad still zeroes the gradient."""
+    r = parity.run_parity(W[name], sizes=[4096, 333, 70000, 9], ora=ora, steps=4, zero_grad=True,
+                          skip_nonfinite=True, grad_hook=_plant([bad]))
+    g_norm, o_norm, g_factor, o_factor = r["norms"][1]
+    assert not (np.float32(g_factor) > 0) and not (np.float32(o_factor) > 0)
+
+
 def _misaligned_state(wl, sizes, off):
     """Tensors placed `off` elements (or packed words) past a 16-byte boundary: the element-by-element path."""
     st = workloads.make_state(wl, "cuda", sizes=[n + 8 for n in sizes])

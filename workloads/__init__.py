@@ -37,7 +37,7 @@ class Workload:
     name: str
     shapes: tuple
     grad_dtype: str = "f32"        # "f32" or "f16"
-    moments: str = "f32"           # "f32" or "bf16x2" (two BF16 per uint32 word)
+    moments: str = "f32"           # "f32", "bf16x2" (two BF16 per uint32 word) or "bf16x2_m" (m packed, v f32)
     w_std: float = 0.02
     g_std: float = 1e-3
     spike_p: float = 0.0           # probability that a gradient entry is multiplied by spike_mult
@@ -143,7 +143,12 @@ class State:
 
     @property
     def packed(self) -> bool:
+        """Both moments packed."""
         return self.wl.moments == "bf16x2"
+
+    @property
+    def m_packed(self) -> bool:
+        return self.wl.moments in ("bf16x2", "bf16x2_m")
 
 
 def make_state(wl: Workload, device="cpu", sizes=None, seed: int | None = None) -> State:
@@ -157,22 +162,24 @@ def make_state(wl: Workload, device="cpu", sizes=None, seed: int | None = None) 
     w_off, w_len = _layout(sizes, 4)
     g_es = 2 if wl.grad_dtype == "f16" else 4
     g_off, g_len = _layout(sizes, g_es)
-    m_off, m_len = _layout(sizes, 4, packed=packed)
+    m_packed = wl.moments in ("bf16x2", "bf16x2_m")
+    m_off, m_len = _layout(sizes, 4, packed=m_packed)
+    v_off, v_len = _layout(sizes, 4, packed=packed)
     gdt = torch.float16 if wl.grad_dtype == "f16" else torch.float32
-    mdt = torch.int32 if packed else torch.float32  # packed words are stored in int32 tensors (uint32 bits)
+    mdt = torch.int32 if m_packed else torch.float32  # packed words are stored in int32 tensors (uint32 bits)
+    vdt = torch.int32 if packed else torch.float32
 
     w_flat = torch.empty(w_len, dtype=torch.float32, device=device)
     w_flat.normal_(0.0, wl.w_std, generator=_gen(device, _mix(seed, 0xA)))
     g_flat = torch.zeros(g_len, dtype=gdt, device=device)
     m_flat = torch.zeros(m_len, dtype=mdt, device=device)
-    v_flat = torch.zeros(m_len, dtype=mdt, device=device)
+    v_flat = torch.zeros(v_len, dtype=vdt, device=device)
     st = State(wl, device, sizes, w_flat, g_flat, m_flat, v_flat)
-    for n, wo, go, mo in zip(sizes, w_off, g_off, m_off):
-        cnt = (n + 1) // 2 if packed else n
+    for n, wo, go, mo, vo in zip(sizes, w_off, g_off, m_off, v_off):
         st.w.append(w_flat[wo:wo + n])
         st.g.append(g_flat[go:go + n])
-        st.m.append(m_flat[mo:mo + cnt])
-        st.v.append(v_flat[mo:mo + cnt])
+        st.m.append(m_flat[mo:mo + ((n + 1) // 2 if m_packed else n)])
+        st.v.append(v_flat[vo:vo + ((n + 1) // 2 if packed else n)])
     return st
 
 
