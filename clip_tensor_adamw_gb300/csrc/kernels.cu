@@ -161,9 +161,10 @@ __device__ __forceinline__ void adam8(float (&w)[8], const float (&g)[8], float 
     }
 }
 
-// A step to skip: the caller asked to skip steps whose norm was not finite, and the factor is not > 0 (a NaN norm
-// gives a NaN factor, an infinite one a zero factor).
-__device__ __forceinline__ bool skip_step(const StepScalars& s, float f) { return s.skip_nonfinite && !(f > 0.0f); }
+// A step to skip: the caller asked to skip steps whose norm was not finite (kSkip), and the factor is not > 0 (a
+// NaN norm gives a NaN factor, an infinite one a zero factor). Without kSkip the test compiles away.
+template <bool kSkip>
+__device__ __forceinline__ bool skip_step(float f) { return kSkip && !(f > 0.0f); }
 
 // One packed-moment octet's 4 words, element by element (words past the tensor's last element are not read).
 __device__ __forceinline__ void load_words(const void* base, int64_t o, int cnt, uint32_t (&word)[4],
@@ -193,7 +194,7 @@ __device__ __forceinline__ void store_words(void* base, int64_t o, int cnt, cons
 
 // One octet element by element: for bases not aligned for the vectors, and for a tensor's last, partial octet.
 // Elements past n are neither read nor written, nor is the high half of a last packed word that holds no element.
-template <Dtype G, Dtype M, bool kCoupled>
+template <Dtype G, Dtype M, bool kCoupled, bool kSkip>
 __device__ __noinline__ void adam_oct_elements(const TensorRec& r, int64_t o, const StepScalars& s, Factor& fac) {
     using L = MomentLayout<M>;
     const int64_t i0 = o * kOct;
@@ -218,7 +219,7 @@ __device__ __noinline__ void adam_oct_elements(const TensorRec& r, int64_t o, co
     if constexpr (L::kMPacked) load_words(r.m, o, cnt, om, m);
     if constexpr (L::kVPacked) load_words(r.v, o, cnt, ov, v);
     const float f = fac.get();
-    const bool skip = skip_step(s, f);
+    const bool skip = skip_step<kSkip>(f);
     if (!skip) adam8<M, kCoupled>(w, g, m, v, pm, pv, s, f);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -260,7 +261,7 @@ __device__ __forceinline__ void prefetch_octets(const TensorRec& r, int64_t a, i
 // Octets [ob, oe) of one tensor: octet ob + lane first, then every `stride`-th. With `prefetch` (a whole CTA on
 // one slice: lane is the thread index and stride the CTA size) thread 0 asks L2 for the rounds one and two ahead,
 // so that the other threads' loads of those rounds find their data in L2 rather than waiting on DRAM.
-template <Dtype G, Dtype M, bool kCoupled>
+template <Dtype G, Dtype M, bool kCoupled, bool kSkip>
 __device__ __forceinline__ void adam_range(const TensorRec& r, int64_t ob, int64_t oe, int lane, int stride,
                                            const StepScalars& s, Factor& fac, bool prefetch = false) {
     using L = MomentLayout<M>;
@@ -283,7 +284,7 @@ __device__ __forceinline__ void adam_range(const TensorRec& r, int64_t ob, int64
             if constexpr (L::kVPacked) vp = ld16_stream(static_cast<const uint32_t*>(r.v) + 4 * o);
             else ld8_stream(static_cast<const float*>(r.v) + kOct * o, v);
             const float f = fac.get();
-            if (!skip_step(s, f)) {
+            if (!skip_step<kSkip>(f)) {
                 uint32_t pm[4], pv[4];
                 if constexpr (G == kF16) h8_to(gh, g);
                 if constexpr (L::kMPacked) bf8_to(mp, m);
@@ -306,15 +307,15 @@ __device__ __forceinline__ void adam_range(const TensorRec& r, int64_t ob, int64
         }
         // the last, partial octet (n % 8 != 0), when it lies in this range
         if (full < oe && full >= ob && lane == (int)((full - ob) % stride))
-            adam_oct_elements<G, M, kCoupled>(r, full, s, fac);
+            adam_oct_elements<G, M, kCoupled, kSkip>(r, full, s, fac);
     } else {
-        for (int64_t o = ob + lane; o < oe; o += stride) adam_oct_elements<G, M, kCoupled>(r, o, s, fac);
+        for (int64_t o = ob + lane; o < oe; o += stride) adam_oct_elements<G, M, kCoupled, kSkip>(r, o, s, fac);
     }
 }
 
 // One CTA per work item, items taken in reverse order (the norm reads them forwards, so the gradient it read last
 // may still be in L2 when this kernel starts).
-template <Dtype G, Dtype M, bool kCoupled>
+template <Dtype G, Dtype M, bool kCoupled, bool kSkip>
 __global__ void __launch_bounds__(kThreads, 3) adamw_kernel(const TensorRec* __restrict__ recs,
                                                             const WorkItem* __restrict__ items, int32_t num_items,
                                                             int32_t item_octs, StepScalars s,
@@ -328,11 +329,11 @@ __global__ void __launch_bounds__(kThreads, 3) adamw_kernel(const TensorRec* __r
             const TensorRec r = recs[item.t];
             const int64_t no = (r.n + kOct - 1) / kOct;
             const int64_t oe = item.o0 + item_octs < no ? item.o0 + item_octs : no;
-            adam_range<G, M, kCoupled>(r, item.o0, oe, threadIdx.x, kThreads, s, fac, true);
+            adam_range<G, M, kCoupled, kSkip>(r, item.o0, oe, threadIdx.x, kThreads, s, fac, true);
         } else {
             for (int j = warp; j < item.count; j += kWarps) {
                 const TensorRec r = recs[item.t + j];
-                adam_range<G, M, kCoupled>(r, 0, (r.n + kOct - 1) / kOct, lane, 32, s, fac);
+                adam_range<G, M, kCoupled, kSkip>(r, 0, (r.n + kOct - 1) / kOct, lane, 32, s, fac);
             }
         }
     }
@@ -856,7 +857,7 @@ __global__ void __launch_bounds__(kThreads) scale_kernel(const TensorRec* __rest
     }
 }
 
-template <Dtype G, Dtype M, bool kCoupled>
+template <Dtype G, Dtype M, bool kCoupled, bool kSkip>
 cudaError_t launch_adamw_t(const WorkItem* items, const TensorRec* recs, int32_t num_items, int32_t item_octs,
                            cudaStream_t st, const StepScalars& s, const float* d_factor) {
     cudaLaunchConfig_t cfg = {};
@@ -869,14 +870,18 @@ cudaError_t launch_adamw_t(const WorkItem* items, const TensorRec* recs, int32_t
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, adamw_kernel<G, M, kCoupled>, recs, items, num_items, item_octs, s, d_factor);
+    return cudaLaunchKernelEx(&cfg, adamw_kernel<G, M, kCoupled, kSkip>, recs, items, num_items, item_octs, s,
+                              d_factor);
 }
 
 template <Dtype G, Dtype M>
 cudaError_t launch_adamw_c(bool coupled, const WorkItem* items, const TensorRec* recs, int32_t num_items,
                            int32_t item_octs, cudaStream_t st, const StepScalars& s, const float* d_factor) {
-    return coupled ? launch_adamw_t<G, M, true>(items, recs, num_items, item_octs, st, s, d_factor)
-                   : launch_adamw_t<G, M, false>(items, recs, num_items, item_octs, st, s, d_factor);
+    if (s.skip_nonfinite)
+        return coupled ? launch_adamw_t<G, M, true, true>(items, recs, num_items, item_octs, st, s, d_factor)
+                       : launch_adamw_t<G, M, false, true>(items, recs, num_items, item_octs, st, s, d_factor);
+    return coupled ? launch_adamw_t<G, M, true, false>(items, recs, num_items, item_octs, st, s, d_factor)
+                   : launch_adamw_t<G, M, false, false>(items, recs, num_items, item_octs, st, s, d_factor);
 }
 
 template <Dtype G>
