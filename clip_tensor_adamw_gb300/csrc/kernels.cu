@@ -629,18 +629,19 @@ __device__ __forceinline__ void bulk_copy_g2s(void* smem_dst, const void* gmem_s
 // the joint norm: a TMA pipeline over equal contiguous chunks
 // ------------------------------------------------------------------------------------------------------------------
 
-// Each CTA streams its chunk of the list's octets through kNormStages shared-memory stages of 256 octets. One
+// Each CTA streams its chunk of the list's octets through kNormStages shared-memory stages of 512 octets. One
 // producer warp (its lane 0) walks the chunk and, per stage, issues one bulk copy per run of whole octets of an
 // aligned tensor (a stage may cross tensor boundaries), completing on the stage's `full` barrier; the 8 consumer
-// warps wait on it, thread t takes the stage's octet t (from shared memory, or element by element from global
-// memory for a tensor's partial last octet or an unaligned tensor), then each warp arrives on the stage's `empty`
-// barrier so the producer may refill it. The bytes in flight (up to 8 stages x 8 KB per CTA, 3 CTAs per SM) cost
-// shared memory, not registers.
-constexpr int kNormStages = 8;
+// warps wait on it, thread t takes the stage's octets t and t + 256 (from shared memory, or element by element from
+// global memory for a tensor's partial last octet or an unaligned tensor), then each warp arrives on the stage's
+// `empty` barrier so the producer may refill it. The bytes in flight (up to 4 stages x 16 KB per CTA, 3 CTAs per
+// SM) cost shared memory, not registers; two octets per thread and stage halve the per-stage bookkeeping.
+constexpr int kNormStages = 4;
+constexpr int kNormStageOcts = 2 * kThreads;
 constexpr int kNormThreads = kThreads + 32;
 
 template <Dtype G>
-__host__ __device__ constexpr int norm_stage_bytes() { return kThreads * ((G == kF16) ? 16 : 32); }
+__host__ __device__ constexpr int norm_stage_bytes() { return kNormStageOcts * ((G == kF16) ? 16 : 32); }
 
 template <Dtype G>
 size_t norm_smem_bytes() { return (size_t)kNormStages * norm_stage_bytes<G>(); }
@@ -665,7 +666,7 @@ __global__ void __launch_bounds__(kNormThreads, kNormTmaCtasPerSm) norm_tma_kern
     const int64_t c0 = ct.total_octs * blockIdx.x / ct.grid;
     const int64_t c1 = ct.total_octs * (blockIdx.x + 1) / ct.grid;
     const int32_t k0 = ct.first[blockIdx.x];
-    const int64_t nstage = (c1 - c0 + kThreads - 1) / kThreads;
+    const int64_t nstage = (c1 - c0 + kNormStageOcts - 1) / kNormStageOcts;
     if (t == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);          // the producer's arrive (with the stage's byte count)
@@ -684,14 +685,15 @@ __global__ void __launch_bounds__(kNormThreads, kNormTmaCtasPerSm) norm_tma_kern
             pc.init(ct, k0);
             bool ok = true;
             int64_t i = 0;
+            int slot = 0;
+            uint32_t round = 0;  // how many times the ring has wrapped
             for (; i < nstage; ++i) {
-                const int slot = (int)(i % S);
-                if (i >= S && !mbar_wait(&empty[slot], (uint32_t)((i / S - 1) & 1))) {
+                if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1u)) {
                     ok = false;
                     break;
                 }
-                const int64_t a = c0 + i * kThreads;
-                const int64_t b = a + kThreads < c1 ? a + kThreads : c1;
+                const int64_t a = c0 + i * kNormStageOcts;
+                const int64_t b = a + kNormStageOcts < c1 ? a + kNormStageOcts : c1;
                 unsigned char* stage = stages + (size_t)slot * kStageBytes;
                 // the runs of whole octets of aligned tensors in [a, b): counted first, then copied
                 for (int pass = 0; pass < 2; ++pass) {
@@ -716,6 +718,10 @@ __global__ void __launch_bounds__(kNormThreads, kNormTmaCtasPerSm) norm_tma_kern
                         pc = c;
                     }
                 }
+                if (++slot == S) {
+                    slot = 0;
+                    ++round;
+                }
             }
             // every copy this CTA issued has landed before it may exit: wait for each slot's last use
             const int64_t from = i > S ? i - S : 0;
@@ -728,19 +734,15 @@ __global__ void __launch_bounds__(kNormThreads, kNormTmaCtasPerSm) norm_tma_kern
         Cursor cc;
         cc.init(ct, k0);
         bool ok = true;
-        for (int64_t i = 0; i < nstage; ++i) {
-            const int slot = (int)(i % S);
-            if (!mbar_wait(&full[slot], (uint32_t)((i / S) & 1))) {
-                ok = false;
-                break;
-            }
-            const int64_t o = c0 + i * kThreads + t;
-            float x[8];
+        int slot = 0;
+        uint32_t phase = 0;
+        // octet o of the list, at position pos of the current stage
+        auto read_octet = [&](int64_t o, int pos, float (&x)[8]) {
             if (o < c1) {
                 cc.advance(ct, o);
                 const int64_t local = o - cc.lo;
                 if (cc.vec && local < cc.full) {
-                    const unsigned char* src = stages + (size_t)slot * kStageBytes + (size_t)t * kOctBytes;
+                    const unsigned char* src = stages + (size_t)slot * kStageBytes + (size_t)pos * kOctBytes;
                     const float4 p0 = *reinterpret_cast<const float4*>(src);
                     if constexpr (G == kF16) {
                         h8_to(*reinterpret_cast<const uint4*>(&p0), x);
@@ -756,9 +758,24 @@ __global__ void __launch_bounds__(kNormThreads, kNormTmaCtasPerSm) norm_tma_kern
 #pragma unroll
                 for (int j = 0; j < 8; ++j) x[j] = 0.0f;
             }
+        };
+        for (int64_t i = 0; i < nstage; ++i) {
+            if (!mbar_wait(&full[slot], phase)) {
+                ok = false;
+                break;
+            }
+            const int64_t a = c0 + i * kNormStageOcts;
+            float x0[8], x1[8];
+            read_octet(a + t, t, x0);
+            read_octet(a + t + kThreads, t + kThreads, x1);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);  // this warp is done reading the stage
-            acc.add8<kScaled>(x, inv_scale);
+            acc.add8<kScaled>(x0, inv_scale);
+            acc.add8<kScaled>(x1, inv_scale);
+            if (++slot == S) {
+                slot = 0;
+                phase ^= 1u;
+            }
         }
         mine = acc.total();
         if (!acc.exact(mine)) mine = sumsq_chunk_double<G>(ct, k0, c0, c1, kScaled ? inv_scale : 1.0f);
