@@ -78,6 +78,13 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.ora_adam_steps_flags.argtypes = [_P, _P, _P, _P, _I64P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                          ctypes.POINTER(_Scalars), ctypes.c_float, ctypes.c_int32, ctypes.c_uint32]
     lib.ora_adam_steps_flags.restype = None
+    lib.ora_adam_steps_grouped.argtypes = [_P, _P, _P, _P, _I64P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                           _P, ctypes.POINTER(_Scalars), ctypes.c_float, ctypes.c_int32,
+                                           ctypes.c_uint32]
+    lib.ora_adam_steps_grouped.restype = None
+    lib.ora_sgd_steps.argtypes = [_P, _P, _P, _I64P, ctypes.c_int32, ctypes.c_int32, ctypes.c_double,
+                                  ctypes.c_double, ctypes.c_float, ctypes.c_int32, ctypes.c_uint32]
+    lib.ora_sgd_steps.restype = None
     lib.ora_clip_grad_norms.argtypes = [_P, _I64P, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, ctypes.c_float,
                                         ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float),
                                         ctypes.POINTER(ctypes.c_double)]
@@ -217,6 +224,49 @@ class Oracle:
         fn = self.lib.ora_adamw_steps if decoupled else self.lib.ora_adam_l2_steps
         fn(_ptrs(ws), _ptrs(gs), _ptrs(ms), _ptrs(vs), _sizes([w.size for w in ws]), T, gdt, mdt, ctypes.byref(s),
            np.float32(factor), int(bool(zero_grad)))
+
+    def adamw_steps_grouped(self, ws, gs, ms, vs, group, hps, factor: float = 1.0, zero_grad: bool = False,
+                            decoupled: bool = True, skip_nonfinite: bool = False) -> None:
+        """As ``adamw_steps`` over a list split into parameter groups: tensor k steps with ``hps[group[k]]``."""
+        T = len(ws)
+        if T == 0:
+            return
+        assert len(group) == T and all(0 <= int(x) < len(hps) for x in group)
+        gdt, mdt = _gdt(gs[0]), _mdt(ms[0], vs[0])
+        for w, g, m, v in zip(ws, gs, ms, vs):
+            assert w.dtype == np.float32 and w.flags.c_contiguous and g.size == w.size
+            half = (w.size + 1) // 2
+            assert m.size == (half if mdt in (BF16X2, BF16X2_M) else w.size)
+            assert v.size == (half if mdt == BF16X2 else w.size)
+        ss = (_Scalars * len(hps))(*[self._scalars_struct(hp) for hp in hps])
+        grp = np.ascontiguousarray(group, dtype=np.int32)
+        flags = (SKIP_NONFINITE if skip_nonfinite else 0) | (0 if decoupled else COUPLED_L2)
+        self.lib.ora_adam_steps_grouped(_ptrs(ws), _ptrs(gs), _ptrs(ms), _ptrs(vs), _sizes([w.size for w in ws]), T,
+                                        gdt, mdt, grp.ctypes.data, ss, np.float32(factor), int(bool(zero_grad)),
+                                        flags)
+
+    # ---- SGD and SGD with momentum ----
+    def sgd_steps(self, ws, gs, bufs, lr: float, momentum: float = 0.0, factor: float = 1.0,
+                  zero_grad: bool = False, skip_nonfinite: bool = False) -> None:
+        """In place; ``bufs`` None is plain SGD, else one float32 momentum buffer per tensor."""
+        T = len(ws)
+        if T == 0:
+            return
+        gdt = _gdt(gs[0])
+        for k, (w, g) in enumerate(zip(ws, gs)):
+            assert w.dtype == np.float32 and w.flags.c_contiguous and g.size == w.size
+            if bufs is not None:
+                assert bufs[k].dtype == np.float32 and bufs[k].size == w.size
+        self.lib.ora_sgd_steps(_ptrs(ws), _ptrs(gs), None if bufs is None else _ptrs(bufs),
+                               _sizes([w.size for w in ws]), T, gdt, float(lr), float(momentum), np.float32(factor),
+                               int(bool(zero_grad)), SKIP_NONFINITE if skip_nonfinite else 0)
+
+    def clip_sgd_step(self, ws, gs, bufs, lr: float, momentum: float, max_norm: float, inv_scale: float = 1.0,
+                      zero_grad: bool = False, skip_nonfinite: bool = False):
+        """Norm, clip factor, then SGD (or SGD with momentum) over every tensor. Returns ``(norm, factor)``."""
+        norm, factor, _ = self.clip_grad_norms(gs, max_norm, inv_scale)
+        self.sgd_steps(ws, gs, bufs, lr, momentum, factor=factor, zero_grad=zero_grad, skip_nonfinite=skip_nonfinite)
+        return norm, factor
 
     # ---- ScaleTensors ----
     def scale_tensors(self, ts, factor: float) -> None:

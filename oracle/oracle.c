@@ -12,7 +12,8 @@
  *           multiplies every cell of several tensors by one factor (the unscaling of a float16 step).
  *   [OPT]   BendTorch "main.bend", section "Optimizers": AdamW element by element in PyTorch's order of
  *           operations, the gradient written back as zero, c1 = 1 - b1 and c2 = 1 - b2 taken as constants of
- *           their own.
+ *           their own; the same section's plain SGD (w + (-lr) g) and SGD with momentum (b = b mu + g,
+ *           w + (-lr) b), both as PyTorch's SGD without weight decay, dampening or Nesterov.
  *   [BF16]  BendTorch "main.bend", section "Optimizers", part "AdamW over packed BF16 moments (CAdamWBF16)": BF16
  *           rounding to nearest-even with NaN -> 0xFFFF, element 2k in the low half of word k, and the weight update
  *           reading the rounded moments.
@@ -30,6 +31,8 @@
  *   - The clip coefficient is PyTorch's clip_grad_norm_: f32(max_norm) / f32(norm + f32(1e-6)), clamped at 1 with
  *     a NaN passed through. The unscale and the clip fold into one factor f32(inv_scale * clip) that multiplies g
  *     inside the update; the gradient is never rewritten by the clip.
+ *   - Parameter groups (PyTorch's param_groups: a list split into groups with their own lr and weight decay, e.g.
+ *     no decay on biases and norm gains) step every tensor exactly as a call over its group alone would.
  *
  * Build with -O2 -ffp-contract=off and without -ffast-math: every float operation below rounds on its own, with no
  * fused multiply-add, exactly in the order written.
@@ -308,6 +311,64 @@ void ora_adam_steps_flags(float* const* w, void* const* g, void* const* m, void*
     for (int32_t k = 0; k < T; ++k) {
         if (!skip) {
             ora_adam_group(w[k], g[k], m[k], v[k], n[k], gdt, mdt, s, factor, zero_grad, decoupled);
+        } else if (zero_grad) {
+            for (int64_t i = 0; i < n[k]; ++i) {
+                if (gdt == ORA_F16) ((uint16_t*)g[k])[i] = 0;
+                else ((float*)g[k])[i] = 0.0f;
+            }
+        }
+    }
+}
+
+/* The Adam family over a list split into parameter groups: tensor k steps with the scalars s[group[k]] (group ==
+ * NULL: every tensor in group 0), and the options of `flags` as in ora_adam_steps_flags. */
+void ora_adam_steps_grouped(float* const* w, void* const* g, void* const* m, void* const* v, const int64_t* n,
+                            int32_t T, int32_t gdt, int32_t mdt, const int32_t* group, const ora_scalars* s,
+                            float factor, int32_t zero_grad, uint32_t flags) {
+    for (int32_t k = 0; k < T; ++k) {
+        const ora_scalars* sk = group ? &s[group[k]] : &s[0];
+        ora_adam_steps_flags(&w[k], &g[k], &m[k], &v[k], &n[k], 1, gdt, mdt, sk, factor, zero_grad, flags);
+    }
+}
+
+/* ------------------------------------------------------------------------------------------------------------ */
+/* SGD and SGD with momentum [OPT]                                                                                */
+/* ------------------------------------------------------------------------------------------------------------ */
+
+/* One group of the page's two plain optimizers, with PyTorch's SGD arithmetic (no weight decay, dampening or
+ * Nesterov). lr and mu arrive as float32. Element by element, each float operation rounded on its own:
+ *   gh = g * factor                        (unscale and clip, folded)
+ *   buf == NULL (SGD):       w = w + (-lr) * gh
+ *   buf != NULL (momentum):  b = b * mu + gh;  w = w + (-lr) * b;  buf = b
+ *   g = 0                                  (when zero_grad) */
+void ora_sgd_group(float* w, void* g, float* buf, int64_t n, int32_t gdt, float lr, float mu, float factor,
+                   int32_t zero_grad) {
+    float neg_lr = -lr;
+    for (int64_t i = 0; i < n; ++i) {
+        float gh = grad_at(g, gdt, i) * factor;
+        if (buf) {
+            float b = buf[i] * mu + gh;
+            buf[i] = b;
+            w[i] = w[i] + neg_lr * b;
+        } else {
+            w[i] = w[i] + neg_lr * gh;
+        }
+        if (zero_grad) {
+            if (gdt == ORA_F16) ((uint16_t*)g)[i] = 0;
+            else ((float*)g)[i] = 0.0f;
+        }
+    }
+}
+
+/* SGD (buf == NULL) or SGD with momentum over a list; lr and mu are rounded once to float32, as PyTorch passes its
+ * Python-float scalars to float32 arithmetic. Bit 0 of `flags` skips the update when the factor is not > 0, as in
+ * ora_adam_steps_flags (only the gradient is then zeroed, when zero_grad). */
+void ora_sgd_steps(float* const* w, void* const* g, float* const* buf, const int64_t* n, int32_t T, int32_t gdt,
+                   double lr, double mu, float factor, int32_t zero_grad, uint32_t flags) {
+    const int skipped = (flags & 1u) && !(factor > 0.0f);
+    for (int32_t k = 0; k < T; ++k) {
+        if (!skipped) {
+            ora_sgd_group(w[k], g[k], buf ? buf[k] : 0, n[k], gdt, (float)lr, (float)mu, factor, zero_grad);
         } else if (zero_grad) {
             for (int64_t i = 0; i < n[k]; ++i) {
                 if (gdt == ORA_F16) ((uint16_t*)g[k])[i] = 0;

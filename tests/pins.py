@@ -6,10 +6,11 @@ the oracle with one plausible mistake planted each and requires every planted mi
 
 What the pins hold the oracle to (no pin re-types the oracle's own formula):
 
-* library routines: PyTorch's CPU ``torch.optim.AdamW`` / ``torch.optim.Adam`` and ``clip_grad_norm_``, PyTorch's
+* library routines: PyTorch's CPU ``torch.optim.AdamW`` / ``torch.optim.Adam`` (also with two param_groups),
+  ``torch.optim.SGD`` (plain and with momentum), ``GradScaler`` and ``clip_grad_norm_``, PyTorch's
   float32 -> bfloat16 conversion, numpy's binary16 conversions, Python's exactly rounded ``math.fsum``;
-* closed forms: the first step from zero moments, a constant gradient over many steps, norms of all-ones and
-  Pythagorean vectors, and the b1 = b2 = eps = 0 step whose weight update is lr * m / sqrt(v) of rounded moments;
+* closed forms: the first step from zero moments, a constant gradient over many steps (also for SGD and momentum in
+  dyadic values, where every operation is exact), norms of all-ones and Pythagorean vectors, and the b1 = b2 = eps = 0 step whose weight update is lr * m / sqrt(v) of rounded moments;
 * the pages' printed values (``tests/golden/printed_values.txt``): the F32 rounding of 1 - 0.999 and the BF16 codes
   of NaN and zero;
 * invariants: one call over a list equals one call per group; zero_grad zeroes exactly the gradient; a factor of
@@ -494,6 +495,161 @@ def pin_skip_nonfinite_vs_gradscaler(o: oracle.Oracle) -> None:
     _close(v, st["exp_avg_sq"].numpy(), 2e-5, 1e-16)
 
 
+# ------------------------------------------------------------------------------------------------------------------
+# parameter groups
+# ------------------------------------------------------------------------------------------------------------------
+
+def pin_torch_adamw_param_groups(o: oracle.Oracle) -> None:
+    """Five steps of clip + AdamW over two parameter groups (matrices: lr 6e-4, weight decay 0.1; vectors: lr 3e-4,
+    no decay) against PyTorch's CPU AdamW given the same two param_groups."""
+    rng = _rng(15)
+    sizes = [(24, 16), (16,), (16, 40), (40,), (7,)]
+    ns = [int(np.prod(s)) for s in sizes]
+    group = [0 if len(s) == 2 else 1 for s in sizes]
+    hps = [dict(HP0), dict(HP0, lr=3e-4, weight_decay=0.0)]
+    ws = [rng.normal(0, 0.02, size=n).astype(np.float32) for n in ns]
+    steps = [[rng.normal(0, 0.05, size=n).astype(np.float32) for n in ns] for _ in range(5)]
+    ps = [torch.nn.Parameter(torch.from_numpy(w.copy())) for w in ws]
+    opt = torch.optim.AdamW(
+        [{"params": [p for p, gr in zip(ps, group) if gr == j], "lr": hps[j]["lr"],
+          "weight_decay": hps[j]["weight_decay"]} for j in range(2)],
+        betas=(HP0["beta1"], HP0["beta2"]), eps=HP0["eps"], foreach=False, fused=False)
+    max_norm = 0.5
+    for gs in steps:
+        for p, g in zip(ps, gs):
+            p.grad = torch.from_numpy(g.copy())
+        torch.nn.utils.clip_grad_norm_(ps, max_norm, foreach=False)
+        opt.step()
+    w = [x.copy() for x in ws]
+    m = [np.zeros(n, np.float32) for n in ns]
+    v = [np.zeros(n, np.float32) for n in ns]
+    for t, gs in enumerate(steps, start=1):
+        gs = [g.copy() for g in gs]
+        _, factor, _ = o.clip_grad_norms(gs, max_norm)
+        o.adamw_steps_grouped(w, gs, m, v, group, [Hyper(step=t, **hp) for hp in hps], factor=factor)
+    for k, p in enumerate(ps):
+        _close(w[k], p.detach().numpy(), 1e-6, 1e-7)
+        st = opt.state[p]
+        _close(m[k], st["exp_avg"].numpy(), 2e-5, 1e-5 * np.abs(st["exp_avg"].numpy()).max())
+        _close(v[k], st["exp_avg_sq"].numpy(), 2e-5, 1e-5 * np.abs(st["exp_avg_sq"].numpy()).max())
+
+
+# ------------------------------------------------------------------------------------------------------------------
+# SGD and SGD with momentum
+# ------------------------------------------------------------------------------------------------------------------
+
+def _torch_sgd(ws, gs_per_step, lr, momentum, max_norm, inv_scale, factors=None):
+    """PyTorch's CPU SGD (foreach=False). With ``factors`` each step's gradient is handed over already multiplied by
+    that step's factor (float32 product) and not clipped; otherwise it is unscaled and clipped by clip_grad_norm_."""
+    ps = [torch.nn.Parameter(torch.from_numpy(w.copy())) for w in ws]
+    opt = torch.optim.SGD(ps, lr=lr, momentum=momentum, foreach=False)
+    for t, gs in enumerate(gs_per_step):
+        for p, g in zip(ps, gs):
+            if factors is None:
+                p.grad = torch.from_numpy(g.astype(np.float32)) * inv_scale
+            else:
+                p.grad = torch.from_numpy(g.astype(np.float32) * np.float32(factors[t]))
+        if factors is None:
+            torch.nn.utils.clip_grad_norm_(ps, max_norm, foreach=False)
+        opt.step()
+    bufs = [opt.state[p].get("momentum_buffer") for p in ps]
+    return [p.detach().numpy().copy() for p in ps], [None if b is None else b.numpy().copy() for b in bufs]
+
+
+def pin_torch_sgd(o: oracle.Oracle) -> None:
+    """Six steps of SGD, and of SGD with momentum 0.9, against PyTorch's CPU SGD, with float32 and with loss-scaled
+    float16 gradients. Given the same folded factor, the momentum buffers agree exactly and the weights to a few
+    float32 ulps (PyTorch's w + (-lr) b may round once, as a fused multiply-add, where the page rounds twice). The
+    whole clip + step agrees within float32 rounding with clip_grad_norm_ (whose coefficient PyTorch takes as
+    max_norm * (1 / d), one ulp away from the quotient at times)."""
+    rng = _rng(16)
+    sizes = [33, 1, 300, 64]
+    for gkind in ("f32", "f16"):
+        for mom in (0.0, 0.9):
+            ws = [rng.normal(0, 0.02, size=n).astype(np.float32) for n in sizes]
+            steps = []
+            for t in range(6):
+                if gkind == "f16":
+                    steps.append([(rng.normal(0, 1e-3, size=n) * 65536).astype(np.float16) for n in sizes])
+                else:
+                    steps.append([rng.normal(0, 0.05 if t % 2 else 1e-3, size=n).astype(np.float32) for n in sizes])
+            inv = 2.0 ** -16 if gkind == "f16" else 1.0
+            factors = [o.clip_grad_norms([g.copy() for g in gs], 0.3, inv)[1] for gs in steps]
+            tw, tb = _torch_sgd(ws, steps, 0.05, mom, 0.3, inv, factors=factors)
+            cw, cb = _torch_sgd(ws, steps, 0.05, mom, 0.3, inv)
+            w = [x.copy() for x in ws]
+            bufs = [np.zeros(n, np.float32) for n in sizes] if mom else None
+            for gs, f in zip(steps, factors):
+                o.sgd_steps(w, [g.copy() for g in gs], bufs, 0.05, mom, factor=f)
+            w2 = [x.copy() for x in ws]
+            bufs2 = [np.zeros(n, np.float32) for n in sizes] if mom else None
+            for gs in steps:
+                o.clip_sgd_step(w2, [g.copy() for g in gs], bufs2, 0.05, mom, 0.3, inv)
+            for k in range(len(sizes)):
+                _close(w[k], tw[k], 8 * 2.0 ** -24, 1e-9)
+                # the coefficient's ulp reaches the weights through up to ~60 lr-sized updates: 1e-6 of their sum
+                _close(w2[k], cw[k], 8 * 2.0 ** -24, 2e-8)
+                if mom:
+                    np.testing.assert_array_equal(bufs[k], tb[k])
+                    # relative to the tensor's scale: b * mu + gh may cancel to a value with few significant bits
+                    _close(bufs2[k], cb[k], 8 * 2.0 ** -24, 1e-6 * np.abs(cb[k]).max())
+
+
+def pin_sgd_dyadic_closed_form(o: oracle.Oracle) -> None:
+    """Dyadic values, where every float32 operation is exact: a constant gradient g, lr = 1/8, momentum 1/2 and a
+    folded factor of 1/2 give b_t = gh (2 - 2^(1-t)) and w_t = w_0 - lr gh sum_j (2 - 2^(1-j)) with gh = g/2;
+    plain SGD gives w_t = w_0 - t lr gh."""
+    g = np.array([0.25, -0.5, 1.0, 0.0, -2.0], np.float32)
+    w0 = np.array([1.0, -1.0, 0.5, 2.0, 0.0], np.float32)
+    lr, mu, factor = 0.125, 0.5, 0.5
+    gh = g.astype(np.float64) * factor
+    for mom in (False, True):
+        w = w0.copy()
+        b = np.zeros(g.size, np.float32) if mom else None
+        for t in range(1, 7):
+            gg = g.copy()
+            o.sgd_steps([w], [gg], None if b is None else [b], lr, mu if mom else 0.0, factor=factor, zero_grad=True)
+            assert not gg.any()
+            if mom:
+                bt = gh * (2.0 - 2.0 ** (1 - t))
+                np.testing.assert_array_equal(b, bt.astype(np.float32))
+                acc = sum(2.0 - 2.0 ** (1 - j) for j in range(1, t + 1))
+            else:
+                acc = float(t)
+            np.testing.assert_array_equal(w, (w0.astype(np.float64) - lr * gh * acc).astype(np.float32))
+
+
+def pin_sgd_skip_vs_gradscaler(o: oracle.Oracle) -> None:
+    """SGD with momentum under PyTorch's GradScaler: the step whose scaled gradient overflowed is skipped (w and the
+    momentum buffer unchanged), the next one taken on the unscaled gradient."""
+    rng = _rng(17)
+    n = 48
+    w0 = rng.normal(0, 0.02, size=n).astype(np.float32)
+    grads = [rng.normal(0, 1e-2, size=n).astype(np.float32) for _ in range(3)]
+    grads[1][7] = np.inf
+    p = torch.nn.Parameter(torch.from_numpy(w0.copy()))
+    opt = torch.optim.SGD([p], lr=0.1, momentum=0.9, foreach=False)
+    scaler = torch.amp.GradScaler("cpu", init_scale=512.0, growth_interval=1000)
+    scales = []
+    for gnp in grads:
+        scales.append(scaler.get_scale())
+        opt.zero_grad()
+        scaler.scale((p * torch.from_numpy(gnp)).sum()).backward()
+        scaler.step(opt)
+        scaler.update()
+    w = w0.copy()
+    b = np.zeros(n, np.float32)
+    for j, (gnp, sc) in enumerate(zip(grads, scales)):
+        g_scaled = (gnp.astype(np.float64) * sc).astype(np.float32)
+        w_before, b_before = w.copy(), b.copy()
+        o.clip_sgd_step([w], [g_scaled], [b], 0.1, 0.9, np.inf, 1.0 / sc, zero_grad=True, skip_nonfinite=True)
+        if j == 1:
+            np.testing.assert_array_equal(w, w_before)
+            np.testing.assert_array_equal(b, b_before)
+    _close(w, p.detach().numpy(), 8 * 2.0 ** -24, 1e-9)
+    np.testing.assert_array_equal(b, opt.state[p]["momentum_buffer"].numpy())
+
+
 def read_golden(name: str) -> dict:
     out = {}
     with open(os.path.join(GOLDEN, name)) as f:
@@ -525,4 +681,5 @@ ALL_PINS = [
     pin_torch_adamw, pin_torch_adam_l2, pin_first_step_closed_form, pin_constant_gradient,
     pin_packed_reads_rounded_moments, pin_odd_tail_untouched, pin_zero_grad, pin_list_equals_groups,
     pin_scale_tensors, pin_printed_beta_rounding, pin_packed_m_float_v, pin_skip_nonfinite_vs_gradscaler,
+    pin_torch_adamw_param_groups, pin_torch_sgd, pin_sgd_dyadic_closed_form, pin_sgd_skip_vs_gradscaler,
 ]

@@ -38,7 +38,10 @@ MUTATIONS = {
     "clip_not_clamped": ("float clip = (coef > 1.0f) ? 1.0f : coef;", "float clip = coef;"),
     "clip_eps_dropped": ("float denom = norm + 1e-6f;", "float denom = norm;"),
     "c2_taken_in_f32": ("s->c2 = (float)(1.0 - b2);", "s->c2 = 1.0f - (float)b2;"),
-    "zero_grad_ignored": ("        if (zero_grad) {\n", "        if (0) {\n"),
+    "zero_grad_ignored": ("w[i] = wdec + (neg_step * m_new) / denom;\n\n        if (zero_grad) {\n",
+                          "w[i] = wdec + (neg_step * m_new) / denom;\n\n        if (0) {\n"),
+    "sgd_zero_grad_ignored": ("w[i] = w[i] + neg_lr * gh;\n        }\n        if (zero_grad) {",
+                              "w[i] = w[i] + neg_lr * gh;\n        }\n        if (0) {"),
     "f16_exponent_bias": ("mag = ldexpf((float)(f | 0x400), e - 25);", "mag = ldexpf((float)(f | 0x400), e - 24);"),
     "f16_round_down": ("if (rem > half || (rem == half && (kept & 1u))) kept += 1u;", ";"),
     "scale_ignores_factor": ("p[i] = p[i] * factor;", "p[i] = p[i];"),
@@ -46,6 +49,15 @@ MUTATIONS = {
                               "const int v_packed = (mdt == ORA_BF16X2 || mdt == ORA_BF16X2_M);"),
     "skip_ignored": ("const int skip = (flags & 1u) && !(factor > 0.0f);", "const int skip = 0;"),
     "skip_on_finite": ("const int skip = (flags & 1u) && !(factor > 0.0f);", "const int skip = (flags & 1u);"),
+    "groups_ignored": ("const ora_scalars* sk = group ? &s[group[k]] : &s[0];", "const ora_scalars* sk = &s[0];"),
+    "sgd_sign": ("float neg_lr = -lr;", "float neg_lr = lr;"),
+    "sgd_momentum_dropped": ("float b = buf[i] * mu + gh;", "float b = gh;"),
+    "sgd_momentum_not_decayed": ("float b = buf[i] * mu + gh;", "float b = buf[i] + gh;"),
+    "sgd_w_reads_gradient": ("w[i] = w[i] + neg_lr * b;", "w[i] = w[i] + neg_lr * gh;"),
+    "sgd_buffer_not_stored": ("buf[i] = b;", ";"),
+    "sgd_ignores_factor": ("float gh = grad_at(g, gdt, i) * factor;\n        if (buf) {",
+                           "float gh = grad_at(g, gdt, i);\n        if (buf) {"),
+    "sgd_skip_ignored": ("const int skipped = (flags & 1u) && !(factor > 0.0f);", "const int skipped = 0;"),
     "odd_tail_clobbered": ("if (i & 1) return (word & 0x0000FFFFu) | ((uint32_t)h << 16);\n    return (word & 0xFFFF0000u) | (uint32_t)h;",
                            "if (i & 1) return (word & 0x0000FFFFu) | ((uint32_t)h << 16);\n    return (uint32_t)h;"),
 }
