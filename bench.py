@@ -44,18 +44,25 @@ PROFILE = os.path.join(ROOT, "profiles", "adamw_gpt2_small.md")
 # the byte model: algorithmic bytes per parameter
 # ----------------------------------------------------------------------------------------------------------------
 
-def adamw_bytes_per_param(wl: workloads.Workload, zero_grad: bool = False) -> float:
-    """AdamW kernel: w read + write (8), g read (4 or 2), m and v read + write (16 float32, 8 packed BF16); the
-    gradient's zero write (4 or 2) only with zero_grad. 28 B/param with float32 moments, 20 with packed ones."""
+def adamw_bytes_per_param(wl: workloads.Workload, zero_grad: bool = False, opt: str = "adamw") -> float:
+    """The update kernel. AdamW: w read + write (8), g read (4 or 2), m and v read + write (16 float32, 8 packed
+    BF16): 28 B/param with float32 moments, 20 with packed ones. SGD: w (8) and g; with momentum also the buffer's
+    read + write (8). The gradient's zero write (4 or 2) only with zero_grad."""
     g = 2.0 if wl.grad_dtype == "f16" else 4.0
-    mv = {"bf16x2": 8.0, "bf16x2_m": 12.0}.get(wl.moments, 16.0)
+    if opt == "sgd":
+        mv = 0.0
+    elif opt == "momentum":
+        mv = 8.0
+    else:
+        mv = {"bf16x2": 8.0, "bf16x2_m": 12.0}.get(wl.moments, 16.0)
     return 8.0 + g + mv + (g if zero_grad else 0.0)
 
 
-def step_bytes_per_param(wl: workloads.Workload, zero_grad: bool = False) -> float:
-    """The whole step: the norm's read of g plus the AdamW kernel (28 / 20 B + 4 B with float32 gradients)."""
+def step_bytes_per_param(wl: workloads.Workload, zero_grad: bool = False, opt: str = "adamw") -> float:
+    """The whole step: the norm's read of g plus the update kernel (AdamW: 28 / 20 B + 4 B with float32
+    gradients)."""
     g = 2.0 if wl.grad_dtype == "f16" else 4.0
-    return g + adamw_bytes_per_param(wl, zero_grad)
+    return g + adamw_bytes_per_param(wl, zero_grad, opt)
 
 
 def describe(wl: workloads.Workload) -> str:
@@ -231,9 +238,20 @@ def job_value(world: int, params: int, steps: int, total_ms: float) -> float:
     return world * params * steps / (total_ms / 1e3)
 
 
+def decay_groups(wl: workloads.Workload):
+    """Parameter groups of a transformer's usual split: matrices decay (group 0); vectors do not and take half the
+    lr (group 1)."""
+    group = [0 if len(s) >= 2 else 1 for s in wl.shapes]
+    return group, [dict(lr=wl.lr, weight_decay=wl.weight_decay), dict(lr=wl.lr / 2, weight_decay=0.0)]
+
+
+SGD_LR, SGD_MOMENTUM = 0.1, 0.9
+
+
 def measure(wl: workloads.Workload, steps: int, warmup: int, zero_grad: bool, dist=None, sampler=None,
-            coupled_l2: bool = False):
-    """Times `steps` steps of the whole hot path on the device (inputs resident). Returns a dict of figures."""
+            coupled_l2: bool = False, opt: str = "adamw"):
+    """Times `steps` steps of the whole hot path on the device (inputs resident): the norm and clip factor, then the
+    update (``opt``: "adamw", "adamw_groups", "sgd" or "momentum"). Returns a dict of figures."""
     import clip_tensor_adamw_gb300 as mica
     st = workloads.make_state(wl, "cuda")
     workloads.fill_grad(st, 1)
@@ -247,11 +265,28 @@ def measure(wl: workloads.Workload, steps: int, warmup: int, zero_grad: bool, di
               zero_grad=zero_grad, factor=factor, coupled_l2=coupled_l2)
     stream = torch.cuda.current_stream()
 
+    if opt == "adamw_groups":
+        group, hps = decay_groups(wl)
+        gi = mica.GroupIndex(group)
+        gkw = dict(beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps, zero_grad=zero_grad, factor=factor)
+
+        def update(t):
+            mica.mica_adamw_steps_grouped(W, G, M, V, gi, hps, step=t, **gkw)
+    elif opt in ("sgd", "momentum"):
+        B = M if opt == "momentum" else None
+        mu = SGD_MOMENTUM if opt == "momentum" else 0.0
+
+        def update(t):
+            mica.mica_sgd_steps(W, G, B, lr=SGD_LR, momentum=mu, zero_grad=zero_grad, factor=factor)
+    else:
+        def update(t):
+            mica.mica_adamw_steps(W, G, M, V, step=t, **kw)
+
     def step(t, ev_mid=None):
         mica.mica_clip_grad_norms(G, wl.max_norm, wl.inv_scale, norm_out=norm, factor_out=factor)
         if ev_mid is not None:
             ev_mid.record(stream)
-        mica.mica_adamw_steps(W, G, M, V, step=t, **kw)
+        update(t)
 
     for t in range(1, warmup + 1):
         step(t)
@@ -419,23 +454,29 @@ def main():
                                "hbm_gbs_model": P * step_bytes_per_param(wl) / (zg["ms_per_step"] / 1e3) / 1e9,
                                "hbm_gbs_actual": P * step_bytes_per_param(wl, True) / (zg["ms_per_step"] / 1e3) / 1e9,
                                "bytes_per_param_actual": step_bytes_per_param(wl, True)}
-        others = [(n, workloads.WORKLOADS[n], False) for n in ("gpt2_small_bf16", "gpt2_xl", "fp16_scaled", "tiny")]
-        others += [("gpt2_small_bf16_m", dataclasses.replace(workloads.WORKLOADS["gpt2_small"],
-                                                             name="gpt2_small_bf16_m", moments="bf16x2_m"), False),
-                   ("gpt2_small_adam_l2", workloads.WORKLOADS["gpt2_small"], True)]
-        for other, owl, coupled in others:
+        small = workloads.WORKLOADS["gpt2_small"]
+        others = [(n, workloads.WORKLOADS[n], False, "adamw")
+                  for n in ("gpt2_small_bf16", "gpt2_xl", "fp16_scaled", "tiny")]
+        others += [("gpt2_small_bf16_m", dataclasses.replace(small, name="gpt2_small_bf16_m", moments="bf16x2_m"),
+                    False, "adamw"),
+                   ("gpt2_small_adam_l2", small, True, "adamw"),
+                   ("gpt2_small_param_groups", small, False, "adamw_groups"),
+                   ("gpt2_small_sgd", small, False, "sgd"),
+                   ("gpt2_small_sgd_momentum", small, False, "momentum")]
+        for other, owl, coupled, opt in others:
             if other == wl.name:
                 continue
             k = 40 if other == "gpt2_xl" else max(20, args.steps // 4)
-            f, _ = measure(owl, k, args.warmup, zero_grad=False, coupled_l2=coupled)
+            f, _ = measure(owl, k, args.warmup, zero_grad=False, coupled_l2=coupled, opt=opt)
             torch.cuda.empty_cache()
+            bpp = step_bytes_per_param(owl, opt=opt)
             extras[other] = {"params": owl.params, "ms_per_step": f["ms_per_step"],
                              "params_per_s": owl.params / (f["ms_per_step"] / 1e3),
-                             "hbm_gbs": owl.params * step_bytes_per_param(owl) / (f["ms_per_step"] / 1e3) / 1e9,
-                             "pct_of_8tbs": 100 * owl.params * step_bytes_per_param(owl) /
-                             (f["ms_per_step"] / 1e3) / 1e9 / NOMINAL_HBM_GBS,
-                             "adamw_ms": f["adamw_ms"], "clip_ms": f["clip_ms"],
-                             "bytes_per_param": step_bytes_per_param(owl)}
+                             "hbm_gbs": owl.params * bpp / (f["ms_per_step"] / 1e3) / 1e9,
+                             "pct_of_8tbs": 100 * owl.params * bpp / (f["ms_per_step"] / 1e3) / 1e9 / NOMINAL_HBM_GBS,
+                             "update_ms": f["adamw_ms"], "clip_ms": f["clip_ms"], "bytes_per_param": bpp,
+                             "update_gbs": owl.params * adamw_bytes_per_param(owl, opt=opt) / (f["adamw_ms"] / 1e3)
+                             / 1e9}
         ms, h2d, d2h = measure_e2e(wl, max(20, args.steps // 4), args.warmup)
         e2e = {"value": P / (ms / 1e3), "unit": "params/s", "ms_per_step": ms, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h}

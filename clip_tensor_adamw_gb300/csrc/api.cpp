@@ -139,7 +139,7 @@ struct Span {
 };
 
 static const char* span_name(int32_t kind) {
-    static const char* names[] = {"w", "g", "m", "v", "t"};
+    static const char* names[] = {"w", "g", "m", "v", "t", "buf"};
     return names[kind];
 }
 
@@ -165,7 +165,7 @@ static bool overlaps_any(const std::vector<Span>& sorted, const void* p, size_t 
 // per-list device tables
 // ------------------------------------------------------------------------------------------------------------------
 
-enum Kind : uint64_t { kAdamW = 1, kNorm = 2, kScale = 3 };
+enum Kind : uint64_t { kAdamW = 1, kNorm = 2, kScale = 3, kSGD = 4, kMomentum = 5 };
 
 struct Plan {
     // the list it was built for (compared in full on every lookup)
@@ -175,6 +175,8 @@ struct Plan {
     int32_t T = 0;
     std::vector<int64_t> n;
     std::vector<const void*> ptrs[4];  // the pointer arrays the kind uses, in ListDesc order
+    std::vector<int32_t> group;        // AdamW over parameter groups: each tensor's group (empty: none)
+    int32_t max_group = 0;             // the largest entry of `group`
     int64_t total = 0;                 // elements
     const void* checked_scalar[2] = {nullptr, nullptr};  // the last scalar outputs found valid for this list
     void* dev = nullptr;  // one allocation: TensorRec[T] | WorkItem[I] | double[I] (norm)
@@ -278,6 +280,7 @@ struct ListDesc {
     void* const* m;      // adamw
     void* const* v;      // adamw
     Dtype gdt, mdt;      // scale: gdt is the tensors' type
+    const int32_t* group = nullptr;  // AdamW over parameter groups: T group indices (validated by the caller)
 };
 
 static size_t elem_bytes(Dtype d) { return d == kF16 ? 2 : 4; }
@@ -290,6 +293,12 @@ static int list_arrays(const ListDesc& L, const void* const* out[4]) {
     if (L.kind == kNorm) {
         out[0] = L.g;
         return 1;
+    }
+    if (L.kind == kSGD || L.kind == kMomentum) {
+        out[0] = reinterpret_cast<const void* const*>(L.w);
+        out[1] = L.g;
+        out[2] = L.m;  // the momentum buffers
+        return L.kind == kMomentum ? 3 : 2;
     }
     out[0] = reinterpret_cast<const void* const*>(L.w);
     out[1] = L.g;
@@ -306,6 +315,7 @@ static uint64_t list_hash(const ListDesc& L, int device) {
     h = mix(h, (uint64_t)device);
     h = mix(h, ((uint64_t)L.gdt << 8) | (uint64_t)L.mdt);
     h = mix(h, (uint64_t)L.T);
+    h = mix(h, L.group ? 1u : 0u);
     if (L.T == 0) return h;
     const void* const* arr[4];
     const int na = list_arrays(L, arr);
@@ -313,6 +323,7 @@ static uint64_t list_hash(const ListDesc& L, int device) {
     for (int32_t k = 0; k < L.T; k += step) {
         h = mix(h, (uint64_t)L.n[k]);
         for (int a = 0; a < na; ++a) h = mix(h, ptr_u(arr[a][k]));
+        if (L.group) h = mix(h, (uint64_t)(uint32_t)L.group[k]);
     }
     h = mix(h, (uint64_t)L.n[L.T - 1]);
     for (int a = 0; a < na; ++a) h = mix(h, ptr_u(arr[a][L.T - 1]));
@@ -327,6 +338,8 @@ static bool same_list(const Plan& p, const ListDesc& L, int device) {
     const int na = list_arrays(L, arr);
     for (int a = 0; a < na; ++a)
         if (std::memcmp(p.ptrs[a].data(), arr[a], (size_t)L.T * sizeof(void*)) != 0) return false;
+    if (p.group.empty() != (L.group == nullptr)) return false;
+    if (L.group && std::memcmp(p.group.data(), L.group, (size_t)L.T * sizeof(int32_t)) != 0) return false;
     return true;
 }
 
@@ -342,6 +355,10 @@ static mica_status build_plan(const ListDesc& L, int device, uint64_t h, Plan** 
         const void* const* arr[4];
         const int na = list_arrays(L, arr);
         for (int a = 0; a < na; ++a) plan->ptrs[a].assign(arr[a], arr[a] + L.T);
+        if (L.group) {
+            plan->group.assign(L.group, L.group + L.T);
+            plan->max_group = *std::max_element(plan->group.begin(), plan->group.end());
+        }
     }
     for (int32_t k = 0; k < L.T; ++k) plan->total += L.n[k];
 
@@ -352,7 +369,7 @@ static mica_status build_plan(const ListDesc& L, int device, uint64_t h, Plan** 
     for (int32_t k = 0; k < L.T; ++k) {
         const int64_t n = L.n[k];
         TensorRec& r = recs[k];
-        r = TensorRec{nullptr, nullptr, nullptr, nullptr, n, 0, 0};
+        r = TensorRec{nullptr, nullptr, nullptr, nullptr, n, 0, L.group ? L.group[k] : 0};
         if (n == 0) continue;
         total_octs += (n + kOct - 1) / kOct;
         mica_status s;
@@ -386,6 +403,18 @@ static mica_status build_plan(const ListDesc& L, int device, uint64_t h, Plan** 
             const uint64_t ma = (L.mdt == kBF16x2 || L.mdt == kBF16x2M) ? 16 : 32;  // packed: 4 words an octet
             const uint64_t va = (L.mdt == kBF16x2) ? 16 : 32;
             vec = vec && ptr_u(r.w) % 32 == 0 && ptr_u(r.m) % ma == 0 && ptr_u(r.v) % va == 0;
+        } else if (L.kind == kSGD || L.kind == kMomentum) {
+            const size_t wb = (size_t)n * 4;
+            if ((s = check_device_span(L.w[k], wb, 4, device, "w", k)) != MICA_OK) return s;
+            r.w = L.w[k];
+            spans.push_back({(uintptr_t)ptr_u(r.w), (uintptr_t)(ptr_u(r.w) + wb), 0, k});
+            vec = vec && ptr_u(r.w) % 32 == 0;
+            if (L.kind == kMomentum) {
+                if ((s = check_device_span(L.m[k], wb, 4, device, "buf", k)) != MICA_OK) return s;
+                r.m = L.m[k];
+                spans.push_back({(uintptr_t)ptr_u(r.m), (uintptr_t)(ptr_u(r.m) + wb), 5, k});
+                vec = vec && ptr_u(r.m) % 32 == 0;
+            }
         }
         r.vec = vec ? 1 : 0;
     }
@@ -423,7 +452,8 @@ static mica_status build_plan(const ListDesc& L, int device, uint64_t h, Plan** 
         plan->chunks.grid = grid;
         plan->chunks.total_octs = total_octs;
     } else {
-        plan->item_octs = choose_item_octs(total_octs, sms, L.kind == kAdamW && L.mdt == kF32);
+        plan->item_octs = choose_item_octs(total_octs, sms, (L.kind == kAdamW && L.mdt == kF32) ||
+                                                                L.kind == kSGD || L.kind == kMomentum);
         items = build_items(L.n, L.T, plan->item_octs);
         if (items.size() > (size_t)INT32_MAX) return fail(MICA_ERR_COUNT, "too many work items (%zu)", items.size());
         plan->num_items = (int32_t)items.size();
@@ -635,46 +665,71 @@ extern "C" mica_status mica_clip_grad_norms(const void* const* g, const int64_t*
                         stream, "ClipGradNorms launch");
 }
 
-extern "C" mica_status mica_adamw_steps(float* const* w, void* const* g, void* const* m, void* const* v,
-                                        const int64_t* n, int32_t T, mica_dtype gdt, mica_dtype mdt,
-                                        const mica_adamw_hp* hp, const float* d_factor, void* stream) {
+namespace mica {
+
+static mica_status check_adam_hp(const mica_adamw_hp* hp, int32_t j) {
+    if (!finite_nonneg(hp->lr)) return fail(MICA_ERR_HYPER, "hp[%d].lr %g is not finite and >= 0", j, hp->lr);
+    if (!finite_nonneg(hp->eps)) return fail(MICA_ERR_HYPER, "hp[%d].eps %g is not finite and >= 0", j, hp->eps);
+    if (!finite_nonneg(hp->weight_decay))
+        return fail(MICA_ERR_HYPER, "hp[%d].weight_decay %g is not finite and >= 0", j, hp->weight_decay);
+    if (hp->step < 1) return fail(MICA_ERR_HYPER, "hp[%d].step %lld is not >= 1", j, (long long)hp->step);
+    if (hp->flags & ~(MICA_STEP_SKIP_NONFINITE | MICA_STEP_COUPLED_L2))
+        return fail(MICA_ERR_HYPER, "hp[%d].flags has unknown bits (0x%x)", j, hp->flags);
+    if (!(hp->beta1 >= 0.0 && hp->beta1 < 1.0))
+        return fail(MICA_ERR_BETA, "hp[%d].beta1 %g is outside [0, 1)", j, hp->beta1);
+    if (!(hp->beta2 >= 0.0 && hp->beta2 < 1.0))
+        return fail(MICA_ERR_BETA, "hp[%d].beta2 %g is outside [0, 1)", j, hp->beta2);
+    return MICA_OK;
+}
+
+// AdamWSteps with num_groups >= 1 parameter groups (group == nullptr: one group, every tensor in it).
+static mica_status adamw_steps(float* const* w, void* const* g, void* const* m, void* const* v, const int64_t* n,
+                               int32_t T, mica_dtype gdt, mica_dtype mdt, const int32_t* group,
+                               const mica_adamw_hp* hp, int32_t num_groups, const float* d_factor, void* stream) {
     if (!hp) return fail(MICA_ERR_NULL, "hp is NULL");
     if (gdt != MICA_F32 && gdt != MICA_F16) return fail(MICA_ERR_DTYPE, "gradients must be float32 or float16");
     if (mdt != MICA_F32 && mdt != MICA_BF16X2 && mdt != MICA_BF16X2_M)
         return fail(MICA_ERR_DTYPE, "moments must be float32, packed BF16, or packed m with float32 v");
-    if (!finite_nonneg(hp->lr)) return fail(MICA_ERR_HYPER, "lr %g is not finite and >= 0", hp->lr);
-    if (!finite_nonneg(hp->eps)) return fail(MICA_ERR_HYPER, "eps %g is not finite and >= 0", hp->eps);
-    if (!finite_nonneg(hp->weight_decay))
-        return fail(MICA_ERR_HYPER, "weight_decay %g is not finite and >= 0", hp->weight_decay);
-    if (hp->step < 1) return fail(MICA_ERR_HYPER, "step %lld is not >= 1", (long long)hp->step);
-    if (hp->flags & ~(MICA_STEP_SKIP_NONFINITE | MICA_STEP_COUPLED_L2))
-        return fail(MICA_ERR_HYPER, "hp->flags has unknown bits (0x%x)", hp->flags);
-    if (!(hp->beta1 >= 0.0 && hp->beta1 < 1.0)) return fail(MICA_ERR_BETA, "beta1 %g is outside [0, 1)", hp->beta1);
-    if (!(hp->beta2 >= 0.0 && hp->beta2 < 1.0)) return fail(MICA_ERR_BETA, "beta2 %g is outside [0, 1)", hp->beta2);
+    mica_status s;
+    for (int32_t j = 0; j < num_groups; ++j) {
+        if ((s = check_adam_hp(&hp[j], j)) != MICA_OK) return s;
+        const mica_adamw_hp& a = hp[j];
+        const mica_adamw_hp& z = hp[0];
+        if (a.beta1 != z.beta1 || a.beta2 != z.beta2 || a.eps != z.eps || a.step != z.step ||
+            (a.zero_grad != 0) != (z.zero_grad != 0) || a.flags != z.flags)
+            return fail(MICA_ERR_HYPER, "hp[%d] differs from hp[0] in beta1, beta2, eps, step, zero_grad or flags "
+                        "(only lr and weight_decay may differ between groups)", j);
+    }
     if (T < 0 || T > MICA_MAX_TENSORS) return fail(MICA_ERR_COUNT, "T = %d is outside [0, %d]", T, MICA_MAX_TENSORS);
     if (T > 0 && (!w || !g || !m || !v || !n)) return fail(MICA_ERR_NULL, "a pointer array is NULL");
-    mica_status s;
     int dev = 0;
-    ListDesc L{kAdamW, T, n, w, g, m, v, (Dtype)gdt, (Dtype)mdt};
+    ListDesc L{kAdamW, T, n, w, g, m, v, (Dtype)gdt, (Dtype)mdt, group};
     Plan* p = nullptr;
     if (T > 0 && current_device(&dev) == MICA_OK) p = cached_plan(L, dev);
     if (!p) {
         int64_t total = 0;
         if ((s = check_list(T, n, {reinterpret_cast<const void* const*>(w), g, m, v}, &total)) != MICA_OK) return s;
+        if (group)
+            for (int32_t k = 0; k < T; ++k)
+                if (group[k] < 0 || group[k] >= num_groups)
+                    return fail(MICA_ERR_COUNT, "group[%d] = %d is outside [0, %d)", k, group[k], num_groups);
         if (total == 0) return ok();
         if ((s = current_device(&dev)) != MICA_OK) return s;
         if ((s = get_plan(L, dev, &p, stream)) != MICA_OK) return s;
     }
     if (p->total == 0) return ok();
+    if (group && p->max_group >= num_groups)  // a list seen before with more groups
+        return fail(MICA_ERR_COUNT, "group index %d is outside [0, %d)", p->max_group, num_groups);
     if ((s = check_scalars(p, dev, d_factor, nullptr, "one of the step's buffers")) != MICA_OK) return s;
 
     // the step's scalars: PyTorch's, each in double and rounded once to float32
     const double t = (double)hp->step;
+    const double q1 = 1.0 - std::pow(hp->beta1, t);
     StepScalars sc{};
     sc.c1 = (float)(1.0 - hp->beta1);
     sc.b2 = (float)hp->beta2;
     sc.c2 = (float)(1.0 - hp->beta2);
-    sc.neg_step = -(float)(hp->lr / (1.0 - std::pow(hp->beta1, t)));
+    sc.neg_step = -(float)(hp->lr / q1);
     sc.bc2 = (float)std::sqrt(1.0 - std::pow(hp->beta2, t));
     sc.dec = (float)(1.0 - hp->lr * hp->weight_decay);
     sc.eps = (float)hp->eps;
@@ -682,9 +737,74 @@ extern "C" mica_status mica_adamw_steps(float* const* w, void* const* g, void* c
     sc.zero_grad = hp->zero_grad ? 1 : 0;
     sc.skip_nonfinite = (hp->flags & MICA_STEP_SKIP_NONFINITE) ? 1 : 0;
     const bool coupled = (hp->flags & MICA_STEP_COUPLED_L2) != 0;
+    GroupScalars gs{};
+    for (int32_t j = 0; j < num_groups; ++j) {
+        gs.neg_step[j] = -(float)(hp[j].lr / q1);
+        gs.dec[j] = (float)(1.0 - hp[j].lr * hp[j].weight_decay);
+        gs.wd[j] = (float)hp[j].weight_decay;
+    }
     return after_launch(launch_adamw(p->recs, p->items, p->num_items, p->item_octs, (Dtype)gdt, (Dtype)mdt, coupled,
-                                     sc, d_factor, stream),
+                                     sc, group ? &gs : nullptr, d_factor, stream),
                         stream, "AdamWSteps launch");
+}
+
+}  // namespace mica
+
+extern "C" mica_status mica_adamw_steps(float* const* w, void* const* g, void* const* m, void* const* v,
+                                        const int64_t* n, int32_t T, mica_dtype gdt, mica_dtype mdt,
+                                        const mica_adamw_hp* hp, const float* d_factor, void* stream) {
+    return adamw_steps(w, g, m, v, n, T, gdt, mdt, nullptr, hp, 1, d_factor, stream);
+}
+
+extern "C" mica_status mica_adamw_steps_grouped(float* const* w, void* const* g, void* const* m, void* const* v,
+                                                const int64_t* n, int32_t T, mica_dtype gdt, mica_dtype mdt,
+                                                const int32_t* group, const mica_adamw_hp* hp, int32_t num_groups,
+                                                const float* d_factor, void* stream) {
+    if (num_groups < 1 || num_groups > MICA_MAX_GROUPS)
+        return fail(MICA_ERR_COUNT, "num_groups = %d is outside [1, %d]", num_groups, MICA_MAX_GROUPS);
+    if (T > 0 && !group) return fail(MICA_ERR_NULL, "group is NULL");
+    return adamw_steps(w, g, m, v, n, T, gdt, mdt, T > 0 ? group : nullptr, hp, num_groups, d_factor, stream);
+}
+
+extern "C" mica_status mica_sgd_steps(float* const* w, void* const* g, float* const* buf, const int64_t* n,
+                                      int32_t T, mica_dtype gdt, const mica_sgd_hp* hp, const float* d_factor,
+                                      void* stream) {
+    if (!hp) return fail(MICA_ERR_NULL, "hp is NULL");
+    if (gdt != MICA_F32 && gdt != MICA_F16) return fail(MICA_ERR_DTYPE, "gradients must be float32 or float16");
+    if (!finite_nonneg(hp->lr)) return fail(MICA_ERR_HYPER, "lr %g is not finite and >= 0", hp->lr);
+    if (!finite_nonneg(hp->momentum)) return fail(MICA_ERR_HYPER, "momentum %g is not finite and >= 0", hp->momentum);
+    if (!buf && hp->momentum != 0.0) return fail(MICA_ERR_NULL, "momentum %g > 0 needs the buffer array", hp->momentum);
+    if (hp->flags & ~MICA_STEP_SKIP_NONFINITE)
+        return fail(MICA_ERR_HYPER, "hp->flags has bits SGD does not take (0x%x)", hp->flags);
+    if (T < 0 || T > MICA_MAX_TENSORS) return fail(MICA_ERR_COUNT, "T = %d is outside [0, %d]", T, MICA_MAX_TENSORS);
+    if (T > 0 && (!w || !g || !n)) return fail(MICA_ERR_NULL, "a pointer array is NULL");
+    mica_status s;
+    int dev = 0;
+    const Kind kind = buf ? kMomentum : kSGD;
+    ListDesc L{kind, T, n, w, g, reinterpret_cast<void* const*>(buf), nullptr, (Dtype)gdt, kF32};
+    Plan* p = nullptr;
+    if (T > 0 && current_device(&dev) == MICA_OK) p = cached_plan(L, dev);
+    if (!p) {
+        int64_t total = 0;
+        if (buf)
+            s = check_list(T, n, {reinterpret_cast<const void* const*>(w), g,
+                                  reinterpret_cast<const void* const*>(buf)}, &total);
+        else
+            s = check_list(T, n, {reinterpret_cast<const void* const*>(w), g}, &total);
+        if (s != MICA_OK) return s;
+        if (total == 0) return ok();
+        if ((s = current_device(&dev)) != MICA_OK) return s;
+        if ((s = get_plan(L, dev, &p, stream)) != MICA_OK) return s;
+    }
+    if (p->total == 0) return ok();
+    if ((s = check_scalars(p, dev, d_factor, nullptr, "one of the step's buffers")) != MICA_OK) return s;
+    SgdScalars sc{};
+    sc.neg_lr = -(float)hp->lr;
+    sc.mu = (float)hp->momentum;
+    sc.zero_grad = hp->zero_grad ? 1 : 0;
+    return after_launch(launch_sgd(p->recs, p->items, p->num_items, p->item_octs, (Dtype)gdt, buf != nullptr,
+                                   (hp->flags & MICA_STEP_SKIP_NONFINITE) != 0, sc, d_factor, stream),
+                        stream, "SGDSteps launch");
 }
 
 extern "C" mica_status mica_sync(void* stream) {
@@ -726,4 +846,4 @@ extern "C" const char* mica_last_error_detail(void) { return t_detail.c_str(); }
 
 extern "C" uint64_t mica_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
-extern "C" int32_t mica_abi_version(void) { return 1; }
+extern "C" int32_t mica_abi_version(void) { return 2; }

@@ -13,49 +13,12 @@
 #include <cstdint>
 
 #include "plan.h"
+#include "stream.cuh"
 
 namespace mica {
 namespace {
 
 constexpr int kUnrollScale = 2;  // octets in flight per thread and round in ScaleTensors
-
-// ------------------------------------------------------------------------------------------------------------------
-// memory access
-// ------------------------------------------------------------------------------------------------------------------
-
-// 32 bytes, not kept in L1, first to leave L2 (each byte is used once)
-__device__ __forceinline__ void ld8_stream(const float* p, float (&a)[8]) {
-    asm volatile("ld.global.L1::no_allocate.L2::evict_first.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                 : "=f"(a[0]), "=f"(a[1]), "=f"(a[2]), "=f"(a[3]), "=f"(a[4]), "=f"(a[5]), "=f"(a[6]), "=f"(a[7])
-                 : "l"(p));
-}
-__device__ __forceinline__ void st8(float* p, const float (&a)[8]) {
-    asm volatile("st.global.cs.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(a[0]), "f"(a[1]), "f"(a[2]),
-                 "f"(a[3]), "f"(a[4]), "f"(a[5]), "f"(a[6]), "f"(a[7])
-                 : "memory");
-}
-__device__ __forceinline__ uint4 ld16_stream(const void* p) {
-    uint4 r;
-    asm volatile("ld.global.cs.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
-    return r;
-}
-__device__ __forceinline__ void st16(void* p, uint4 x) {
-    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(x.x), "r"(x.y), "r"(x.z), "r"(x.w)
-                 : "memory");
-}
-
-// eight binary16 values (16 bytes) -> float32 (exact)
-__device__ __forceinline__ void h8_to(const uint4& x, float (&a)[8]) {
-    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
-        a[2 * k] = f.x;
-        a[2 * k + 1] = f.y;
-    }
-}
 
 // ------------------------------------------------------------------------------------------------------------------
 // packed BF16 (BendTorch "main.bend", "AdamW over packed BF16 moments"): element 2k is the low half of word k
@@ -81,32 +44,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float even, float odd) {
     if (odd != odd) r |= 0xFFFF0000u;
     return r;
 }
-
-// ------------------------------------------------------------------------------------------------------------------
-// programmatic dependent launch
-// ------------------------------------------------------------------------------------------------------------------
-
-// Lets the kernel queued after this one start launching (it still waits for this one before using its results).
-__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-
-// Waits until the kernel queued before this one has completed and its writes are visible (returns at once when this
-// kernel was not launched as a programmatic dependent).
-__device__ __forceinline__ void wait_prerequisite() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-// The gradient factor, read once per thread right before its first update (after the prerequisite has finished).
-struct Factor {
-    const float* src;
-    float value;
-    bool ready;
-    __device__ __forceinline__ float get() {
-        if (!ready) {
-            wait_prerequisite();
-            value = src ? __ldcg(src) : 1.0f;
-            ready = true;
-        }
-        return value;
-    }
-};
 
 // ------------------------------------------------------------------------------------------------------------------
 // AdamW on one octet, in registers
@@ -160,11 +97,6 @@ __device__ __forceinline__ void adam8(float (&w)[8], const float (&g)[8], float 
         w[j] = __fadd_rn(wdec[j], __fdiv_rn(__fmul_rn(s.neg_step, m[j]), denom));
     }
 }
-
-// A step to skip: the caller asked to skip steps whose norm was not finite (kSkip), and the factor is not > 0 (a
-// NaN norm gives a NaN factor, an infinite one a zero factor). Without kSkip the test compiles away.
-template <bool kSkip>
-__device__ __forceinline__ bool skip_step(float f) { return kSkip && !(f > 0.0f); }
 
 // One packed-moment octet's 4 words, element by element (words past the tensor's last element are not read).
 __device__ __forceinline__ void load_words(const void* base, int64_t o, int cnt, uint32_t (&word)[4],
@@ -241,11 +173,6 @@ __device__ __noinline__ void adam_oct_elements(const TensorRec& r, int64_t o, co
     }
 }
 
-// Asks L2 to fetch `bytes` (a multiple of 16) from `p` (16-byte aligned), without waiting for them.
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 // The four streams of octets [a, b) of tensor r into L2 (a < b, whole octets of an aligned tensor).
 template <Dtype G, Dtype M>
 __device__ __forceinline__ void prefetch_octets(const TensorRec& r, int64_t a, int64_t b) {
@@ -313,12 +240,27 @@ __device__ __forceinline__ void adam_range(const TensorRec& r, int64_t ob, int64
     }
 }
 
+// The scalars of tensor r: with kGrouped its group's neg_step, dec and wd replace those of s (the rest is shared).
+template <bool kGrouped>
+__device__ __forceinline__ StepScalars group_scalars(const StepScalars& s, const GroupScalars& gs,
+                                                     const TensorRec& r) {
+    StepScalars x = s;
+    if constexpr (kGrouped) {
+        x.neg_step = gs.neg_step[r.group];
+        x.dec = gs.dec[r.group];
+        x.wd = gs.wd[r.group];
+    }
+    return x;
+}
+
 // One CTA per work item, items taken in reverse order (the norm reads them forwards, so the gradient it read last
-// may still be in L2 when this kernel starts).
-template <Dtype G, Dtype M, bool kCoupled, bool kSkip>
+// may still be in L2 when this kernel starts). Without kGrouped the scalars are read straight from the kernel's
+// parameters; with it each tensor's group picks its own (the parameter array is indexed in place).
+template <Dtype G, Dtype M, bool kCoupled, bool kSkip, bool kGrouped>
 __global__ void __launch_bounds__(kThreads, 3) adamw_kernel(const TensorRec* __restrict__ recs,
                                                             const WorkItem* __restrict__ items, int32_t num_items,
                                                             int32_t item_octs, StepScalars s,
+                                                            const __grid_constant__ GroupScalars gs,
                                                             const float* __restrict__ d_factor) {
     allow_dependents();  // the next step's norm may launch and set up while this kernel's last CTAs run
     Factor fac{d_factor, 1.0f, false};
@@ -329,11 +271,21 @@ __global__ void __launch_bounds__(kThreads, 3) adamw_kernel(const TensorRec* __r
             const TensorRec r = recs[item.t];
             const int64_t no = (r.n + kOct - 1) / kOct;
             const int64_t oe = item.o0 + item_octs < no ? item.o0 + item_octs : no;
-            adam_range<G, M, kCoupled, kSkip>(r, item.o0, oe, threadIdx.x, kThreads, s, fac, true);
+            if constexpr (kGrouped) {
+                const StepScalars x = group_scalars<kGrouped>(s, gs, r);
+                adam_range<G, M, kCoupled, kSkip>(r, item.o0, oe, threadIdx.x, kThreads, x, fac, true);
+            } else {
+                adam_range<G, M, kCoupled, kSkip>(r, item.o0, oe, threadIdx.x, kThreads, s, fac, true);
+            }
         } else {
             for (int j = warp; j < item.count; j += kWarps) {
                 const TensorRec r = recs[item.t + j];
-                adam_range<G, M, kCoupled, kSkip>(r, 0, (r.n + kOct - 1) / kOct, lane, 32, s, fac);
+                if constexpr (kGrouped) {
+                    const StepScalars x = group_scalars<kGrouped>(s, gs, r);
+                    adam_range<G, M, kCoupled, kSkip>(r, 0, (r.n + kOct - 1) / kOct, lane, 32, x, fac);
+                } else {
+                    adam_range<G, M, kCoupled, kSkip>(r, 0, (r.n + kOct - 1) / kOct, lane, 32, s, fac);
+                }
             }
         }
     }
@@ -874,40 +826,52 @@ __global__ void __launch_bounds__(kThreads) scale_kernel(const TensorRec* __rest
     }
 }
 
-template <Dtype G, Dtype M, bool kCoupled, bool kSkip>
-cudaError_t launch_adamw_t(const WorkItem* items, const TensorRec* recs, int32_t num_items, int32_t item_octs,
-                           cudaStream_t st, const StepScalars& s, const float* d_factor) {
+// The AdamW launch options: each selects a kernel instantiation, so that the common step compiles without the
+// others' tests.
+struct AdamwLaunch {
+    const WorkItem* items;
+    const TensorRec* recs;
+    int32_t num_items, item_octs;
+    cudaStream_t st;
+    const StepScalars* s;
+    const GroupScalars* groups;  // nullptr: one group
+    const float* d_factor;
+};
+
+template <Dtype G, Dtype M, bool kCoupled, bool kSkip, bool kGrouped>
+cudaError_t launch_adamw_t(const AdamwLaunch& a) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(num_items);
+    cfg.gridDim = dim3(a.num_items);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = 0;
-    cfg.stream = st;
+    cfg.stream = a.st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, adamw_kernel<G, M, kCoupled, kSkip>, recs, items, num_items, item_octs, s,
-                              d_factor);
+    const GroupScalars gs = a.groups ? *a.groups : GroupScalars{};
+    return cudaLaunchKernelEx(&cfg, adamw_kernel<G, M, kCoupled, kSkip, kGrouped>, a.recs, a.items, a.num_items,
+                              a.item_octs, *a.s, gs, a.d_factor);
+}
+
+template <Dtype G, Dtype M, bool kCoupled, bool kSkip>
+cudaError_t launch_adamw_g(const AdamwLaunch& a) {
+    return a.groups ? launch_adamw_t<G, M, kCoupled, kSkip, true>(a) : launch_adamw_t<G, M, kCoupled, kSkip, false>(a);
 }
 
 template <Dtype G, Dtype M>
-cudaError_t launch_adamw_c(bool coupled, const WorkItem* items, const TensorRec* recs, int32_t num_items,
-                           int32_t item_octs, cudaStream_t st, const StepScalars& s, const float* d_factor) {
-    if (s.skip_nonfinite)
-        return coupled ? launch_adamw_t<G, M, true, true>(items, recs, num_items, item_octs, st, s, d_factor)
-                       : launch_adamw_t<G, M, false, true>(items, recs, num_items, item_octs, st, s, d_factor);
-    return coupled ? launch_adamw_t<G, M, true, false>(items, recs, num_items, item_octs, st, s, d_factor)
-                   : launch_adamw_t<G, M, false, false>(items, recs, num_items, item_octs, st, s, d_factor);
+cudaError_t launch_adamw_c(bool coupled, const AdamwLaunch& a) {
+    if (a.s->skip_nonfinite)
+        return coupled ? launch_adamw_g<G, M, true, true>(a) : launch_adamw_g<G, M, false, true>(a);
+    return coupled ? launch_adamw_g<G, M, true, false>(a) : launch_adamw_g<G, M, false, false>(a);
 }
 
 template <Dtype G>
-cudaError_t launch_adamw_m(Dtype mdt, bool coupled, const WorkItem* items, const TensorRec* recs,
-                           int32_t num_items, int32_t item_octs, cudaStream_t st, const StepScalars& s,
-                           const float* d_factor) {
-    if (mdt == kBF16x2) return launch_adamw_c<G, kBF16x2>(coupled, items, recs, num_items, item_octs, st, s, d_factor);
-    if (mdt == kBF16x2M) return launch_adamw_c<G, kBF16x2M>(coupled, items, recs, num_items, item_octs, st, s, d_factor);
-    return launch_adamw_c<G, kF32>(coupled, items, recs, num_items, item_octs, st, s, d_factor);
+cudaError_t launch_adamw_m(Dtype mdt, bool coupled, const AdamwLaunch& a) {
+    if (mdt == kBF16x2) return launch_adamw_c<G, kBF16x2>(coupled, a);
+    if (mdt == kBF16x2M) return launch_adamw_c<G, kBF16x2M>(coupled, a);
+    return launch_adamw_c<G, kF32>(coupled, a);
 }
 
 }  // namespace
@@ -917,12 +881,11 @@ cudaError_t launch_adamw_m(Dtype mdt, bool coupled, const WorkItem* items, const
 // ------------------------------------------------------------------------------------------------------------------
 
 int launch_adamw(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_octs, Dtype gdt,
-                 Dtype mdt, bool coupled, const StepScalars& s, const float* d_factor, void* stream) {
+                 Dtype mdt, bool coupled, const StepScalars& s, const GroupScalars* groups, const float* d_factor,
+                 void* stream) {
     if (num_items <= 0) return (int)cudaSuccess;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const cudaError_t e =
-        (gdt == kF16) ? launch_adamw_m<kF16>(mdt, coupled, items, recs, num_items, item_octs, st, s, d_factor)
-                      : launch_adamw_m<kF32>(mdt, coupled, items, recs, num_items, item_octs, st, s, d_factor);
+    const AdamwLaunch a{items, recs, num_items, item_octs, static_cast<cudaStream_t>(stream), &s, groups, d_factor};
+    const cudaError_t e = (gdt == kF16) ? launch_adamw_m<kF16>(mdt, coupled, a) : launch_adamw_m<kF32>(mdt, coupled, a);
     count_launches(1);
     return (int)(e != cudaSuccess ? e : cudaGetLastError());
 }

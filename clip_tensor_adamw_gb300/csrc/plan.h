@@ -1,4 +1,5 @@
-// Internal layout shared by the host side (api.cpp: validation, tables, launches) and the kernels (kernels.cu).
+// Internal layout shared by the host side (api.cpp: validation, tables, launches) and the kernels (kernels.cu,
+// sgd.cu).
 //
 // A call's tensor list becomes one device table:
 //   TensorRec[T]   the four base pointers and the element count of every tensor;
@@ -23,14 +24,14 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kOct = 8;        // elements per vector unit
 
 struct TensorRec {
-    float* w;      // weights (AdamW) / the tensor itself (scale) / unused (norm)
-    void* g;       // gradient (AdamW, norm)
-    void* m;       // first moment
+    float* w;      // weights (AdamW, SGD) / the tensor itself (scale) / unused (norm)
+    void* g;       // gradient (AdamW, SGD, norm)
+    void* m;       // first moment (AdamW) / momentum buffer (SGD with momentum)
     void* v;       // second moment
     int64_t n;     // elements
     int32_t vec;   // 1 when every base pointer is aligned for its octet vector (32 B for float32 streams, 16 B for
                    // binary16 and packed streams): the vector path; 0: the element path
-    int32_t pad;
+    int32_t group; // AdamW over parameter groups: the tensor's group (0 otherwise)
 };
 static_assert(sizeof(TensorRec) == 48, "TensorRec layout");
 
@@ -84,15 +85,38 @@ struct StepScalars {
     int32_t skip_nonfinite;  // leave w, m, v as they are when the factor is not > 0
 };
 
+// Parameter groups (PyTorch's param_groups): per group, the scalars that depend on its lr and weight decay. The
+// other scalars are the same for every group.
+constexpr int kMaxGroups = 8;
+struct GroupScalars {
+    float neg_step[kMaxGroups];
+    float dec[kMaxGroups];
+    float wd[kMaxGroups];
+};
+
+// SGD and SGD with momentum, float32 scalars rounded once from the host's doubles.
+struct SgdScalars {
+    float neg_lr;    // -lr
+    float mu;        // momentum
+    int32_t zero_grad;
+    int32_t pad;
+};
+
 // kBF16x2M (moments only): m packed as kBF16x2, v float32
 enum Dtype : int32_t { kF32 = 0, kF16 = 1, kBF16x2 = 2, kBF16x2M = 3 };
 
-// Kernel launchers (kernels.cu). Each returns the cudaError_t of its launch as an int.
-// AdamW (or, with `coupled`, Adam with the coupled L2 term) over every item, one CTA per item. It is launched as a programmatic dependent of the kernel queued before
-// it: it may start and load its tensors while that kernel finishes, and reads d_factor only once that kernel has
-// completed.
+// Kernel launchers (kernels.cu, sgd.cu). Each returns the cudaError_t of its launch as an int.
+// AdamW (or, with `coupled`, Adam with the coupled L2 term) over every item, one CTA per item. It is launched as a
+// programmatic dependent of the kernel queued before it: it may start and load its tensors while that kernel
+// finishes, and reads d_factor only once that kernel has completed. With `groups`, tensor k takes neg_step, dec and
+// wd from entry recs[k].group of it instead of from s.
 int launch_adamw(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_octs, Dtype gdt,
-                 Dtype mdt, bool coupled, const StepScalars& s, const float* d_factor, void* stream);
+                 Dtype mdt, bool coupled, const StepScalars& s, const GroupScalars* groups, const float* d_factor,
+                 void* stream);
+// SGD (momentum false) or SGD with momentum over every item, launched as AdamW is. `skip`: leave w (and the
+// buffer) as they are when the factor is not > 0.
+int launch_sgd(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_octs, Dtype gdt,
+               bool momentum, bool skip, const SgdScalars& s, const float* d_factor, void* stream);
 // The joint norm in one launch of ct.grid CTAs: one partial square sum per CTA into `partials` (ct.grid doubles),
 // and the CTA that finishes last sums them in a fixed order and writes norm and factor. `ticket` must be 0 before
 // the launch; the kernel leaves it 0.

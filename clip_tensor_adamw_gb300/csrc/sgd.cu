@@ -1,0 +1,188 @@
+// SGD and SGD with momentum over a tensor list in one launch, with the clip factor folded in: BendTorch "main.bend",
+// section "Optimizers", whose two plain optimizers are w + (-lr) g and, with a momentum buffer b, b = b mu + g then
+// w + (-lr) b (PyTorch's SGD without weight decay, dampening or Nesterov). The gradient entering either is
+// gh = g * f, f the factor of the joint-norm clip (and of the loss-scale unscale), read from device memory.
+//
+// Same work items and access scheme as the AdamW kernel: one CTA per item (a slice of a large tensor, or a pack of
+// small tensors shared out one per warp), 32-byte streaming loads and stores, L2 prefetch two rounds ahead on the
+// slices, and a programmatic-dependent launch so that the loads start while the norm kernel finishes. Every float
+// operation is a separate correctly rounded intrinsic, in the page's order, so the result is bit-identical to the
+// same step on the CPU.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "plan.h"
+#include "stream.cuh"
+
+namespace mica {
+namespace {
+
+// One octet in registers: w, the gradient g (already widened to float32) and, with kMomentum, the buffer b.
+template <bool kMomentum>
+__device__ __forceinline__ void sgd8(float (&w)[8], const float (&g)[8], float (&b)[8], const SgdScalars& s,
+                                     float f) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float gh = __fmul_rn(g[j], f);
+        if constexpr (kMomentum) {
+            b[j] = __fadd_rn(__fmul_rn(b[j], s.mu), gh);
+            w[j] = __fadd_rn(w[j], __fmul_rn(s.neg_lr, b[j]));
+        } else {
+            w[j] = __fadd_rn(w[j], __fmul_rn(s.neg_lr, gh));
+        }
+    }
+}
+
+// One octet element by element (an unaligned tensor, or a tensor's last, partial octet): elements past n are
+// neither read nor written.
+template <Dtype G, bool kMomentum, bool kSkip>
+__device__ __noinline__ void sgd_oct_elements(const TensorRec& r, int64_t o, const SgdScalars& s, Factor& fac) {
+    const int64_t i0 = o * kOct;
+    const int64_t left = r.n - i0;
+    const int cnt = left < kOct ? (int)left : kOct;
+    float w[8], g[8], b[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        w[j] = g[j] = b[j] = 0.f;
+        if (j < cnt) {
+            w[j] = r.w[i0 + j];
+            g[j] = (G == kF16) ? __half2float(static_cast<const __half*>(r.g)[i0 + j])
+                               : static_cast<const float*>(r.g)[i0 + j];
+            if constexpr (kMomentum) b[j] = static_cast<const float*>(r.m)[i0 + j];
+        }
+    }
+    const float f = fac.get();
+    const bool skip = skip_step<kSkip>(f);
+    if (!skip) sgd8<kMomentum>(w, g, b, s, f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        if (j < cnt) {
+            if (!skip) {
+                r.w[i0 + j] = w[j];
+                if constexpr (kMomentum) static_cast<float*>(r.m)[i0 + j] = b[j];
+            }
+            if (s.zero_grad) {
+                if (G == kF16) static_cast<__half*>(r.g)[i0 + j] = __ushort_as_half(0);
+                else static_cast<float*>(r.g)[i0 + j] = 0.f;
+            }
+        }
+    }
+}
+
+// The streams of octets [a, b) of tensor r into L2 (whole octets of an aligned tensor).
+template <Dtype G, bool kMomentum>
+__device__ __forceinline__ void sgd_prefetch(const TensorRec& r, int64_t a, int64_t b) {
+    constexpr int kGb = (G == kF16) ? 16 : 32;
+    const uint32_t n = (uint32_t)(b - a);
+    prefetch_l2(reinterpret_cast<const char*>(r.w) + a * 32, n * 32);
+    prefetch_l2(static_cast<const char*>(r.g) + a * kGb, n * kGb);
+    if constexpr (kMomentum) prefetch_l2(static_cast<const char*>(r.m) + a * 32, n * 32);
+}
+
+// Octets [ob, oe) of one tensor: octet ob + lane first, then every `stride`-th; with `prefetch` (a whole CTA on one
+// slice) thread 0 asks L2 for the rounds one and two ahead.
+template <Dtype G, bool kMomentum, bool kSkip>
+__device__ __forceinline__ void sgd_range(const TensorRec& r, int64_t ob, int64_t oe, int lane, int stride,
+                                          const SgdScalars& s, Factor& fac, bool prefetch = false) {
+    const int64_t full = r.n / kOct;
+    if (r.vec) {
+        const int64_t vend = oe < full ? oe : full;
+        if (prefetch && lane == 0 && ob + stride < vend)
+            sgd_prefetch<G, kMomentum>(r, ob + stride, ob + 2 * stride < vend ? ob + 2 * stride : vend);
+        for (int64_t o = ob + lane; o < vend; o += stride) {
+            if (prefetch && lane == 0 && o + 2 * stride < vend)
+                sgd_prefetch<G, kMomentum>(r, o + 2 * stride, o + 3 * stride < vend ? o + 3 * stride : vend);
+            float w[8], g[8], b[8];
+            uint4 gh;
+            ld8_stream(r.w + kOct * o, w);
+            if constexpr (G == kF16) gh = ld16_stream(static_cast<const __half*>(r.g) + kOct * o);
+            else ld8_stream(static_cast<const float*>(r.g) + kOct * o, g);
+            if constexpr (kMomentum) ld8_stream(static_cast<const float*>(r.m) + kOct * o, b);
+            const float f = fac.get();
+            if (!skip_step<kSkip>(f)) {
+                if constexpr (G == kF16) h8_to(gh, g);
+                sgd8<kMomentum>(w, g, b, s, f);
+                st8(r.w + kOct * o, w);
+                if constexpr (kMomentum) st8(static_cast<float*>(r.m) + kOct * o, b);
+            }
+            if (s.zero_grad) {
+                if constexpr (G == kF16) {
+                    st16(static_cast<__half*>(r.g) + kOct * o, make_uint4(0u, 0u, 0u, 0u));
+                } else {
+                    const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                    st8(static_cast<float*>(r.g) + kOct * o, z);
+                }
+            }
+        }
+        if (full < oe && full >= ob && lane == (int)((full - ob) % stride))
+            sgd_oct_elements<G, kMomentum, kSkip>(r, full, s, fac);
+    } else {
+        for (int64_t o = ob + lane; o < oe; o += stride) sgd_oct_elements<G, kMomentum, kSkip>(r, o, s, fac);
+    }
+}
+
+template <Dtype G, bool kMomentum, bool kSkip>
+__global__ void __launch_bounds__(kThreads, 3) sgd_kernel(const TensorRec* __restrict__ recs,
+                                                          const WorkItem* __restrict__ items, int32_t num_items,
+                                                          int32_t item_octs, SgdScalars s,
+                                                          const float* __restrict__ d_factor) {
+    allow_dependents();
+    Factor fac{d_factor, 1.0f, false};
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int32_t k = blockIdx.x; k < num_items; k += gridDim.x) {
+        const WorkItem item = items[num_items - 1 - k];
+        if (item.count == 1) {
+            const TensorRec r = recs[item.t];
+            const int64_t no = (r.n + kOct - 1) / kOct;
+            const int64_t oe = item.o0 + item_octs < no ? item.o0 + item_octs : no;
+            sgd_range<G, kMomentum, kSkip>(r, item.o0, oe, threadIdx.x, kThreads, s, fac, true);
+        } else {
+            for (int j = warp; j < item.count; j += kWarps) {
+                const TensorRec r = recs[item.t + j];
+                sgd_range<G, kMomentum, kSkip>(r, 0, (r.n + kOct - 1) / kOct, lane, 32, s, fac);
+            }
+        }
+    }
+}
+
+template <Dtype G, bool kMomentum, bool kSkip>
+cudaError_t launch_sgd_t(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_octs,
+                         const SgdScalars& s, const float* d_factor, cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_items);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, sgd_kernel<G, kMomentum, kSkip>, recs, items, num_items, item_octs, s, d_factor);
+}
+
+template <Dtype G>
+cudaError_t launch_sgd_g(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_octs,
+                         bool momentum, bool skip, const SgdScalars& s, const float* d_factor, cudaStream_t st) {
+    if (momentum)
+        return skip ? launch_sgd_t<G, true, true>(recs, items, num_items, item_octs, s, d_factor, st)
+                    : launch_sgd_t<G, true, false>(recs, items, num_items, item_octs, s, d_factor, st);
+    return skip ? launch_sgd_t<G, false, true>(recs, items, num_items, item_octs, s, d_factor, st)
+                : launch_sgd_t<G, false, false>(recs, items, num_items, item_octs, s, d_factor, st);
+}
+
+}  // namespace
+
+int launch_sgd(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_octs, Dtype gdt,
+               bool momentum, bool skip, const SgdScalars& s, const float* d_factor, void* stream) {
+    if (num_items <= 0) return (int)cudaSuccess;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const cudaError_t e =
+        (gdt == kF16) ? launch_sgd_g<kF16>(recs, items, num_items, item_octs, momentum, skip, s, d_factor, st)
+                      : launch_sgd_g<kF32>(recs, items, num_items, item_octs, momentum, skip, s, d_factor, st);
+    count_launches(1);
+    return (int)(e != cudaSuccess ? e : cudaGetLastError());
+}
+
+}  // namespace mica

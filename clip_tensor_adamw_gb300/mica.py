@@ -1,4 +1,4 @@
-"""Python binding of libmica_optim.so: the same three verbs as the C ABI (include/mica_optim.h), taking torch tensors.
+"""Python binding of libmica_optim.so: the entry points of the C ABI (include/mica_optim.h), taking torch tensors.
 
 This module only marshals arguments: it collects data pointers, element counts, the current CUDA stream and the
 hyperparameters into the C call, and turns a non-OK status into an exception. Every element of the step is read and
@@ -31,6 +31,14 @@ class MicaError(RuntimeError):
         super().__init__(f"{self.status}: {detail}")
 
 
+MICA_MAX_GROUPS = 8
+
+
+class _SgdHP(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_double), ("momentum", ctypes.c_double), ("zero_grad", ctypes.c_int32),
+                ("flags", ctypes.c_uint32)]
+
+
 class _HP(ctypes.Structure):
     _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double), ("beta2", ctypes.c_double),
                 ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double), ("step", ctypes.c_int64),
@@ -54,8 +62,12 @@ def lib() -> ctypes.CDLL:
                                            ctypes.c_float, _P, _P, _P]
         L.mica_adamw_steps.argtypes = [_P, _P, _P, _P, _I64P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                        ctypes.POINTER(_HP), _P, _P]
-        for f in ("mica_scale_tensors", "mica_clip_grad_norms", "mica_adamw_steps", "mica_sync",
-                  "mica_release_cache"):
+        L.mica_adamw_steps_grouped.argtypes = [_P, _P, _P, _P, _I64P, ctypes.c_int32, ctypes.c_int32,
+                                               ctypes.c_int32, _P, ctypes.POINTER(_HP), ctypes.c_int32, _P, _P]
+        L.mica_sgd_steps.argtypes = [_P, _P, _P, _I64P, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(_SgdHP),
+                                     _P, _P]
+        for f in ("mica_scale_tensors", "mica_clip_grad_norms", "mica_adamw_steps", "mica_adamw_steps_grouped",
+                  "mica_sgd_steps", "mica_sync", "mica_release_cache"):
             getattr(L, f).restype = ctypes.c_int
         L.mica_sync.argtypes = [_P]
         L.mica_release_cache.argtypes = []
@@ -176,6 +188,57 @@ def mica_adamw_steps(w, g, m, v, *, lr: float, beta1: float, beta2: float, eps: 
              flags)
     _check(lib().mica_adamw_steps(W.ptrs, G.ptrs, M.ptrs, V.ptrs, W.n, W.T, gdt, mdt, ctypes.byref(hp), _ptr(factor),
                                   _stream(stream)))
+
+
+class GroupIndex:
+    """The per-tensor group indices of mica_adamw_steps_grouped as a host int32 array, built once and reusable."""
+
+    def __init__(self, group: Sequence[int]):
+        self.values = [int(x) for x in group]
+        self.arr = (ctypes.c_int32 * max(len(self.values), 1))(*self.values)
+
+
+def mica_adamw_steps_grouped(w, g, m, v, group, groups: Sequence[dict], *, beta1: float, beta2: float, eps: float,
+                             step: int, zero_grad: bool = False, factor: torch.Tensor | None = None, stream=None,
+                             skip_nonfinite: bool = False, coupled_l2: bool = False) -> None:
+    """AdamWSteps over parameter groups in one launch: tensor k is stepped with ``groups[group[k]]``, a dict with
+    ``lr`` and ``weight_decay`` (the other hyperparameters are shared). ``group`` is a sequence of ints or a
+    GroupIndex; the rest is as mica_adamw_steps."""
+    W = _as_list(w)
+    sizes = W.counts
+    G = _as_list(g)
+    M = _as_list(m, sizes)
+    V = _as_list(v, sizes)
+    if not (W.T == G.T == M.T == V.T):
+        raise ValueError("w, g, m and v must list the same number of tensors")
+    gi = group if isinstance(group, GroupIndex) else GroupIndex(group)
+    if len(gi.values) != W.T:
+        raise ValueError("group must hold one index per tensor")
+    gdt = _dtype_code(G.tensors[0] if G.T else None, "g")
+    mdt = _dtype_code(M.tensors[0] if M.T else None, "m")
+    if mdt == MICA_BF16X2 and V.T and _dtype_code(V.tensors[0], "v") == MICA_F32:
+        mdt = MICA_BF16X2_M
+    flags = (MICA_STEP_SKIP_NONFINITE if skip_nonfinite else 0) | (MICA_STEP_COUPLED_L2 if coupled_l2 else 0)
+    hps = (_HP * max(len(groups), 1))(*[
+        _HP(float(gr["lr"]), float(beta1), float(beta2), float(eps), float(gr["weight_decay"]), int(step),
+            int(bool(zero_grad)), flags) for gr in groups])
+    _check(lib().mica_adamw_steps_grouped(W.ptrs, G.ptrs, M.ptrs, V.ptrs, W.n, W.T, gdt, mdt, gi.arr, hps,
+                                          len(groups), _ptr(factor), _stream(stream)))
+
+
+def mica_sgd_steps(w, g, buf=None, *, lr: float, momentum: float = 0.0, zero_grad: bool = False,
+                   factor: torch.Tensor | None = None, stream=None, skip_nonfinite: bool = False) -> None:
+    """SGD (``buf`` None) or SGD with momentum (one float32 buffer per tensor, zeros before the first step) over
+    every tensor in one launch, in place; ``factor`` is the device scalar from mica_clip_grad_norms (None: 1)."""
+    W = _as_list(w)
+    G = _as_list(g)
+    B = None if buf is None else _as_list(buf)
+    if W.T != G.T or (B is not None and B.T != W.T):
+        raise ValueError("w, g (and buf) must list the same number of tensors")
+    gdt = _dtype_code(G.tensors[0] if G.T else None, "g")
+    hp = _SgdHP(float(lr), float(momentum), int(bool(zero_grad)), MICA_STEP_SKIP_NONFINITE if skip_nonfinite else 0)
+    _check(lib().mica_sgd_steps(W.ptrs, G.ptrs, None if B is None else B.ptrs, W.n, W.T, gdt, ctypes.byref(hp),
+                                _ptr(factor), _stream(stream)))
 
 
 def mica_sync(stream=None) -> None:

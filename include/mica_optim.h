@@ -10,6 +10,12 @@
  *   mica_adamw_steps      AdamWSteps: AdamW over every (w, g, m, v) group in one launch, each group updated exactly
  *                         as a single-group step would update it.
  *
+ * and, over the same lists, the other optimizer steps of BendTorch "main.bend", section "Optimizers":
+ *
+ *   mica_adamw_steps_grouped  AdamWSteps over a list split into parameter groups (PyTorch's param_groups) with
+ *                             their own lr and weight decay, still one launch.
+ *   mica_sgd_steps            SGD, and SGD with momentum, over every (w, g[, buf]) group in one launch.
+ *
  * The per-element arithmetic is BendTorch "main.bend", section "Optimizers" (AdamW in PyTorch's order of operations;
  * the part "AdamW over packed BF16 moments (CAdamWBF16)" for packed moments), with PyTorch's scalars:
  *   step = lr / (1 - beta1^t), bc2 = sqrt(1 - beta2^t), decay w *= 1 - lr*wd,
@@ -80,6 +86,7 @@ typedef enum { MICA_F32 = 0, MICA_F16 = 1, MICA_BF16X2 = 2, MICA_BF16X2_M = 3 } 
                                        "main.bend", section "Optimizers": the Adam case of its Adam family). */
 
 #define MICA_MAX_TENSORS (1 << 24)
+#define MICA_MAX_GROUPS 8 /* parameter groups of one mica_adamw_steps_grouped call */
 
 /* One AdamW step's hyperparameters. */
 typedef struct {
@@ -144,6 +151,47 @@ MICA_API mica_status mica_adamw_steps(float* const* w, void* const* g, void* con
                              const float* d_factor, void* stream);
 
 /*
+ * AdamWSteps over parameter groups (PyTorch's param_groups, e.g. weight decay on the matrices and none on biases and
+ * norm gains): tensor k is stepped exactly as mica_adamw_steps would step it with hyperparameters hp[group[k]], all
+ * tensors in one launch. group: a host array of T indices in [0, num_groups); hp: num_groups entries, which may
+ * differ only in lr and weight_decay (beta1, beta2, eps, step, zero_grad and flags must equal hp[0]'s, else
+ * MICA_ERR_HYPER). 1 <= num_groups <= MICA_MAX_GROUPS (else MICA_ERR_COUNT). The group array is part of the list's
+ * identity: its cached table records each tensor's group. The pages' optimizer takes one weight decay for every
+ * tensor (the section "Optimizers" of BendTorch "main.bend"); the groups are this library's addition, for the
+ * usual split of a transformer's parameters.
+ * Errors: those of mica_adamw_steps, and COUNT for a group index or num_groups out of range.
+ */
+MICA_API mica_status mica_adamw_steps_grouped(float* const* w, void* const* g, void* const* m, void* const* v,
+                                              const int64_t* n, int32_t T, mica_dtype gdt, mica_dtype mdt,
+                                              const int32_t* group, const mica_adamw_hp* hp, int32_t num_groups,
+                                              const float* d_factor, void* stream);
+
+/* One SGD step's hyperparameters. */
+typedef struct {
+    double lr;          /* finite, >= 0 */
+    double momentum;    /* finite, >= 0; must be 0 when buf is NULL */
+    int32_t zero_grad;  /* nonzero: the gradient is written back as zeros */
+    uint32_t flags;     /* MICA_STEP_SKIP_NONFINITE or 0 */
+} mica_sgd_hp;
+
+/*
+ * SGD and SGD with momentum (BendTorch "main.bend", section "Optimizers": its SGD and Momentum cases, which are
+ * PyTorch's SGD without weight decay, dampening or Nesterov). For every tensor k and element i < n[k], in float32,
+ * each operation rounded on its own:
+ *   gh = g * f                    f = *d_factor (device float32) or 1 when d_factor is NULL
+ *   buf == NULL:   w = w + (-lr) * gh
+ *   buf != NULL:   b = buf * momentum + gh;  buf = b;  w = w + (-lr) * b
+ *   g  = 0                        when hp->zero_grad
+ * w: float32 [n]; g: gdt (MICA_F32 or MICA_F16) [n]; buf: NULL, or a host array of T device pointers to float32
+ * momentum buffers [n] (zeros before the first step: b = g then, as PyTorch's first step sets it). lr and momentum
+ * are rounded once to float32. With MICA_STEP_SKIP_NONFINITE, w and buf are left as they are when the factor is not
+ * > 0. In place, one launch; bit-identical to the same step on the CPU.
+ * Errors: NULL / COUNT / DTYPE / HYPER / ADDRESS / OVERLAP / DEVICE / CUDA / NOMEM.
+ */
+MICA_API mica_status mica_sgd_steps(float* const* w, void* const* g, float* const* buf, const int64_t* n, int32_t T,
+                                    mica_dtype gdt, const mica_sgd_hp* hp, const float* d_factor, void* stream);
+
+/*
  * ClipGradNorms for callers that cannot let a library allocate device memory: a runtime that reserves its whole
  * device-memory budget at start-up and treats any later cudaMalloc as a failure, a caller whose memory is all held
  * by another allocator, or a loop that cannot afford cudaMalloc's implicit synchronisation. The method's pages have
@@ -184,7 +232,7 @@ MICA_API const char* mica_last_error_detail(void);
 /* How many kernels this library has queued since it was loaded, over all threads. */
 MICA_API uint64_t mica_launch_count(void);
 
-/* The ABI version of this header: 1. */
+/* The ABI version of this header: 2 (1 had neither mica_adamw_steps_grouped nor mica_sgd_steps). */
 MICA_API int32_t mica_abi_version(void);
 
 #ifdef __cplusplus

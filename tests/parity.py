@@ -144,3 +144,99 @@ def run_parity(wl: workloads.Workload, sizes=None, steps: int | None = None, zer
             compare_state(st, host, bool(same), f"{wl.name} step {t}")
     mica.mica_sync()  # raises if a kernel's bounded pipeline wait gave up
     return {"norms": norms, "same_factor_every_step": same_all, "state": st}
+
+
+# ------------------------------------------------------------------------------------------------------------------
+# AdamW over parameter groups; SGD and SGD with momentum
+# ------------------------------------------------------------------------------------------------------------------
+
+def decay_groups(shapes) -> list[int]:
+    """The usual split of a transformer's parameters: matrices (group 0) decay, vectors (group 1) do not."""
+    return [0 if len(s) >= 2 else 1 for s in shapes]
+
+
+def group_hps(wl: workloads.Workload) -> list[dict]:
+    return [dict(lr=wl.lr, weight_decay=wl.weight_decay), dict(lr=wl.lr / 2, weight_decay=0.0)]
+
+
+def run_parity_groups(wl: workloads.Workload, group, sizes=None, steps: int | None = None, zero_grad: bool = False,
+                      ora: oracle.Oracle | None = None, check_every_step: bool = True) -> dict:
+    """As run_parity, with the update split into parameter groups (``group[k]`` the group of tensor k)."""
+    ora = ora or oracle.Oracle()
+    steps = wl.steps if steps is None else steps
+    st = workloads.make_state(wl, "cuda", sizes=sizes)
+    W, G, M, V = tensor_lists(st)
+    gi = mica.GroupIndex(group)
+    hps = group_hps(wl)
+    host = workloads.host_lists(st)
+    same_all = True
+    for t in range(1, steps + 1):
+        workloads.fill_grad(st, t)
+        host = (host[0], [x.copy() for x in workloads.host_lists(st)[1]], host[2], host[3])
+        d_norm, d_factor = mica.mica_clip_grad_norms(G, wl.max_norm, wl.inv_scale)
+        mica.mica_adamw_steps_grouped(W, G, M, V, gi, hps, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps, step=t,
+                                      zero_grad=zero_grad, factor=d_factor)
+        o_norm, o_factor, _ = ora.clip_grad_norms(host[1], wl.max_norm, wl.inv_scale)
+        ohps = [oracle.Hyper(lr=h["lr"], beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps, weight_decay=h["weight_decay"],
+                             step=t) for h in hps]
+        ora.adamw_steps_grouped(*host, group, ohps, factor=o_factor, zero_grad=zero_grad)
+        torch.cuda.synchronize()
+        assert abs(d_norm.item() - float(o_norm)) <= NORM_RTOL * abs(float(o_norm)), (t, d_norm.item(), o_norm)
+        same = np.float32(d_factor.item()).view(np.uint32) == o_factor.view(np.uint32)
+        same_all &= bool(same)
+        if check_every_step or t == steps:
+            compare_state(st, host, bool(same), f"{wl.name} groups step {t}")
+    mica.mica_sync()
+    return {"same_factor_every_step": same_all, "state": st}
+
+
+SGD_LR = 0.1
+
+
+def run_parity_sgd(wl: workloads.Workload, momentum: float, sizes=None, steps: int | None = None,
+                   zero_grad: bool = False, skip_nonfinite: bool = False, grad_hook=None,
+                   ora: oracle.Oracle | None = None, check_every_step: bool = True) -> dict:
+    """Clip + SGD (momentum 0: no buffers) or clip + SGD with momentum, the momentum buffers being the workload's
+    float32 first-moment buffers (zeros), against the oracle, element by element every step."""
+    assert wl.moments == "f32"
+    ora = ora or oracle.Oracle()
+    steps = wl.steps if steps is None else steps
+    st = workloads.make_state(wl, "cuda", sizes=sizes)
+    W, G, M, _ = tensor_lists(st)
+    B = M if momentum else None
+    hw, _, hb, _ = workloads.host_lists(st)
+    same_all = True
+    for t in range(1, steps + 1):
+        workloads.fill_grad(st, t)
+        if grad_hook is not None:
+            grad_hook(st, t)
+        hg = [x.copy() for x in workloads.host_lists(st)[1]]
+        d_norm, d_factor = mica.mica_clip_grad_norms(G, wl.max_norm, wl.inv_scale)
+        mica.mica_sgd_steps(W, G, B, lr=SGD_LR, momentum=momentum, zero_grad=zero_grad, factor=d_factor,
+                            skip_nonfinite=skip_nonfinite)
+        o_norm, o_factor = ora.clip_sgd_step(hw, hg, hb if momentum else None, SGD_LR, momentum, wl.max_norm,
+                                             wl.inv_scale, zero_grad=zero_grad, skip_nonfinite=skip_nonfinite)
+        torch.cuda.synchronize()
+        g_norm = np.float32(d_norm.item())
+        if np.isfinite(o_norm):
+            assert abs(float(g_norm) - float(o_norm)) <= NORM_RTOL * abs(float(o_norm)), (t, g_norm, o_norm)
+        else:
+            assert (np.isnan(g_norm) and np.isnan(o_norm)) or g_norm == o_norm, (t, g_norm, o_norm)
+        same = np.float32(d_factor.item()).view(np.uint32) == o_factor.view(np.uint32)
+        same_all &= bool(same)
+        if check_every_step or t == steps:
+            gw, gg, gb, _ = workloads.host_lists(st)
+            tag = f"{wl.name} sgd(mu={momentum}) step {t}"
+            for k, n in enumerate(st.sizes):
+                if n == 0:
+                    continue
+                f32_close(gw[k], hw[k], f"{tag} w[{k}]")
+                if momentum:
+                    f32_close(gb[k], hb[k], f"{tag} buf[{k}]")
+                if same:
+                    exact(gw[k], hw[k], f"{tag} w[{k}] bits")
+                    exact(gg[k], hg[k], f"{tag} g[{k}] bits")
+                    if momentum:
+                        exact(gb[k], hb[k], f"{tag} buf[{k}] bits")
+    mica.mica_sync()
+    return {"same_factor_every_step": same_all, "state": st}

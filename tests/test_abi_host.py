@@ -9,7 +9,7 @@ import re
 import pytest
 
 import clip_tensor_adamw_gb300 as mica
-from clip_tensor_adamw_gb300.mica import _HP
+from clip_tensor_adamw_gb300.mica import _HP, _SgdHP
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 OK, NULL, COUNT, DTYPE, HYPER, BETA, OVERLAP, DEVICE, ADDRESS, CUDA, NOMEM = range(11)
@@ -29,7 +29,7 @@ def test_exports_every_declared_symbol():
     assert len(names) >= 9
     for name in names:
         assert hasattr(L, name), name
-    assert L.mica_abi_version() == 1
+    assert L.mica_abi_version() == 2
 
 
 def test_status_strings():
@@ -73,6 +73,60 @@ def test_adamw_host_validation():
     assert adamw(T=1, ptrs=0, hp=_hp()) == NULL            # a NULL tensor with n > 0
     assert adamw(T=1, n=(0,), ptrs=0, hp=_hp()) == OK       # empty tensors may be NULL: nothing to do
     assert adamw(T=0, hp=_hp()) == OK
+
+
+def grouped(T=2, n=(4, 4), ptrs=0x1000, group=(0, 1), hps=None, num_groups=None, null_group=False):
+    L = mica.lib()
+    P = _arr(ctypes.c_void_p, [ptrs] * T)
+    N = _arr(ctypes.c_int64, list(n)[:T])
+    hps = [_hp(), _hp(lr=5e-4, weight_decay=0.0)] if hps is None else hps
+    H = (_HP * len(hps))(*hps)
+    G = None if null_group else _arr(ctypes.c_int32, list(group)[:T])
+    ng = len(hps) if num_groups is None else num_groups
+    return L.mica_adamw_steps_grouped(P, P, P, P, N, T, 0, 0, G, H, ng, None, None)
+
+
+def test_grouped_host_validation():
+    assert grouped(num_groups=0) == COUNT
+    assert grouped(num_groups=9) == COUNT
+    assert grouped(null_group=True) == NULL
+    assert grouped(group=(0, 2)) == COUNT                   # index past num_groups
+    assert grouped(group=(-1, 0)) == COUNT
+    for field, val, want in (("beta1", 0.8, HYPER), ("beta2", 0.9, HYPER), ("eps", 1e-6, HYPER), ("step", 2, HYPER),
+                             ("zero_grad", 1, HYPER), ("flags", 1, HYPER), ("lr", -1.0, HYPER),
+                             ("weight_decay", math.nan, HYPER), ("beta1", 1.0, BETA)):
+        assert grouped(hps=[_hp(), _hp(**{field: val})]) == want, field
+    assert grouped(T=0) == OK
+    assert grouped(n=(0, 0), ptrs=0) == OK
+
+
+def sgd(T=1, n=(4,), ptrs=0x1000, gdt=0, hp=None, with_buf=True, null_arrays=False):
+    L = mica.lib()
+    P = _arr(ctypes.c_void_p, [ptrs] * T)
+    N = _arr(ctypes.c_int64, list(n)[:T])
+    hp_ref = ctypes.byref(hp) if hp is not None else None
+    arrays = [None, None] if null_arrays else [P, P]
+    return L.mica_sgd_steps(*arrays, P if with_buf else None, N, T, gdt, hp_ref, None, None)
+
+
+def _sgd_hp(**kw):
+    d = dict(lr=0.1, momentum=0.9, zero_grad=0, flags=0)
+    d.update(kw)
+    return _SgdHP(**d)
+
+
+def test_sgd_host_validation():
+    assert sgd(hp=None) == NULL
+    assert sgd(hp=_sgd_hp(), gdt=2) == DTYPE
+    for bad in (dict(lr=math.nan), dict(lr=-0.1), dict(momentum=-0.5), dict(momentum=math.inf), dict(flags=2),
+                dict(flags=4)):
+        assert sgd(hp=_sgd_hp(**bad)) == HYPER, bad
+    assert sgd(hp=_sgd_hp(momentum=0.9), with_buf=False) == NULL   # momentum needs its buffers
+    assert sgd(T=-1, hp=_sgd_hp()) == COUNT
+    assert sgd(hp=_sgd_hp(), null_arrays=True) == NULL
+    assert sgd(ptrs=0, hp=_sgd_hp()) == NULL
+    assert sgd(T=0, hp=_sgd_hp()) == OK
+    assert sgd(n=(0,), ptrs=0, hp=_sgd_hp(momentum=0.0), with_buf=False) == OK
 
 
 def test_adamw_needs_device_memory():

@@ -239,6 +239,94 @@ def test_scale_tensors(ora, dtype):
 
 
 # ------------------------------------------------------------------------------------------------------------------
+# AdamW over parameter groups; SGD and SGD with momentum
+# ------------------------------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["gpt2_small", "gpt2_small_bf16", "fp16_scaled"])
+def test_param_groups(ora, name):
+    """Matrices with decay, vectors without and at half the lr, in one launch, against the oracle's per-group step."""
+    if name == "fp16_scaled":
+        shapes = list(W[name].shapes[:700]) + [(768, 3072)] * 2
+    else:
+        shapes = workloads._gpt2_shapes(90, 2, 1003, 67)
+    sizes = [int(np.prod(s)) for s in shapes]
+    r = parity.run_parity_groups(W[name], parity.decay_groups(shapes), sizes=sizes, ora=ora, zero_grad=True)
+    assert r["same_factor_every_step"]
+
+
+def test_param_groups_ragged_and_many(ora):
+    """Eight groups (the most one call takes) assigned round-robin over ragged sizes."""
+    group = [k % 8 for k in range(len(RAGGED))]
+    wl = W["gpt2_small_bf16"]
+    st_hps = [dict(lr=wl.lr * (1 + j) / 8, weight_decay=0.02 * j) for j in range(8)]
+    orig = parity.group_hps
+    parity.group_hps = lambda _wl: st_hps
+    try:
+        r = parity.run_parity_groups(wl, group, sizes=RAGGED, ora=ora)
+    finally:
+        parity.group_hps = orig
+    assert r["same_factor_every_step"]
+
+
+def test_param_groups_index_checked_on_cached_list():
+    """A list first stepped with two groups, then called with one group: refused, not run with a missing group."""
+    wl = W["tiny"]
+    st = workloads.make_state(wl, "cuda")
+    Wl, G, M, V = parity.tensor_lists(st)
+    gi = mica.GroupIndex([0, 1, 0, 1])
+    kw = dict(beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps, step=1)
+    mica.mica_adamw_steps_grouped(Wl, G, M, V, gi, parity.group_hps(wl), **kw)
+    with pytest.raises(mica.MicaError, match="MICA_ERR_COUNT"):
+        mica.mica_adamw_steps_grouped(Wl, G, M, V, gi, parity.group_hps(wl)[:1], **kw)
+    mica.mica_sync()
+
+
+@pytest.mark.parametrize("momentum", [0.0, 0.9])
+@pytest.mark.parametrize("name,sizes", [("tiny", None), ("gpt2_small", "small"), ("gpt2_small", "ragged"),
+                                        ("fp16_scaled", "scaled")])
+def test_sgd(ora, name, sizes, momentum):
+    sz = {None: None, "small": small_gpt2_sizes(), "ragged": RAGGED,
+          "scaled": list(W["fp16_scaled"].sizes[:700]) + [768 * 3072]}[sizes]
+    r = parity.run_parity_sgd(W[name], momentum, sizes=sz, ora=ora, zero_grad=(sizes == "ragged"))
+    assert r["same_factor_every_step"]
+
+
+@pytest.mark.parametrize("momentum", [0.0, 0.9])
+def test_sgd_full_size(ora, momentum):
+    r = parity.run_parity_sgd(W["gpt2_small"], momentum, ora=ora, steps=4, check_every_step=False)
+    assert r["same_factor_every_step"]
+
+
+def test_sgd_skip_step_with_nonfinite_gradient(ora):
+    def poison(st, t):
+        if t == 2:
+            st.g[4].view(-1)[5] = float("inf")  # tensor 4 holds 7 elements
+    r = parity.run_parity_sgd(W["fp16_scaled"], 0.9, sizes=RAGGED, ora=ora, steps=4, zero_grad=True,
+                              skip_nonfinite=True, grad_hook=poison)
+    assert r["same_factor_every_step"]
+
+
+def test_sgd_unaligned(ora):
+    """Tensors one element past a 16-byte boundary take the element path."""
+    wl = W["gpt2_small"]
+    st = _misaligned_state(wl, [1, 7, 9, 1000, 4099], off=1)
+    for t in range(1, 4):
+        for g in st.g:
+            g.copy_(torch.randn(g.numel(), device="cuda", generator=workloads._gen("cuda", 200 + t)) * 0.05)
+        hw, hg, hb, _ = workloads.host_lists(st) if t == 1 else (hw, workloads.host_lists(st)[1], hb, None)
+        d_norm, d_factor = mica.mica_clip_grad_norms(st.g, wl.max_norm)
+        mica.mica_sgd_steps(st.w, st.g, st.m, lr=parity.SGD_LR, momentum=0.9, factor=d_factor)
+        _, o_factor = ora.clip_sgd_step(hw, hg, hb, parity.SGD_LR, 0.9, wl.max_norm)
+        torch.cuda.synchronize()
+        assert np.float32(d_factor.item()) == o_factor
+        gw, _, gb, _ = workloads.host_lists(st)
+        for k in range(len(st.sizes)):
+            parity.exact(gw[k], hw[k], f"step {t} w[{k}]")
+            parity.exact(gb[k], hb[k], f"step {t} buf[{k}]")
+    mica.mica_sync()
+
+
+# ------------------------------------------------------------------------------------------------------------------
 # the full-size workloads, in the benchmark's launch configuration
 # ------------------------------------------------------------------------------------------------------------------
 
