@@ -36,7 +36,7 @@ import workloads  # noqa: E402
 METRIC = "clip+AdamW params/sec and achieved HBM GB/s (% of 8 TB/s roofline), 1 GB300"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SRC = os.path.join(ROOT, "clip_tensor_adamw_gb300", "csrc", "kernels.cu")
+KERNEL_SRCS = [os.path.join(ROOT, "clip_tensor_adamw_gb300", "csrc", f) for f in ("kernels.cu", "stream.cuh")]
 PROFILE = os.path.join(ROOT, "profiles", "adamw_gpt2_small.md")
 
 
@@ -87,13 +87,22 @@ def hbm_peak() -> tuple[float, str]:
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def kernel_source_sha() -> str:
+    """The first 16 hex digits of the SHA-256 of the AdamW kernel's sources (kernels.cu, then stream.cuh)."""
+    h = hashlib.sha256()
+    for path in KERNEL_SRCS:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def profiled_traffic() -> float | None:
     """DRAM bytes per AdamW launch from the committed ncu summary, if it was taken on the current kernel source."""
     try:
         text = open(PROFILE).read()
     except OSError:
         return None
-    sha = hashlib.sha256(open(KERNEL_SRC, "rb").read()).hexdigest()[:16]
+    sha = kernel_source_sha()
     m_sha = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]{16})", text)
     m_b = re.search(r"dram_bytes_per_launch_full_size:\s*([0-9.eE+]+)", text)
     if not m_sha or not m_b or m_sha.group(1) != sha:

@@ -219,15 +219,22 @@ static int sm_count(int device) {
     return n;
 }
 
-// Octets per work item: for AdamW with float32 moments 512 (4,096 elements: 64 KB of loads, a short tail), else 2048
-// (16,384 elements), measured best on GB300; halved down to 128 for small lists so that all SMs still get work.
-// MICA_ITEM_OCTS overrides it (a power of two).
-static int32_t choose_item_octs(int64_t total_octs, int sms, bool f32_moments) {
+// Octets per work item, measured best on GB300 for each kernel and stream set: AdamW with float32 moments 512 (4,096
+// elements: 64 KB of loads, a short tail), AdamW with packed moments and ScaleTensors 2048, SGD 2048, SGD with
+// momentum 1024; halved down to 128 for small lists so that all SMs still get work. MICA_ITEM_OCTS overrides it (a
+// power of two).
+static int32_t base_item_octs(Kind kind, Dtype mdt) {
+    if (kind == kAdamW) return mdt == kF32 ? 512 : 2048;
+    if (kind == kMomentum) return 1024;
+    return 2048;
+}
+
+static int32_t choose_item_octs(int64_t total_octs, int sms, int32_t base) {
     if (const char* s = std::getenv("MICA_ITEM_OCTS")) {
         const long v = std::strtol(s, nullptr, 10);
         if (v >= 16 && v <= (1 << 20) && (v & (v - 1)) == 0) return (int32_t)v;
     }
-    int32_t io = f32_moments ? 512 : 2048;
+    int32_t io = base;
     const int64_t target = (int64_t)sms * 16;
     while (io > 128 && total_octs / io < target) io /= 2;
     return io;
@@ -452,8 +459,7 @@ static mica_status build_plan(const ListDesc& L, int device, uint64_t h, Plan** 
         plan->chunks.grid = grid;
         plan->chunks.total_octs = total_octs;
     } else {
-        plan->item_octs = choose_item_octs(total_octs, sms, (L.kind == kAdamW && L.mdt == kF32) ||
-                                                                L.kind == kSGD || L.kind == kMomentum);
+        plan->item_octs = choose_item_octs(total_octs, sms, base_item_octs(L.kind, L.mdt));
         items = build_items(L.n, L.T, plan->item_octs);
         if (items.size() > (size_t)INT32_MAX) return fail(MICA_ERR_COUNT, "too many work items (%zu)", items.size());
         plan->num_items = (int32_t)items.size();
