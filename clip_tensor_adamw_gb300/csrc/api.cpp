@@ -179,9 +179,10 @@ struct Plan {
     int32_t max_group = 0;             // the largest entry of `group`
     int64_t total = 0;                 // elements
     const void* checked_scalar[2] = {nullptr, nullptr};  // the last scalar outputs found valid for this list
-    void* dev = nullptr;  // one allocation: TensorRec[T] | WorkItem[I] | double[I] (norm)
+    void* dev = nullptr;  // one allocation: TensorRec[T] | WorkItem[I] | pack table | the norm's tables
     TensorRec* recs = nullptr;
     WorkItem* items = nullptr;
+    int32_t* pack_pre = nullptr;  // per pack: the first pack octet of each tensor, and the total
     int32_t num_items = 0;
     int32_t item_octs = 0;
     // norm plans
@@ -240,15 +241,26 @@ static int32_t choose_item_octs(int64_t total_octs, int sms, int32_t base) {
     return io;
 }
 
-// Work items over the tensors' octets (see plan.h).
-static std::vector<WorkItem> build_items(const int64_t* n, int32_t T, int32_t io) {
+// Work items over the tensors' octets (see plan.h), and the pack table: for each pack of two or more tensors, the
+// first pack octet of each of its tensors and the pack's total (its item's o0 says where they start).
+static std::vector<WorkItem> build_items(const int64_t* n, int32_t T, int32_t io, std::vector<int32_t>* pack_pre) {
     std::vector<WorkItem> items;
     const int64_t small = io / 2;
     bool open = false;
     WorkItem pack{};
     int64_t pack_o = 0;
     auto close = [&] {
-        if (open) items.push_back(pack);
+        if (!open) return;
+        if (pack.count > 1) {
+            pack.o0 = (int64_t)pack_pre->size();
+            int32_t at = 0;
+            for (int32_t j = 0; j < pack.count; ++j) {
+                pack_pre->push_back(at);
+                at += (int32_t)((n[pack.t + j] + kOct - 1) / kOct);
+            }
+            pack_pre->push_back(at);
+        }
+        items.push_back(pack);
         open = false;
     };
     for (int32_t k = 0; k < T; ++k) {
@@ -435,6 +447,7 @@ static mica_status build_plan(const ListDesc& L, int device, uint64_t h, Plan** 
 
     const int sms = sm_count(device);
     std::vector<WorkItem> items;
+    std::vector<int32_t> pack_pre;
     std::vector<int64_t> prefix;
     std::vector<int32_t> first;
     int64_t nonempty = 0;
@@ -460,7 +473,7 @@ static mica_status build_plan(const ListDesc& L, int device, uint64_t h, Plan** 
         plan->chunks.total_octs = total_octs;
     } else {
         plan->item_octs = choose_item_octs(total_octs, sms, base_item_octs(L.kind, L.mdt));
-        items = build_items(L.n, L.T, plan->item_octs);
+        items = build_items(L.n, L.T, plan->item_octs, &pack_pre);
         if (items.size() > (size_t)INT32_MAX) return fail(MICA_ERR_COUNT, "too many work items (%zu)", items.size());
         plan->num_items = (int32_t)items.size();
     }
@@ -469,7 +482,9 @@ static mica_status build_plan(const ListDesc& L, int device, uint64_t h, Plan** 
     const size_t rec_b = recs.size() * sizeof(TensorRec);
     const size_t item_off = up(rec_b);
     const size_t item_b = items.size() * sizeof(WorkItem);
-    const size_t prefix_off = up(item_off + item_b);
+    const size_t pack_off = up(item_off + item_b);
+    const size_t pack_b = pack_pre.size() * sizeof(int32_t);
+    const size_t prefix_off = up(pack_off + pack_b);
     const size_t prefix_b = prefix.size() * sizeof(int64_t);
     const size_t first_off = up(prefix_off + prefix_b);
     const size_t first_b = first.size() * sizeof(int32_t);
@@ -487,6 +502,7 @@ static mica_status build_plan(const ListDesc& L, int device, uint64_t h, Plan** 
     char* base = static_cast<char*>(plan->dev);
     plan->recs = reinterpret_cast<TensorRec*>(base);
     plan->items = reinterpret_cast<WorkItem*>(base + item_off);
+    plan->pack_pre = reinterpret_cast<int32_t*>(base + pack_off);
     if (chunked) {
         plan->chunks.recs = plan->recs;
         plan->chunks.prefix = reinterpret_cast<const int64_t*>(base + prefix_off);
@@ -503,6 +519,9 @@ static mica_status build_plan(const ListDesc& L, int device, uint64_t h, Plan** 
         return cuda_fail(e, "uploading the tensor records");
     if (item_b && (e = cudaMemcpyAsync(plan->items, items.data(), item_b, cudaMemcpyHostToDevice, st)) != cudaSuccess)
         return cuda_fail(e, "uploading the work items");
+    if (pack_b && (e = cudaMemcpyAsync(plan->pack_pre, pack_pre.data(), pack_b, cudaMemcpyHostToDevice, st)) !=
+                      cudaSuccess)
+        return cuda_fail(e, "uploading the pack table");
     if (prefix_b && (e = cudaMemcpyAsync(base + prefix_off, prefix.data(), prefix_b, cudaMemcpyHostToDevice, st)) !=
                         cudaSuccess)
         return cuda_fail(e, "uploading the octet prefix");
@@ -749,8 +768,8 @@ static mica_status adamw_steps(float* const* w, void* const* g, void* const* m, 
         gs.dec[j] = (float)(1.0 - hp[j].lr * hp[j].weight_decay);
         gs.wd[j] = (float)hp[j].weight_decay;
     }
-    return after_launch(launch_adamw(p->recs, p->items, p->num_items, p->item_octs, (Dtype)gdt, (Dtype)mdt, coupled,
-                                     sc, group ? &gs : nullptr, d_factor, stream),
+    return after_launch(launch_adamw(p->recs, p->items, p->pack_pre, p->num_items, p->item_octs, (Dtype)gdt,
+                                     (Dtype)mdt, coupled, sc, group ? &gs : nullptr, d_factor, stream),
                         stream, "AdamWSteps launch");
 }
 
@@ -808,7 +827,8 @@ extern "C" mica_status mica_sgd_steps(float* const* w, void* const* g, float* co
     sc.neg_lr = -(float)hp->lr;
     sc.mu = (float)hp->momentum;
     sc.zero_grad = hp->zero_grad ? 1 : 0;
-    return after_launch(launch_sgd(p->recs, p->items, p->num_items, p->item_octs, (Dtype)gdt, buf != nullptr,
+    return after_launch(launch_sgd(p->recs, p->items, p->pack_pre, p->num_items, p->item_octs, (Dtype)gdt,
+                                   buf != nullptr,
                                    (hp->flags & MICA_STEP_SKIP_NONFINITE) != 0, sc, d_factor, stream),
                         stream, "SGDSteps launch");
 }

@@ -185,6 +185,43 @@ __device__ __forceinline__ void prefetch_octets(const TensorRec& r, int64_t a, i
     prefetch_l2(static_cast<const char*>(r.v) + a * L::kVb, n * L::kVb);
 }
 
+// One whole octet of a tensor whose bases are aligned for the vectors: 256-bit loads (128-bit for binary16 g and
+// packed moments), the update in registers, 256-bit streaming stores.
+template <Dtype G, Dtype M, bool kCoupled, bool kSkip>
+__device__ __forceinline__ void adam_vec_octet(const TensorRec& r, int64_t o, const StepScalars& s, Factor& fac) {
+    using L = MomentLayout<M>;
+    float w[8], g[8], m[8], v[8];
+    uint4 gh, mp, vp;
+    ld8_stream(r.w + kOct * o, w);
+    if constexpr (G == kF16) gh = ld16_stream(static_cast<const __half*>(r.g) + kOct * o);
+    else ld8_stream(static_cast<const float*>(r.g) + kOct * o, g);
+    if constexpr (L::kMPacked) mp = ld16_stream(static_cast<const uint32_t*>(r.m) + 4 * o);
+    else ld8_stream(static_cast<const float*>(r.m) + kOct * o, m);
+    if constexpr (L::kVPacked) vp = ld16_stream(static_cast<const uint32_t*>(r.v) + 4 * o);
+    else ld8_stream(static_cast<const float*>(r.v) + kOct * o, v);
+    const float f = fac.get();
+    if (!skip_step<kSkip>(f)) {
+        uint32_t pm[4], pv[4];
+        if constexpr (G == kF16) h8_to(gh, g);
+        if constexpr (L::kMPacked) bf8_to(mp, m);
+        if constexpr (L::kVPacked) bf8_to(vp, v);
+        adam8<M, kCoupled>(w, g, m, v, pm, pv, s, f);
+        st8(r.w + kOct * o, w);
+        if constexpr (L::kMPacked) st16(static_cast<uint32_t*>(r.m) + 4 * o, make_uint4(pm[0], pm[1], pm[2], pm[3]));
+        else st8(static_cast<float*>(r.m) + kOct * o, m);
+        if constexpr (L::kVPacked) st16(static_cast<uint32_t*>(r.v) + 4 * o, make_uint4(pv[0], pv[1], pv[2], pv[3]));
+        else st8(static_cast<float*>(r.v) + kOct * o, v);
+    }
+    if (s.zero_grad) {
+        if constexpr (G == kF16) {
+            st16(static_cast<__half*>(r.g) + kOct * o, make_uint4(0u, 0u, 0u, 0u));
+        } else {
+            const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            st8(static_cast<float*>(r.g) + kOct * o, z);
+        }
+    }
+}
+
 // Octets [ob, oe) of one tensor: octet ob + lane first, then every `stride`-th. With `prefetch` (a whole CTA on
 // one slice: lane is the thread index and stride the CTA size) thread 0 asks L2 for the rounds one and two ahead,
 // so that the other threads' loads of those rounds find their data in L2 rather than waiting on DRAM.
@@ -201,36 +238,7 @@ __device__ __forceinline__ void adam_range(const TensorRec& r, int64_t ob, int64
         for (int64_t o = ob + lane; o < vend; o += round) {
             if (prefetch && lane == 0 && o + 2 * round < vend)
                 prefetch_octets<G, M>(r, o + 2 * round, o + 3 * round < vend ? o + 3 * round : vend);
-            float w[8], g[8], m[8], v[8];
-            uint4 gh, mp, vp;
-            ld8_stream(r.w + kOct * o, w);
-            if constexpr (G == kF16) gh = ld16_stream(static_cast<const __half*>(r.g) + kOct * o);
-            else ld8_stream(static_cast<const float*>(r.g) + kOct * o, g);
-            if constexpr (L::kMPacked) mp = ld16_stream(static_cast<const uint32_t*>(r.m) + 4 * o);
-            else ld8_stream(static_cast<const float*>(r.m) + kOct * o, m);
-            if constexpr (L::kVPacked) vp = ld16_stream(static_cast<const uint32_t*>(r.v) + 4 * o);
-            else ld8_stream(static_cast<const float*>(r.v) + kOct * o, v);
-            const float f = fac.get();
-            if (!skip_step<kSkip>(f)) {
-                uint32_t pm[4], pv[4];
-                if constexpr (G == kF16) h8_to(gh, g);
-                if constexpr (L::kMPacked) bf8_to(mp, m);
-                if constexpr (L::kVPacked) bf8_to(vp, v);
-                adam8<M, kCoupled>(w, g, m, v, pm, pv, s, f);
-                st8(r.w + kOct * o, w);
-                if constexpr (L::kMPacked) st16(static_cast<uint32_t*>(r.m) + 4 * o, make_uint4(pm[0], pm[1], pm[2], pm[3]));
-                else st8(static_cast<float*>(r.m) + kOct * o, m);
-                if constexpr (L::kVPacked) st16(static_cast<uint32_t*>(r.v) + 4 * o, make_uint4(pv[0], pv[1], pv[2], pv[3]));
-                else st8(static_cast<float*>(r.v) + kOct * o, v);
-            }
-            if (s.zero_grad) {
-                if constexpr (G == kF16) {
-                    st16(static_cast<__half*>(r.g) + kOct * o, make_uint4(0u, 0u, 0u, 0u));
-                } else {
-                    const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                    st8(static_cast<float*>(r.g) + kOct * o, z);
-                }
-            }
+            adam_vec_octet<G, M, kCoupled, kSkip>(r, o, s, fac);
         }
         // the last, partial octet (n % 8 != 0), when it lies in this range
         if (full < oe && full >= ob && lane == (int)((full - ob) % stride))
@@ -253,18 +261,44 @@ __device__ __forceinline__ StepScalars group_scalars(const StepScalars& s, const
     return x;
 }
 
+// A pack of small tensors (t .. t+count-1, whole): their octets, concatenated, are spread over the CTA's threads,
+// thread i taking pack octets i, i + 256, ..., so that every thread has work however small the tensors are.
+// pre[0..count] (in the list's pack table, from entry item.o0) holds the first pack octet of each tensor and the
+// pack's total; a thread finds its octet's tensor by binary search from the last one it found.
+template <Dtype G, Dtype M, bool kCoupled, bool kSkip, bool kGrouped>
+__device__ __forceinline__ void adam_pack(const TensorRec* __restrict__ recs, const WorkItem& item,
+                                          const int32_t* __restrict__ pack_pre, const StepScalars& s,
+                                          const GroupScalars& gs, Factor& fac) {
+    const int32_t* pre = pack_pre + item.o0;
+    const int32_t total = __ldg(pre + item.count);
+    int32_t j = 0;
+    for (int32_t q = threadIdx.x; q < total; q += kThreads) {
+        int32_t hi = item.count - 1;  // the last j with pre[j] <= q: pre[j] <= q holds already
+        while (j < hi) {
+            const int32_t mid = (j + hi + 1) >> 1;
+            if (__ldg(pre + mid) <= q) j = mid;
+            else hi = mid - 1;
+        }
+        const TensorRec r = recs[item.t + j];
+        const int64_t o = q - __ldg(pre + j);
+        const StepScalars x = group_scalars<kGrouped>(s, gs, r);
+        if (r.vec && o < r.n / kOct) adam_vec_octet<G, M, kCoupled, kSkip>(r, o, x, fac);
+        else adam_oct_elements<G, M, kCoupled, kSkip>(r, o, x, fac);
+    }
+}
+
 // One CTA per work item, items taken in reverse order (the norm reads them forwards, so the gradient it read last
 // may still be in L2 when this kernel starts). Without kGrouped the scalars are read straight from the kernel's
 // parameters; with it each tensor's group picks its own (the parameter array is indexed in place).
 template <Dtype G, Dtype M, bool kCoupled, bool kSkip, bool kGrouped>
 __global__ void __launch_bounds__(kThreads, 3) adamw_kernel(const TensorRec* __restrict__ recs,
                                                             const WorkItem* __restrict__ items, int32_t num_items,
-                                                            int32_t item_octs, StepScalars s,
+                                                            int32_t item_octs,
+                                                            const int32_t* __restrict__ pack_pre, StepScalars s,
                                                             const __grid_constant__ GroupScalars gs,
                                                             const float* __restrict__ d_factor) {
     allow_dependents();  // the next step's norm may launch and set up while this kernel's last CTAs run
     Factor fac{d_factor, 1.0f, false};
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int32_t k = blockIdx.x; k < num_items; k += gridDim.x) {
         const WorkItem item = items[num_items - 1 - k];
         if (item.count == 1) {
@@ -278,15 +312,7 @@ __global__ void __launch_bounds__(kThreads, 3) adamw_kernel(const TensorRec* __r
                 adam_range<G, M, kCoupled, kSkip>(r, item.o0, oe, threadIdx.x, kThreads, s, fac, true);
             }
         } else {
-            for (int j = warp; j < item.count; j += kWarps) {
-                const TensorRec r = recs[item.t + j];
-                if constexpr (kGrouped) {
-                    const StepScalars x = group_scalars<kGrouped>(s, gs, r);
-                    adam_range<G, M, kCoupled, kSkip>(r, 0, (r.n + kOct - 1) / kOct, lane, 32, x, fac);
-                } else {
-                    adam_range<G, M, kCoupled, kSkip>(r, 0, (r.n + kOct - 1) / kOct, lane, 32, s, fac);
-                }
-            }
+            adam_pack<G, M, kCoupled, kSkip, kGrouped>(recs, item, pack_pre, s, gs, fac);
         }
     }
 }
@@ -831,6 +857,7 @@ __global__ void __launch_bounds__(kThreads) scale_kernel(const TensorRec* __rest
 struct AdamwLaunch {
     const WorkItem* items;
     const TensorRec* recs;
+    const int32_t* pack_pre;
     int32_t num_items, item_octs;
     cudaStream_t st;
     const StepScalars* s;
@@ -852,7 +879,7 @@ cudaError_t launch_adamw_t(const AdamwLaunch& a) {
     cfg.numAttrs = 1;
     const GroupScalars gs = a.groups ? *a.groups : GroupScalars{};
     return cudaLaunchKernelEx(&cfg, adamw_kernel<G, M, kCoupled, kSkip, kGrouped>, a.recs, a.items, a.num_items,
-                              a.item_octs, *a.s, gs, a.d_factor);
+                              a.item_octs, a.pack_pre, *a.s, gs, a.d_factor);
 }
 
 template <Dtype G, Dtype M, bool kCoupled, bool kSkip>
@@ -880,11 +907,12 @@ cudaError_t launch_adamw_m(Dtype mdt, bool coupled, const AdamwLaunch& a) {
 // launchers
 // ------------------------------------------------------------------------------------------------------------------
 
-int launch_adamw(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_octs, Dtype gdt,
-                 Dtype mdt, bool coupled, const StepScalars& s, const GroupScalars* groups, const float* d_factor,
-                 void* stream) {
+int launch_adamw(const TensorRec* recs, const WorkItem* items, const int32_t* pack_pre, int32_t num_items,
+                 int32_t item_octs, Dtype gdt, Dtype mdt, bool coupled, const StepScalars& s,
+                 const GroupScalars* groups, const float* d_factor, void* stream) {
     if (num_items <= 0) return (int)cudaSuccess;
-    const AdamwLaunch a{items, recs, num_items, item_octs, static_cast<cudaStream_t>(stream), &s, groups, d_factor};
+    const AdamwLaunch a{items, recs, pack_pre, num_items, item_octs, static_cast<cudaStream_t>(stream), &s, groups,
+                        d_factor};
     const cudaError_t e = (gdt == kF16) ? launch_adamw_m<kF16>(mdt, coupled, a) : launch_adamw_m<kF32>(mdt, coupled, a);
     count_launches(1);
     return (int)(e != cudaSuccess ? e : cudaGetLastError());

@@ -10,9 +10,11 @@
 //
 // Work items are counted in octets (8 consecutive elements: one 32-byte float32 vector, one 16-byte vector of
 // binary16 values or of 4 packed BF16 words). A large tensor is cut into slices of `item_octs` octets; runs of
-// consecutive small tensors (each at most item_octs / 2 octets) are packed into one item whose tensors the CTA's
-// warps share out. Every element belongs to exactly one item, so each element is read and written by exactly one
-// thread per launch and the results do not depend on how items are scheduled.
+// consecutive small tensors (each at most item_octs / 2 octets) are packed into one item whose octets the CTA's
+// threads share out one by one (the list's pack table holds, per pack, the first pack octet of each of its tensors
+// and the pack's total; ScaleTensors instead gives each warp whole tensors). Every element belongs to exactly one
+// item, so each element is read and written by exactly one thread per launch and the results do not depend on how
+// items are scheduled.
 #pragma once
 
 #include <cstdint>
@@ -38,7 +40,7 @@ static_assert(sizeof(TensorRec) == 48, "TensorRec layout");
 struct WorkItem {
     int32_t t;      // first tensor
     int32_t count;  // 1: octets [o0, min(o0 + item_octs, ceil(n/8))) of tensor t; > 1: tensors t .. t+count-1 whole
-    int64_t o0;     // first octet of a slice (0 for a pack)
+    int64_t o0;     // a slice: its first octet; a pack: where its count + 1 entries start in the pack table
 };
 static_assert(sizeof(WorkItem) == 16, "WorkItem layout");
 
@@ -110,13 +112,14 @@ enum Dtype : int32_t { kF32 = 0, kF16 = 1, kBF16x2 = 2, kBF16x2M = 3 };
 // programmatic dependent of the kernel queued before it: it may start and load its tensors while that kernel
 // finishes, and reads d_factor only once that kernel has completed. With `groups`, tensor k takes neg_step, dec and
 // wd from entry recs[k].group of it instead of from s.
-int launch_adamw(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_octs, Dtype gdt,
-                 Dtype mdt, bool coupled, const StepScalars& s, const GroupScalars* groups, const float* d_factor,
-                 void* stream);
+int launch_adamw(const TensorRec* recs, const WorkItem* items, const int32_t* pack_pre, int32_t num_items,
+                 int32_t item_octs, Dtype gdt, Dtype mdt, bool coupled, const StepScalars& s,
+                 const GroupScalars* groups, const float* d_factor, void* stream);
 // SGD (momentum false) or SGD with momentum over every item, launched as AdamW is. `skip`: leave w (and the
 // buffer) as they are when the factor is not > 0.
-int launch_sgd(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_octs, Dtype gdt,
-               bool momentum, bool skip, const SgdScalars& s, const float* d_factor, void* stream);
+int launch_sgd(const TensorRec* recs, const WorkItem* items, const int32_t* pack_pre, int32_t num_items,
+               int32_t item_octs, Dtype gdt, bool momentum, bool skip, const SgdScalars& s, const float* d_factor,
+               void* stream);
 // The joint norm in one launch of ct.grid CTAs: one partial square sum per CTA into `partials` (ct.grid doubles),
 // and the CTA that finishes last sums them in a fixed order and writes norm and factor. `ticket` must be 0 before
 // the launch; the kernel leaves it 0.

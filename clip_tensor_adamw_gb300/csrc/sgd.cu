@@ -4,10 +4,10 @@
 // gh = g * f, f the factor of the joint-norm clip (and of the loss-scale unscale), read from device memory.
 //
 // Same work items and access scheme as the AdamW kernel: one CTA per item (a slice of a large tensor, or a pack of
-// small tensors shared out one per warp), 32-byte streaming loads and stores, L2 prefetch two rounds ahead on the
-// slices, and a programmatic-dependent launch so that the loads start while the norm kernel finishes. Every float
-// operation is a separate correctly rounded intrinsic, in the page's order, so the result is bit-identical to the
-// same step on the CPU.
+// small tensors whose octets the threads share out), 32-byte streaming loads and stores, L2 prefetch two rounds
+// ahead on the slices, and a programmatic-dependent launch so that the loads start while the norm kernel finishes.
+// Every float operation is a separate correctly rounded intrinsic, in the page's order, so the result is
+// bit-identical to the same step on the CPU.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -81,6 +81,32 @@ __device__ __forceinline__ void sgd_prefetch(const TensorRec& r, int64_t a, int6
     if constexpr (kMomentum) prefetch_l2(static_cast<const char*>(r.m) + a * 32, n * 32);
 }
 
+// One whole octet of a tensor whose bases are aligned for the vectors.
+template <Dtype G, bool kMomentum, bool kSkip>
+__device__ __forceinline__ void sgd_vec_octet(const TensorRec& r, int64_t o, const SgdScalars& s, Factor& fac) {
+    float w[8], g[8], b[8];
+    uint4 gh;
+    ld8_stream(r.w + kOct * o, w);
+    if constexpr (G == kF16) gh = ld16_stream(static_cast<const __half*>(r.g) + kOct * o);
+    else ld8_stream(static_cast<const float*>(r.g) + kOct * o, g);
+    if constexpr (kMomentum) ld8_stream(static_cast<const float*>(r.m) + kOct * o, b);
+    const float f = fac.get();
+    if (!skip_step<kSkip>(f)) {
+        if constexpr (G == kF16) h8_to(gh, g);
+        sgd8<kMomentum>(w, g, b, s, f);
+        st8(r.w + kOct * o, w);
+        if constexpr (kMomentum) st8(static_cast<float*>(r.m) + kOct * o, b);
+    }
+    if (s.zero_grad) {
+        if constexpr (G == kF16) {
+            st16(static_cast<__half*>(r.g) + kOct * o, make_uint4(0u, 0u, 0u, 0u));
+        } else {
+            const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            st8(static_cast<float*>(r.g) + kOct * o, z);
+        }
+    }
+}
+
 // Octets [ob, oe) of one tensor: octet ob + lane first, then every `stride`-th; with `prefetch` (a whole CTA on one
 // slice) thread 0 asks L2 for the rounds one and two ahead.
 template <Dtype G, bool kMomentum, bool kSkip>
@@ -94,27 +120,7 @@ __device__ __forceinline__ void sgd_range(const TensorRec& r, int64_t ob, int64_
         for (int64_t o = ob + lane; o < vend; o += stride) {
             if (prefetch && lane == 0 && o + 2 * stride < vend)
                 sgd_prefetch<G, kMomentum>(r, o + 2 * stride, o + 3 * stride < vend ? o + 3 * stride : vend);
-            float w[8], g[8], b[8];
-            uint4 gh;
-            ld8_stream(r.w + kOct * o, w);
-            if constexpr (G == kF16) gh = ld16_stream(static_cast<const __half*>(r.g) + kOct * o);
-            else ld8_stream(static_cast<const float*>(r.g) + kOct * o, g);
-            if constexpr (kMomentum) ld8_stream(static_cast<const float*>(r.m) + kOct * o, b);
-            const float f = fac.get();
-            if (!skip_step<kSkip>(f)) {
-                if constexpr (G == kF16) h8_to(gh, g);
-                sgd8<kMomentum>(w, g, b, s, f);
-                st8(r.w + kOct * o, w);
-                if constexpr (kMomentum) st8(static_cast<float*>(r.m) + kOct * o, b);
-            }
-            if (s.zero_grad) {
-                if constexpr (G == kF16) {
-                    st16(static_cast<__half*>(r.g) + kOct * o, make_uint4(0u, 0u, 0u, 0u));
-                } else {
-                    const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                    st8(static_cast<float*>(r.g) + kOct * o, z);
-                }
-            }
+            sgd_vec_octet<G, kMomentum, kSkip>(r, o, s, fac);
         }
         if (full < oe && full >= ob && lane == (int)((full - ob) % stride))
             sgd_oct_elements<G, kMomentum, kSkip>(r, full, s, fac);
@@ -123,14 +129,34 @@ __device__ __forceinline__ void sgd_range(const TensorRec& r, int64_t ob, int64_
     }
 }
 
+// A pack of small tensors, its octets spread over the CTA's threads (as the AdamW kernel's packs).
+template <Dtype G, bool kMomentum, bool kSkip>
+__device__ __forceinline__ void sgd_pack(const TensorRec* __restrict__ recs, const WorkItem& item,
+                                         const int32_t* __restrict__ pack_pre, const SgdScalars& s, Factor& fac) {
+    const int32_t* pre = pack_pre + item.o0;
+    const int32_t total = __ldg(pre + item.count);
+    int32_t j = 0;
+    for (int32_t q = threadIdx.x; q < total; q += kThreads) {
+        int32_t hi = item.count - 1;
+        while (j < hi) {
+            const int32_t mid = (j + hi + 1) >> 1;
+            if (__ldg(pre + mid) <= q) j = mid;
+            else hi = mid - 1;
+        }
+        const TensorRec r = recs[item.t + j];
+        const int64_t o = q - __ldg(pre + j);
+        if (r.vec && o < r.n / kOct) sgd_vec_octet<G, kMomentum, kSkip>(r, o, s, fac);
+        else sgd_oct_elements<G, kMomentum, kSkip>(r, o, s, fac);
+    }
+}
+
 template <Dtype G, bool kMomentum, bool kSkip>
 __global__ void __launch_bounds__(kThreads, 3) sgd_kernel(const TensorRec* __restrict__ recs,
                                                           const WorkItem* __restrict__ items, int32_t num_items,
-                                                          int32_t item_octs, SgdScalars s,
-                                                          const float* __restrict__ d_factor) {
+                                                          int32_t item_octs, const int32_t* __restrict__ pack_pre,
+                                                          SgdScalars s, const float* __restrict__ d_factor) {
     allow_dependents();
     Factor fac{d_factor, 1.0f, false};
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int32_t k = blockIdx.x; k < num_items; k += gridDim.x) {
         const WorkItem item = items[num_items - 1 - k];
         if (item.count == 1) {
@@ -139,17 +165,14 @@ __global__ void __launch_bounds__(kThreads, 3) sgd_kernel(const TensorRec* __res
             const int64_t oe = item.o0 + item_octs < no ? item.o0 + item_octs : no;
             sgd_range<G, kMomentum, kSkip>(r, item.o0, oe, threadIdx.x, kThreads, s, fac, true);
         } else {
-            for (int j = warp; j < item.count; j += kWarps) {
-                const TensorRec r = recs[item.t + j];
-                sgd_range<G, kMomentum, kSkip>(r, 0, (r.n + kOct - 1) / kOct, lane, 32, s, fac);
-            }
+            sgd_pack<G, kMomentum, kSkip>(recs, item, pack_pre, s, fac);
         }
     }
 }
 
 template <Dtype G, bool kMomentum, bool kSkip>
-cudaError_t launch_sgd_t(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_octs,
-                         const SgdScalars& s, const float* d_factor, cudaStream_t st) {
+cudaError_t launch_sgd_t(const TensorRec* recs, const WorkItem* items, const int32_t* pack_pre, int32_t num_items,
+                         int32_t item_octs, const SgdScalars& s, const float* d_factor, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_items);
     cfg.blockDim = dim3(kThreads);
@@ -159,28 +182,31 @@ cudaError_t launch_sgd_t(const TensorRec* recs, const WorkItem* items, int32_t n
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, sgd_kernel<G, kMomentum, kSkip>, recs, items, num_items, item_octs, s, d_factor);
+    return cudaLaunchKernelEx(&cfg, sgd_kernel<G, kMomentum, kSkip>, recs, items, num_items, item_octs, pack_pre, s,
+                              d_factor);
 }
 
 template <Dtype G>
-cudaError_t launch_sgd_g(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_octs,
-                         bool momentum, bool skip, const SgdScalars& s, const float* d_factor, cudaStream_t st) {
+cudaError_t launch_sgd_g(const TensorRec* recs, const WorkItem* items, const int32_t* pp, int32_t num_items,
+                         int32_t item_octs, bool momentum, bool skip, const SgdScalars& s, const float* d_factor,
+                         cudaStream_t st) {
     if (momentum)
-        return skip ? launch_sgd_t<G, true, true>(recs, items, num_items, item_octs, s, d_factor, st)
-                    : launch_sgd_t<G, true, false>(recs, items, num_items, item_octs, s, d_factor, st);
-    return skip ? launch_sgd_t<G, false, true>(recs, items, num_items, item_octs, s, d_factor, st)
-                : launch_sgd_t<G, false, false>(recs, items, num_items, item_octs, s, d_factor, st);
+        return skip ? launch_sgd_t<G, true, true>(recs, items, pp, num_items, item_octs, s, d_factor, st)
+                    : launch_sgd_t<G, true, false>(recs, items, pp, num_items, item_octs, s, d_factor, st);
+    return skip ? launch_sgd_t<G, false, true>(recs, items, pp, num_items, item_octs, s, d_factor, st)
+                : launch_sgd_t<G, false, false>(recs, items, pp, num_items, item_octs, s, d_factor, st);
 }
 
 }  // namespace
 
-int launch_sgd(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_octs, Dtype gdt,
-               bool momentum, bool skip, const SgdScalars& s, const float* d_factor, void* stream) {
+int launch_sgd(const TensorRec* recs, const WorkItem* items, const int32_t* pack_pre, int32_t num_items,
+               int32_t item_octs, Dtype gdt, bool momentum, bool skip, const SgdScalars& s, const float* d_factor,
+               void* stream) {
     if (num_items <= 0) return (int)cudaSuccess;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const cudaError_t e =
-        (gdt == kF16) ? launch_sgd_g<kF16>(recs, items, num_items, item_octs, momentum, skip, s, d_factor, st)
-                      : launch_sgd_g<kF32>(recs, items, num_items, item_octs, momentum, skip, s, d_factor, st);
+        (gdt == kF16) ? launch_sgd_g<kF16>(recs, items, pack_pre, num_items, item_octs, momentum, skip, s, d_factor, st)
+                      : launch_sgd_g<kF32>(recs, items, pack_pre, num_items, item_octs, momentum, skip, s, d_factor, st);
     count_launches(1);
     return (int)(e != cudaSuccess ? e : cudaGetLastError());
 }
