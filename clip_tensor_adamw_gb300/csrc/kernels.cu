@@ -470,41 +470,55 @@ __device__ __noinline__ double sumsq_chunk_double(const ChunkTable& ct, int32_t 
     return t;
 }
 
-// Gradient octet `o` of the list (zeros past the chunk's end or the tensor's end): one 32-byte load (16 for
-// binary16) when the octet is whole and its tensor aligned, else element by element. Normal L2 priority, so the
-// part of the gradient read last may still be in L2 when the AdamW kernel, which walks backwards, reads it again.
+// Up to kStaged consecutive tensors of a chunk, staged in shared memory: tensor i holds the list's octets
+// [lo[i], lo[i + 1]), its gradient starts at base[i] and has n[i] elements, vec[i] says whether it is aligned for
+// the vector loads.
+constexpr int kStaged = 256;
+struct StagedSpan {
+    int64_t lo[kStaged + 1];
+    const char* base[kStaged];
+    int64_t n[kStaged];
+    int32_t vec[kStaged];
+};
+
+// Gradient octet `local` of staged tensor j (zeros past its end): one 32-byte load (16 for binary16) when whole and
+// aligned, else element by element.
 template <Dtype G>
-__device__ __forceinline__ void load_grad_octet(const ChunkTable& ct, Cursor& c, int64_t o, int64_t c1,
-                                                float (&x)[8]) {
-    if (o >= c1) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) x[j] = 0.0f;
-        return;
-    }
-    c.advance(ct, o);
-    const int64_t local = o - c.lo;
-    if (c.vec && local < c.full) {
+__device__ __forceinline__ void load_staged_octet(const StagedSpan& sp, int32_t j, int64_t local, float (&x)[8]) {
+    const char* base = sp.base[j];
+    const int64_t n = sp.n[j];
+    if (sp.vec[j] && local < n / kOct) {
         if constexpr (G == kF16) {
             uint4 h;
             asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                          : "=r"(h.x), "=r"(h.y), "=r"(h.z), "=r"(h.w)
-                         : "l"(c.base + local * 16));
+                         : "l"(base + local * 16));
             h8_to(h, x);
         } else {
             asm volatile("ld.global.L1::no_allocate.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                          : "=f"(x[0]), "=f"(x[1]), "=f"(x[2]), "=f"(x[3]), "=f"(x[4]), "=f"(x[5]), "=f"(x[6]),
                            "=f"(x[7])
-                         : "l"(c.base + local * 32));
+                         : "l"(base + local * 32));
         }
-    } else {  // a tensor's partial last octet, or an unaligned tensor
-        load_elements<G>(c, local, x);
+    } else {
+        const int64_t i0 = local * kOct;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            if (i0 + e < n) {
+                x[e] = (G == kF16) ? __half2float(reinterpret_cast<const __half*>(base)[i0 + e])
+                                   : reinterpret_cast<const float*>(base)[i0 + e];
+            } else {
+                x[e] = 0.0f;
+            }
+        }
     }
 }
 
 // The joint norm for lists of many small tensors, where a stage of the TMA pipeline would cross several tensors:
-// CTA b streams its equal, contiguous chunk of the list's octets straight into registers. Thread t takes octets
-// c0 + t, c0 + t + 256, ..., two at a time, the next two always loading while the current two are summed, each
-// thread following the tensor boundaries with its own cursor; the rest is as in norm_tma_kernel.
+// CTA b streams its equal, contiguous chunk of the list's octets straight into registers. The CTA stages the
+// chunk's tensors (their octet ranges, bases, sizes) in shared memory up to kStaged at a time; thread t takes the
+// staged span's octets c + t, c + t + 256, ..., four at a time (all four loads in flight before they are summed),
+// finding each octet's tensor by walking the staged table forwards. The rest is as in norm_tma_kernel.
 template <Dtype G, bool kScaled>
 __global__ void __launch_bounds__(kThreads, kNormDirectCtasPerSm) norm_direct_kernel(ChunkTable ct, float inv_scale,
                                                                         double* __restrict__ partials,
@@ -512,6 +526,7 @@ __global__ void __launch_bounds__(kThreads, kNormDirectCtasPerSm) norm_direct_ke
                                                                         float* d_norm, float* d_factor) {
     __shared__ double red[kWarps];
     __shared__ int last;
+    __shared__ StagedSpan sp;
     allow_dependents();
     const int t = threadIdx.x;
     const int64_t c0 = ct.total_octs * blockIdx.x / ct.grid;
@@ -519,27 +534,41 @@ __global__ void __launch_bounds__(kThreads, kNormDirectCtasPerSm) norm_direct_ke
     const int32_t k0 = ct.first[blockIdx.x];
 
     SumSq acc{{0.f, 0.f}, {0.f, 0.f}, 0.f};
-    Cursor cur;
-    cur.init(ct, k0);
     wait_prerequisite();  // the kernel queued before may still be writing the gradients (zero_grad)
-    auto sum2 = [&](const float (&a)[8], const float (&b)[8]) {
-        acc.add8<kScaled>(a, inv_scale);
-        acc.add8<kScaled>(b, inv_scale);
-    };
-    float A0[8], A1[8], B0[8], B1[8];
-    int64_t o = c0 + t;
-    load_grad_octet<G>(ct, cur, o, c1, A0);
-    load_grad_octet<G>(ct, cur, o + kThreads, c1, A1);
-    while (o < c1) {
-        const int64_t ob = o + 2 * kThreads;
-        load_grad_octet<G>(ct, cur, ob, c1, B0);
-        load_grad_octet<G>(ct, cur, ob + kThreads, c1, B1);
-        sum2(A0, A1);
-        if (ob >= c1) break;
-        o = ob + 2 * kThreads;
-        load_grad_octet<G>(ct, cur, o, c1, A0);
-        load_grad_octet<G>(ct, cur, o + kThreads, c1, A1);
-        sum2(B0, B1);
+    int32_t k = k0;
+    int64_t ob = c0;
+    while (ob < c1) {
+        // stage tensors k .. k + cnt - 1 (ob lies in the first of them)
+        const int32_t cnt = ct.T - k < kStaged ? ct.T - k : kStaged;
+        __syncthreads();  // every thread is done with the previous span
+        for (int i = t; i <= cnt; i += kThreads) sp.lo[i] = __ldg(ct.prefix + k + i);
+        for (int i = t; i < cnt; i += kThreads) {
+            const TensorRec& r = ct.recs[k + i];
+            sp.base[i] = static_cast<const char*>(r.g);
+            sp.n[i] = r.n;
+            sp.vec[i] = r.vec;
+        }
+        __syncthreads();
+        const int64_t oe = sp.lo[cnt] < c1 ? sp.lo[cnt] : c1;
+        int32_t j = 0;
+        for (int64_t o = ob + t; o < oe; o += 4 * kThreads) {
+            float x[4][8];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t q = o + (int64_t)u * kThreads;
+                if (q < oe) {
+                    while (q >= sp.lo[j + 1]) ++j;
+                    load_staged_octet<G>(sp, j, q - sp.lo[j], x[u]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x[u][e] = 0.0f;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) acc.add8<kScaled>(x[u], inv_scale);
+        }
+        ob = oe;
+        k += cnt;
     }
     double mine = acc.total();
     if (!acc.exact(mine)) mine = sumsq_chunk_double<G>(ct, k0, c0, c1, kScaled ? inv_scale : 1.0f);

@@ -49,6 +49,16 @@ def test_ragged_sizes(ora, name):
     assert r["same_factor_every_step"]
 
 
+@pytest.mark.parametrize("name", ["gpt2_small", "fp16_scaled"])
+def test_many_tiny_tensors(ora, name):
+    """30,000 tensors of 0 to 9 elements (a tenth of them empty): the norm's chunks each span more tensors than it
+    stages in shared memory at once, and every AdamW pack holds hundreds of tensors, empty ones among them."""
+    rng = np.random.Generator(np.random.PCG64(77))
+    sizes = [int(x) for x in rng.integers(0, 10, size=30_000)]
+    r = parity.run_parity(W[name], sizes=sizes, ora=ora, steps=3, zero_grad=True)
+    assert r["same_factor_every_step"]
+
+
 def test_loss_scaled_small(ora):
     sizes = list(W["fp16_scaled"].sizes[:700]) + [768 * 3072]
     r = parity.run_parity(W["fp16_scaled"], sizes=sizes, ora=ora, zero_grad=True)
