@@ -270,6 +270,11 @@ __device__ __forceinline__ void adam_pack(const TensorRec* __restrict__ recs, co
                                           const int32_t* __restrict__ pack_pre, const StepScalars& s,
                                           const GroupScalars& gs, Factor& fac) {
     const int32_t* pre = pack_pre + item.o0;
+    // the whole octets of every aligned tensor of the pack into L2 first, one tensor per thread
+    for (int32_t i = threadIdx.x; i < item.count; i += kThreads) {
+        const TensorRec r = recs[item.t + i];
+        if (r.vec && r.n >= kOct) prefetch_octets<G, M>(r, 0, r.n / kOct);
+    }
     const int32_t total = __ldg(pre + item.count);
     int32_t j = 0;
     for (int32_t q = threadIdx.x; q < total; q += kThreads) {
@@ -281,9 +286,14 @@ __device__ __forceinline__ void adam_pack(const TensorRec* __restrict__ recs, co
         }
         const TensorRec r = recs[item.t + j];
         const int64_t o = q - __ldg(pre + j);
-        const StepScalars x = group_scalars<kGrouped>(s, gs, r);
-        if (r.vec && o < r.n / kOct) adam_vec_octet<G, M, kCoupled, kSkip>(r, o, x, fac);
-        else adam_oct_elements<G, M, kCoupled, kSkip>(r, o, x, fac);
+        if constexpr (kGrouped) {
+            const StepScalars x = group_scalars<kGrouped>(s, gs, r);
+            if (r.vec && o < r.n / kOct) adam_vec_octet<G, M, kCoupled, kSkip>(r, o, x, fac);
+            else adam_oct_elements<G, M, kCoupled, kSkip>(r, o, x, fac);
+        } else {
+            if (r.vec && o < r.n / kOct) adam_vec_octet<G, M, kCoupled, kSkip>(r, o, s, fac);
+            else adam_oct_elements<G, M, kCoupled, kSkip>(r, o, s, fac);
+        }
     }
 }
 

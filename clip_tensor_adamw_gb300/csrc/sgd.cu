@@ -134,6 +134,10 @@ template <Dtype G, bool kMomentum, bool kSkip>
 __device__ __forceinline__ void sgd_pack(const TensorRec* __restrict__ recs, const WorkItem& item,
                                          const int32_t* __restrict__ pack_pre, const SgdScalars& s, Factor& fac) {
     const int32_t* pre = pack_pre + item.o0;
+    for (int32_t i = threadIdx.x; i < item.count; i += kThreads) {  // the pack into L2 first, one tensor a thread
+        const TensorRec r = recs[item.t + i];
+        if (r.vec && r.n >= kOct) sgd_prefetch<G, kMomentum>(r, 0, r.n / kOct);
+    }
     const int32_t total = __ldg(pre + item.count);
     int32_t j = 0;
     for (int32_t q = threadIdx.x; q < total; q += kThreads) {
