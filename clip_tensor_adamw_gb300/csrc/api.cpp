@@ -183,6 +183,9 @@ struct Plan {
     TensorRec* recs = nullptr;
     WorkItem* items = nullptr;
     int32_t* pack_pre = nullptr;  // per pack: the first pack octet of each tensor, and the total
+    unsigned int* queues = nullptr;  // kQueues work queues of the update kernels' persistent grids (2 counters each)
+    std::atomic<uint32_t> launches{0};  // update launches so far: launch i uses queue i % kQueues
+    int32_t sms = 0;
     int32_t num_items = 0;
     int32_t item_octs = 0;
     // norm plans
@@ -200,6 +203,10 @@ struct Plan {
         }
     }
 };
+
+// Work queues per list: a launch may overlap the one before it (programmatic dependent launch), never one of
+// several launches before, so a handful of queues used in turn keeps overlapping launches apart.
+constexpr int kQueues = 8;
 
 static std::mutex g_mu;
 static std::unordered_map<uint64_t, std::vector<std::unique_ptr<Plan>>> g_plans;
@@ -491,7 +498,10 @@ static mica_status build_plan(const ListDesc& L, int device, uint64_t h, Plan** 
     const size_t part_off = up(first_off + first_b);
     const size_t part_b = (L.kind == kNorm) ? first.size() * sizeof(double) : 0;
     const size_t ticket_off = up(part_off + part_b);
-    const size_t total = ticket_off + ((L.kind == kNorm) ? 256 : 0);
+    const size_t ticket_b = (L.kind == kNorm) ? 256 : 0;
+    const size_t queue_off = up(ticket_off + ticket_b);
+    const size_t queue_b = (L.kind == kNorm || L.kind == kScale) ? 0 : kQueues * 2 * sizeof(unsigned int);
+    const size_t total = queue_off + queue_b;
     cudaError_t e = cudaMalloc(&plan->dev, std::max<size_t>(total, 256));
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -511,6 +521,12 @@ static mica_status build_plan(const ListDesc& L, int device, uint64_t h, Plan** 
     if (L.kind == kNorm) {
         plan->partials = reinterpret_cast<double*>(base + part_off);
         plan->ticket = reinterpret_cast<unsigned int*>(base + ticket_off);
+    }
+    plan->sms = sms;
+    if (queue_b) {
+        plan->queues = reinterpret_cast<unsigned int*>(base + queue_off);
+        if ((e = cudaMemsetAsync(plan->queues, 0, queue_b, static_cast<cudaStream_t>(stream))) != cudaSuccess)
+            return cuda_fail(e, "clearing the work queues");
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (plan->ticket && (e = cudaMemsetAsync(plan->ticket, 0, sizeof(unsigned int), st)) != cudaSuccess)
@@ -539,6 +555,12 @@ static mica_status build_plan(const ListDesc& L, int device, uint64_t h, Plan** 
     g_plans[h].push_back(std::move(plan));
     ++g_plan_count;
     return MICA_OK;
+}
+
+// The tables of one update launch on a cached list, with the next of its work queues.
+static UpdateLaunch update_launch(Plan* p) {
+    const uint32_t i = p->launches.fetch_add(1, std::memory_order_relaxed) % kQueues;
+    return UpdateLaunch{p->recs, p->items, p->pack_pre, p->queues + 2 * i, p->num_items, p->item_octs, p->sms};
 }
 
 // The cached table of a list, or nullptr.
@@ -768,8 +790,8 @@ static mica_status adamw_steps(float* const* w, void* const* g, void* const* m, 
         gs.dec[j] = (float)(1.0 - hp[j].lr * hp[j].weight_decay);
         gs.wd[j] = (float)hp[j].weight_decay;
     }
-    return after_launch(launch_adamw(p->recs, p->items, p->pack_pre, p->num_items, p->item_octs, (Dtype)gdt,
-                                     (Dtype)mdt, coupled, sc, group ? &gs : nullptr, d_factor, stream),
+    return after_launch(launch_adamw(update_launch(p), (Dtype)gdt, (Dtype)mdt, coupled, sc, group ? &gs : nullptr,
+                                     d_factor, stream),
                         stream, "AdamWSteps launch");
 }
 
@@ -827,8 +849,7 @@ extern "C" mica_status mica_sgd_steps(float* const* w, void* const* g, float* co
     sc.neg_lr = -(float)hp->lr;
     sc.mu = (float)hp->momentum;
     sc.zero_grad = hp->zero_grad ? 1 : 0;
-    return after_launch(launch_sgd(p->recs, p->items, p->pack_pre, p->num_items, p->item_octs, (Dtype)gdt,
-                                   buf != nullptr,
+    return after_launch(launch_sgd(update_launch(p), (Dtype)gdt, buf != nullptr,
                                    (hp->flags & MICA_STEP_SKIP_NONFINITE) != 0, sc, d_factor, stream),
                         stream, "SGDSteps launch");
 }

@@ -297,19 +297,26 @@ __device__ __forceinline__ void adam_pack(const TensorRec* __restrict__ recs, co
     }
 }
 
-// One CTA per work item, items taken in reverse order (the norm reads them forwards, so the gradient it read last
-// may still be in L2 when this kernel starts). Without kGrouped the scalars are read straight from the kernel's
-// parameters; with it each tensor's group picks its own (the parameter array is indexed in place).
+// A persistent grid (as many CTAs as fit on the GPU at once) taking the work items one at a time from `queue`, in
+// reverse order (the norm reads them forwards, so the gradient it read last may still be in L2 when this kernel
+// starts). Without kGrouped the scalars are read straight from the kernel's parameters; with it each tensor's group
+// picks its own (the parameter array is indexed in place).
 template <Dtype G, Dtype M, bool kCoupled, bool kSkip, bool kGrouped>
 __global__ void __launch_bounds__(kThreads, 3) adamw_kernel(const TensorRec* __restrict__ recs,
                                                             const WorkItem* __restrict__ items, int32_t num_items,
                                                             int32_t item_octs,
-                                                            const int32_t* __restrict__ pack_pre, StepScalars s,
+                                                            const int32_t* __restrict__ pack_pre,
+                                                            unsigned int* queue, StepScalars s,
                                                             const __grid_constant__ GroupScalars gs,
                                                             const float* __restrict__ d_factor) {
     allow_dependents();  // the next step's norm may launch and set up while this kernel's last CTAs run
     Factor fac{d_factor, 1.0f, false};
-    for (int32_t k = blockIdx.x; k < num_items; k += gridDim.x) {
+    __shared__ int32_t s_item[2];
+    if (threadIdx.x == 0) s_item[0] = queue_take(queue);
+    __syncthreads();
+    int32_t cur = 0;
+    for (int32_t k = s_item[0]; k < num_items; k = s_item[cur]) {
+        if (threadIdx.x == 0) s_item[cur ^ 1] = queue_take(queue);
         const WorkItem item = items[num_items - 1 - k];
         if (item.count == 1) {
             const TensorRec r = recs[item.t];
@@ -324,7 +331,10 @@ __global__ void __launch_bounds__(kThreads, 3) adamw_kernel(const TensorRec* __r
         } else {
             adam_pack<G, M, kCoupled, kSkip, kGrouped>(recs, item, pack_pre, s, gs, fac);
         }
+        __syncthreads();  // the next item's index is in s_item[cur ^ 1]; this one's slot may be reused
+        cur ^= 1;
     }
+    queue_finish(queue);
 }
 
 // ------------------------------------------------------------------------------------------------------------------
@@ -897,7 +907,8 @@ struct AdamwLaunch {
     const WorkItem* items;
     const TensorRec* recs;
     const int32_t* pack_pre;
-    int32_t num_items, item_octs;
+    unsigned int* queue;
+    int32_t num_items, item_octs, sms;
     cudaStream_t st;
     const StepScalars* s;
     const GroupScalars* groups;  // nullptr: one group
@@ -906,8 +917,15 @@ struct AdamwLaunch {
 
 template <Dtype G, Dtype M, bool kCoupled, bool kSkip, bool kGrouped>
 cudaError_t launch_adamw_t(const AdamwLaunch& a) {
+    static int per_sm = 0;  // CTAs of this instantiation that fit on one SM
+    if (per_sm <= 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, adamw_kernel<G, M, kCoupled, kSkip, kGrouped>,
+                                                          kThreads, 0) != cudaSuccess ||
+            per_sm <= 0)
+            per_sm = 1;
+    }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.num_items);
+    cfg.gridDim = dim3(persistent_grid(a.num_items, per_sm, a.sms));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = a.st;
@@ -918,7 +936,7 @@ cudaError_t launch_adamw_t(const AdamwLaunch& a) {
     cfg.numAttrs = 1;
     const GroupScalars gs = a.groups ? *a.groups : GroupScalars{};
     return cudaLaunchKernelEx(&cfg, adamw_kernel<G, M, kCoupled, kSkip, kGrouped>, a.recs, a.items, a.num_items,
-                              a.item_octs, a.pack_pre, *a.s, gs, a.d_factor);
+                              a.item_octs, a.pack_pre, a.queue, *a.s, gs, a.d_factor);
 }
 
 template <Dtype G, Dtype M, bool kCoupled, bool kSkip>
@@ -946,12 +964,11 @@ cudaError_t launch_adamw_m(Dtype mdt, bool coupled, const AdamwLaunch& a) {
 // launchers
 // ------------------------------------------------------------------------------------------------------------------
 
-int launch_adamw(const TensorRec* recs, const WorkItem* items, const int32_t* pack_pre, int32_t num_items,
-                 int32_t item_octs, Dtype gdt, Dtype mdt, bool coupled, const StepScalars& s,
+int launch_adamw(const UpdateLaunch& u, Dtype gdt, Dtype mdt, bool coupled, const StepScalars& s,
                  const GroupScalars* groups, const float* d_factor, void* stream) {
-    if (num_items <= 0) return (int)cudaSuccess;
-    const AdamwLaunch a{items, recs, pack_pre, num_items, item_octs, static_cast<cudaStream_t>(stream), &s, groups,
-                        d_factor};
+    if (u.num_items <= 0) return (int)cudaSuccess;
+    const AdamwLaunch a{u.items, u.recs, u.pack_pre, u.queue, u.num_items, u.item_octs, u.sms,
+                        static_cast<cudaStream_t>(stream), &s, groups, d_factor};
     const cudaError_t e = (gdt == kF16) ? launch_adamw_m<kF16>(mdt, coupled, a) : launch_adamw_m<kF32>(mdt, coupled, a);
     count_launches(1);
     return (int)(e != cudaSuccess ? e : cudaGetLastError());

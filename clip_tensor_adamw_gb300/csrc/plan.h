@@ -107,19 +107,36 @@ struct SgdScalars {
 // kBF16x2M (moments only): m packed as kBF16x2, v float32
 enum Dtype : int32_t { kF32 = 0, kF16 = 1, kBF16x2 = 2, kBF16x2M = 3 };
 
+// The tables of an update launch (AdamW, SGD): a persistent grid of at most `sms` x (CTAs that fit on an SM) takes
+// the items from `queue` (two counters, zero before the launch, left zero by it; launches that may overlap need
+// different queues).
+struct UpdateLaunch {
+    const TensorRec* recs;
+    const WorkItem* items;
+    const int32_t* pack_pre;
+    unsigned int* queue;
+    int32_t num_items;
+    int32_t item_octs;
+    int32_t sms;
+};
+
+// The grid of a persistent update launch.
+inline int32_t persistent_grid(int32_t num_items, int per_sm, int sms) {
+    const int64_t cap = (int64_t)(per_sm > 0 ? per_sm : 1) * (sms > 0 ? sms : 1);
+    return (int32_t)(num_items < cap ? num_items : cap);
+}
+
 // Kernel launchers (kernels.cu, sgd.cu). Each returns the cudaError_t of its launch as an int.
-// AdamW (or, with `coupled`, Adam with the coupled L2 term) over every item, one CTA per item. It is launched as a
-// programmatic dependent of the kernel queued before it: it may start and load its tensors while that kernel
-// finishes, and reads d_factor only once that kernel has completed. With `groups`, tensor k takes neg_step, dec and
-// wd from entry recs[k].group of it instead of from s.
-int launch_adamw(const TensorRec* recs, const WorkItem* items, const int32_t* pack_pre, int32_t num_items,
-                 int32_t item_octs, Dtype gdt, Dtype mdt, bool coupled, const StepScalars& s,
+// AdamW (or, with `coupled`, Adam with the coupled L2 term) over every item. It is launched as a programmatic
+// dependent of the kernel queued before it: it may start and load its tensors while that kernel finishes, and reads
+// d_factor only once that kernel has completed. With `groups`, tensor k takes neg_step, dec and wd from entry
+// recs[k].group of it instead of from s.
+int launch_adamw(const UpdateLaunch& u, Dtype gdt, Dtype mdt, bool coupled, const StepScalars& s,
                  const GroupScalars* groups, const float* d_factor, void* stream);
 // SGD (momentum false) or SGD with momentum over every item, launched as AdamW is. `skip`: leave w (and the
 // buffer) as they are when the factor is not > 0.
-int launch_sgd(const TensorRec* recs, const WorkItem* items, const int32_t* pack_pre, int32_t num_items,
-               int32_t item_octs, Dtype gdt, bool momentum, bool skip, const SgdScalars& s, const float* d_factor,
-               void* stream);
+int launch_sgd(const UpdateLaunch& u, Dtype gdt, bool momentum, bool skip, const SgdScalars& s,
+               const float* d_factor, void* stream);
 // The joint norm in one launch of ct.grid CTAs: one partial square sum per CTA into `partials` (ct.grid doubles),
 // and the CTA that finishes last sums them in a fixed order and writes norm and factor. `ticket` must be 0 before
 // the launch; the kernel leaves it 0.

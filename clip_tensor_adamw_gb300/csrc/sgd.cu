@@ -3,11 +3,11 @@
 // w + (-lr) b (PyTorch's SGD without weight decay, dampening or Nesterov). The gradient entering either is
 // gh = g * f, f the factor of the joint-norm clip (and of the loss-scale unscale), read from device memory.
 //
-// Same work items and access scheme as the AdamW kernel: one CTA per item (a slice of a large tensor, or a pack of
-// small tensors whose octets the threads share out), 32-byte streaming loads and stores, L2 prefetch two rounds
-// ahead on the slices, and a programmatic-dependent launch so that the loads start while the norm kernel finishes.
-// Every float operation is a separate correctly rounded intrinsic, in the page's order, so the result is
-// bit-identical to the same step on the CPU.
+// Same work items and access scheme as the AdamW kernel: a persistent grid whose CTAs take the items (a slice of a
+// large tensor, or a pack of small tensors whose octets the threads share out) one at a time from a queue, 32-byte
+// streaming loads and stores, L2 prefetch two rounds ahead on the slices, and a programmatic-dependent launch so that
+// the loads start while the norm kernel finishes. Every float operation is a separate correctly rounded intrinsic,
+// in the page's order, so the result is bit-identical to the same step on the CPU.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -154,14 +154,21 @@ __device__ __forceinline__ void sgd_pack(const TensorRec* __restrict__ recs, con
     }
 }
 
+// A persistent grid taking the items from `queue`, as the AdamW kernel does.
 template <Dtype G, bool kMomentum, bool kSkip>
 __global__ void __launch_bounds__(kThreads, 3) sgd_kernel(const TensorRec* __restrict__ recs,
                                                           const WorkItem* __restrict__ items, int32_t num_items,
                                                           int32_t item_octs, const int32_t* __restrict__ pack_pre,
-                                                          SgdScalars s, const float* __restrict__ d_factor) {
+                                                          unsigned int* queue, SgdScalars s,
+                                                          const float* __restrict__ d_factor) {
     allow_dependents();
     Factor fac{d_factor, 1.0f, false};
-    for (int32_t k = blockIdx.x; k < num_items; k += gridDim.x) {
+    __shared__ int32_t s_item[2];
+    if (threadIdx.x == 0) s_item[0] = queue_take(queue);
+    __syncthreads();
+    int32_t cur = 0;
+    for (int32_t k = s_item[0]; k < num_items; k = s_item[cur]) {
+        if (threadIdx.x == 0) s_item[cur ^ 1] = queue_take(queue);
         const WorkItem item = items[num_items - 1 - k];
         if (item.count == 1) {
             const TensorRec r = recs[item.t];
@@ -171,14 +178,23 @@ __global__ void __launch_bounds__(kThreads, 3) sgd_kernel(const TensorRec* __res
         } else {
             sgd_pack<G, kMomentum, kSkip>(recs, item, pack_pre, s, fac);
         }
+        __syncthreads();
+        cur ^= 1;
     }
+    queue_finish(queue);
 }
 
 template <Dtype G, bool kMomentum, bool kSkip>
-cudaError_t launch_sgd_t(const TensorRec* recs, const WorkItem* items, const int32_t* pack_pre, int32_t num_items,
-                         int32_t item_octs, const SgdScalars& s, const float* d_factor, cudaStream_t st) {
+cudaError_t launch_sgd_t(const UpdateLaunch& u, const SgdScalars& s, const float* d_factor, cudaStream_t st) {
+    static int per_sm = 0;  // CTAs of this instantiation that fit on one SM
+    if (per_sm <= 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sgd_kernel<G, kMomentum, kSkip>, kThreads, 0) !=
+                cudaSuccess ||
+            per_sm <= 0)
+            per_sm = 1;
+    }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(num_items);
+    cfg.gridDim = dim3(persistent_grid(u.num_items, per_sm, u.sms));
     cfg.blockDim = dim3(kThreads);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -186,31 +202,26 @@ cudaError_t launch_sgd_t(const TensorRec* recs, const WorkItem* items, const int
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, sgd_kernel<G, kMomentum, kSkip>, recs, items, num_items, item_octs, pack_pre, s,
-                              d_factor);
+    return cudaLaunchKernelEx(&cfg, sgd_kernel<G, kMomentum, kSkip>, u.recs, u.items, u.num_items, u.item_octs,
+                              u.pack_pre, u.queue, s, d_factor);
 }
 
 template <Dtype G>
-cudaError_t launch_sgd_g(const TensorRec* recs, const WorkItem* items, const int32_t* pp, int32_t num_items,
-                         int32_t item_octs, bool momentum, bool skip, const SgdScalars& s, const float* d_factor,
+cudaError_t launch_sgd_g(const UpdateLaunch& u, bool momentum, bool skip, const SgdScalars& s, const float* d_factor,
                          cudaStream_t st) {
     if (momentum)
-        return skip ? launch_sgd_t<G, true, true>(recs, items, pp, num_items, item_octs, s, d_factor, st)
-                    : launch_sgd_t<G, true, false>(recs, items, pp, num_items, item_octs, s, d_factor, st);
-    return skip ? launch_sgd_t<G, false, true>(recs, items, pp, num_items, item_octs, s, d_factor, st)
-                : launch_sgd_t<G, false, false>(recs, items, pp, num_items, item_octs, s, d_factor, st);
+        return skip ? launch_sgd_t<G, true, true>(u, s, d_factor, st) : launch_sgd_t<G, true, false>(u, s, d_factor, st);
+    return skip ? launch_sgd_t<G, false, true>(u, s, d_factor, st) : launch_sgd_t<G, false, false>(u, s, d_factor, st);
 }
 
 }  // namespace
 
-int launch_sgd(const TensorRec* recs, const WorkItem* items, const int32_t* pack_pre, int32_t num_items,
-               int32_t item_octs, Dtype gdt, bool momentum, bool skip, const SgdScalars& s, const float* d_factor,
-               void* stream) {
-    if (num_items <= 0) return (int)cudaSuccess;
+int launch_sgd(const UpdateLaunch& u, Dtype gdt, bool momentum, bool skip, const SgdScalars& s,
+               const float* d_factor, void* stream) {
+    if (u.num_items <= 0) return (int)cudaSuccess;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const cudaError_t e =
-        (gdt == kF16) ? launch_sgd_g<kF16>(recs, items, pack_pre, num_items, item_octs, momentum, skip, s, d_factor, st)
-                      : launch_sgd_g<kF32>(recs, items, pack_pre, num_items, item_octs, momentum, skip, s, d_factor, st);
+    const cudaError_t e = (gdt == kF16) ? launch_sgd_g<kF16>(u, momentum, skip, s, d_factor, st)
+                                        : launch_sgd_g<kF32>(u, momentum, skip, s, d_factor, st);
     count_launches(1);
     return (int)(e != cudaSuccess ? e : cudaGetLastError());
 }

@@ -1,5 +1,6 @@
 // Device helpers shared by the streaming kernels (kernels.cu, sgd.cu): 32- and 16-byte streaming accesses,
-// binary16 widening, programmatic dependent launch, the gradient factor read, and L2 prefetch.
+// binary16 widening, programmatic dependent launch, the gradient factor read, L2 prefetch, and the persistent grids'
+// work queue.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -84,6 +85,22 @@ __device__ __forceinline__ bool skip_step(float f) { return kSkip && !(f > 0.0f)
 // Asks L2 to fetch `bytes` (a multiple of 16) from `p` (16-byte aligned), without waiting for them.
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// A persistent grid's work queue: q[0] counts the items handed out, q[1] the CTAs that have finished. Each CTA's
+// thread 0 takes items one at a time (the next one while the CTA works on the current one); the CTA that finishes
+// last resets both counters for the launch that uses this queue next. Launches that may overlap (a programmatic
+// dependent starts before its predecessor ends) are given different queues.
+__device__ __forceinline__ int32_t queue_take(unsigned int* q) { return (int32_t)atomicAdd(q, 1u); }
+
+__device__ __forceinline__ void queue_finish(unsigned int* q) {
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(q + 1, 1u) == gridDim.x - 1) {
+            q[0] = 0u;
+            q[1] = 0u;
+        }
+    }
 }
 
 }  // namespace
