@@ -227,13 +227,14 @@ static int sm_count(int device) {
     return n;
 }
 
-// Octets per work item, measured best on GB300 for each kernel and stream set: AdamW with float32 moments 512 (4,096
-// elements: 64 KB of loads, a short tail), AdamW with packed moments and ScaleTensors 2048, SGD 2048, SGD with
-// momentum 1024; halved down to 128 for small lists so that all SMs still get work. MICA_ITEM_OCTS overrides it (a
-// power of two).
+// Octets per slice of a large tensor, measured best on GB300 for each kernel and stream set (the update kernels run
+// as persistent grids): AdamW with float32 moments 512 (4,096 elements: 64 KB of loads), AdamW with packed moments
+// 1024, SGD 1024, SGD with momentum 512, ScaleTensors 2048; halved down to 128 for small lists so that all SMs still
+// get work. MICA_ITEM_OCTS overrides it (a power of two).
 static int32_t base_item_octs(Kind kind, Dtype mdt) {
-    if (kind == kAdamW) return mdt == kF32 ? 512 : 2048;
-    if (kind == kMomentum) return 1024;
+    if (kind == kAdamW) return mdt == kF32 ? 512 : 1024;
+    if (kind == kMomentum) return 512;
+    if (kind == kSGD) return 1024;
     return 2048;
 }
 
@@ -249,10 +250,13 @@ static int32_t choose_item_octs(int64_t total_octs, int sms, int32_t base) {
 }
 
 // Work items over the tensors' octets (see plan.h), and the pack table: for each pack of two or more tensors, the
-// first pack octet of each of its tensors and the pack's total (its item's o0 says where they start).
+// first pack octet of each of its tensors and the pack's total (its item's o0 says where they start). Tensors of up
+// to 512 octets (and at most io) are packed, up to 1024 octets a pack (and at most 2 io): measured best on GB300 for
+// lists of thousands of small tensors.
 static std::vector<WorkItem> build_items(const int64_t* n, int32_t T, int32_t io, std::vector<int32_t>* pack_pre) {
     std::vector<WorkItem> items;
-    const int64_t small = io / 2;
+    const int64_t small = std::min<int64_t>(512, io);
+    const int64_t pack_cap = std::min<int64_t>(1024, 2 * (int64_t)io);
     bool open = false;
     WorkItem pack{};
     int64_t pack_o = 0;
@@ -277,7 +281,7 @@ static std::vector<WorkItem> build_items(const int64_t* n, int32_t T, int32_t io
             continue;
         }
         if (no <= small) {
-            if (open && pack_o + no <= io) {
+            if (open && pack_o + no <= pack_cap) {
                 pack.count += 1;
                 pack_o += no;
             } else {
