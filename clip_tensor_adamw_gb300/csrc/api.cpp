@@ -561,8 +561,11 @@ static mica_status build_plan(const ListDesc& L, int device, uint64_t h, Plan** 
     return MICA_OK;
 }
 
-// The tables of one update launch on a cached list, with the next of its work queues.
-static UpdateLaunch update_launch(Plan* p) {
+// The tables of one update launch on a cached list: a persistent grid with the next of the list's work queues, or
+// (persistent false) one CTA per item. MICA_UPDATE_GRID=items / persistent overrides the choice.
+static UpdateLaunch update_launch(Plan* p, bool persistent) {
+    if (const char* e = std::getenv("MICA_UPDATE_GRID")) persistent = std::strcmp(e, "items") != 0;
+    if (!persistent) return UpdateLaunch{p->recs, p->items, p->pack_pre, nullptr, p->num_items, p->item_octs, p->sms};
     const uint32_t i = p->launches.fetch_add(1, std::memory_order_relaxed) % kQueues;
     return UpdateLaunch{p->recs, p->items, p->pack_pre, p->queues + 2 * i, p->num_items, p->item_octs, p->sms};
 }
@@ -794,7 +797,7 @@ static mica_status adamw_steps(float* const* w, void* const* g, void* const* m, 
         gs.dec[j] = (float)(1.0 - hp[j].lr * hp[j].weight_decay);
         gs.wd[j] = (float)hp[j].weight_decay;
     }
-    return after_launch(launch_adamw(update_launch(p), (Dtype)gdt, (Dtype)mdt, coupled, sc, group ? &gs : nullptr,
+    return after_launch(launch_adamw(update_launch(p, true), (Dtype)gdt, (Dtype)mdt, coupled, sc, group ? &gs : nullptr,
                                      d_factor, stream),
                         stream, "AdamWSteps launch");
 }
@@ -853,7 +856,8 @@ extern "C" mica_status mica_sgd_steps(float* const* w, void* const* g, float* co
     sc.neg_lr = -(float)hp->lr;
     sc.mu = (float)hp->momentum;
     sc.zero_grad = hp->zero_grad ? 1 : 0;
-    return after_launch(launch_sgd(update_launch(p), (Dtype)gdt, buf != nullptr,
+    // plain SGD's short update keeps the next norm waiting less when each item is its own CTA (measured)
+    return after_launch(launch_sgd(update_launch(p, buf != nullptr), (Dtype)gdt, buf != nullptr,
                                    (hp->flags & MICA_STEP_SKIP_NONFINITE) != 0, sc, d_factor, stream),
                         stream, "SGDSteps launch");
 }

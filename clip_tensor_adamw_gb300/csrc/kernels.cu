@@ -297,8 +297,8 @@ __device__ __forceinline__ void adam_pack(const TensorRec* __restrict__ recs, co
     }
 }
 
-// A persistent grid (as many CTAs as fit on the GPU at once) taking the work items one at a time from `queue`, in
-// reverse order (the norm reads them forwards, so the gradient it read last may still be in L2 when this kernel
+// A persistent grid (as many CTAs as fit on the GPU at once) taking the work items one at a time from `queue` (or,
+// with no queue, one CTA per item), in reverse order (the norm reads them forwards, so the gradient it read last may still be in L2 when this kernel
 // starts). Without kGrouped the scalars are read straight from the kernel's parameters; with it each tensor's group
 // picks its own (the parameter array is indexed in place).
 template <Dtype G, Dtype M, bool kCoupled, bool kSkip, bool kGrouped>
@@ -312,11 +312,12 @@ __global__ void __launch_bounds__(kThreads, 3) adamw_kernel(const TensorRec* __r
     allow_dependents();  // the next step's norm may launch and set up while this kernel's last CTAs run
     Factor fac{d_factor, 1.0f, false};
     __shared__ int32_t s_item[2];
-    if (threadIdx.x == 0) s_item[0] = queue_take(queue);
+    const bool persistent = queue != nullptr;  // else one CTA per item: item blockIdx.x
+    if (threadIdx.x == 0) s_item[0] = persistent ? queue_take(queue) : (int32_t)blockIdx.x;
     __syncthreads();
     int32_t cur = 0;
     for (int32_t k = s_item[0]; k < num_items; k = s_item[cur]) {
-        if (threadIdx.x == 0) s_item[cur ^ 1] = queue_take(queue);
+        if (threadIdx.x == 0) s_item[cur ^ 1] = persistent ? queue_take(queue) : num_items;
         const WorkItem item = items[num_items - 1 - k];
         if (item.count == 1) {
             const TensorRec r = recs[item.t];
@@ -334,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 3) adamw_kernel(const TensorRec* __r
         __syncthreads();  // the next item's index is in s_item[cur ^ 1]; this one's slot may be reused
         cur ^= 1;
     }
-    queue_finish(queue);
+    if (persistent) queue_finish(queue);
 }
 
 // ------------------------------------------------------------------------------------------------------------------
@@ -925,7 +926,7 @@ cudaError_t launch_adamw_t(const AdamwLaunch& a) {
             per_sm = 1;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(persistent_grid(a.num_items, per_sm, a.sms));
+    cfg.gridDim = dim3(a.queue ? persistent_grid(a.num_items, per_sm, a.sms) : a.num_items);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = a.st;

@@ -109,7 +109,7 @@ enum Dtype : int32_t { kF32 = 0, kF16 = 1, kBF16x2 = 2, kBF16x2M = 3 };
 
 // The tables of an update launch (AdamW, SGD): a persistent grid of at most `sms` x (CTAs that fit on an SM) takes
 // the items from `queue` (two counters, zero before the launch, left zero by it; launches that may overlap need
-// different queues).
+// different queues), or, with `queue` null, one CTA per item.
 struct UpdateLaunch {
     const TensorRec* recs;
     const WorkItem* items;

@@ -154,7 +154,7 @@ __device__ __forceinline__ void sgd_pack(const TensorRec* __restrict__ recs, con
     }
 }
 
-// A persistent grid taking the items from `queue`, as the AdamW kernel does.
+// A persistent grid taking the items from `queue` (or, with no queue, one CTA per item), as the AdamW kernel does.
 template <Dtype G, bool kMomentum, bool kSkip>
 __global__ void __launch_bounds__(kThreads, 3) sgd_kernel(const TensorRec* __restrict__ recs,
                                                           const WorkItem* __restrict__ items, int32_t num_items,
@@ -164,11 +164,12 @@ __global__ void __launch_bounds__(kThreads, 3) sgd_kernel(const TensorRec* __res
     allow_dependents();
     Factor fac{d_factor, 1.0f, false};
     __shared__ int32_t s_item[2];
-    if (threadIdx.x == 0) s_item[0] = queue_take(queue);
+    const bool persistent = queue != nullptr;  // else one CTA per item: item blockIdx.x
+    if (threadIdx.x == 0) s_item[0] = persistent ? queue_take(queue) : (int32_t)blockIdx.x;
     __syncthreads();
     int32_t cur = 0;
     for (int32_t k = s_item[0]; k < num_items; k = s_item[cur]) {
-        if (threadIdx.x == 0) s_item[cur ^ 1] = queue_take(queue);
+        if (threadIdx.x == 0) s_item[cur ^ 1] = persistent ? queue_take(queue) : num_items;
         const WorkItem item = items[num_items - 1 - k];
         if (item.count == 1) {
             const TensorRec r = recs[item.t];
@@ -181,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 3) sgd_kernel(const TensorRec* __res
         __syncthreads();
         cur ^= 1;
     }
-    queue_finish(queue);
+    if (persistent) queue_finish(queue);
 }
 
 template <Dtype G, bool kMomentum, bool kSkip>
@@ -194,7 +195,7 @@ cudaError_t launch_sgd_t(const UpdateLaunch& u, const SgdScalars& s, const float
             per_sm = 1;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(persistent_grid(u.num_items, per_sm, u.sms));
+    cfg.gridDim = dim3(u.queue ? persistent_grid(u.num_items, per_sm, u.sms) : u.num_items);
     cfg.blockDim = dim3(kThreads);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
