@@ -5,9 +5,9 @@ The compute lives in libmica_optim.so (hand-written CUDA kernels behind the C AB
 package is its Python binding. Build the library with ``python -m clip_tensor_adamw_gb300.build``.
 """
 from .mica import (GroupIndex, MicaError, TensorList, lib, mica_adamw_steps, mica_adamw_steps_grouped,
-                   mica_clip_grad_norms, mica_launch_count, mica_release_cache, mica_scale_tensors, mica_sgd_steps,
-                   mica_sync)
+                   mica_clip_grad_norms, mica_launch_count, mica_release_cache, mica_scale_tensors,
+                   mica_selftest_wait_timeout, mica_sgd_steps, mica_sync)
 
 __all__ = ["GroupIndex", "MicaError", "TensorList", "lib", "mica_adamw_steps", "mica_adamw_steps_grouped",
-           "mica_clip_grad_norms", "mica_launch_count", "mica_release_cache", "mica_scale_tensors", "mica_sgd_steps",
-           "mica_sync"]
+           "mica_clip_grad_norms", "mica_launch_count", "mica_release_cache", "mica_scale_tensors",
+           "mica_selftest_wait_timeout", "mica_sgd_steps", "mica_sync"]

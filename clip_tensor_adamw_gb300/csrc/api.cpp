@@ -862,6 +862,14 @@ extern "C" mica_status mica_sgd_steps(float* const* w, void* const* g, float* co
                         stream, "SGDSteps launch");
 }
 
+extern "C" mica_status mica_selftest_wait_timeout(uint32_t polls, void* stream) {
+    if (polls < 1 || polls > (1u << 20)) return fail(MICA_ERR_HYPER, "polls = %u is outside [1, 2^20]", polls);
+    int dev = 0;
+    mica_status s = current_device(&dev);
+    if (s != MICA_OK) return s;
+    return after_launch(launch_wait_selftest(polls, stream), stream, "wait self-test launch");
+}
+
 extern "C" mica_status mica_sync(void* stream) {
     const cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "mica_sync");

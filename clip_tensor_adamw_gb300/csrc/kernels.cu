@@ -630,9 +630,9 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 // Waits until the barrier's phase of parity `parity` has completed; false if it has not after kMaxPolls rounds.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t max_polls = kMaxPolls) {
     const uint32_t addr = smem_u32(bar);
-    for (uint32_t i = 0; i < kMaxPolls; ++i) {
+    for (uint32_t i = 0; i < max_polls; ++i) {
         uint32_t done;
         asm volatile(
             "{\n\t.reg .pred p;\n\t"
@@ -674,7 +674,19 @@ __host__ __device__ constexpr int norm_stage_bytes() { return kNormStageOcts * (
 template <Dtype G>
 size_t norm_smem_bytes() { return (size_t)kNormStages * norm_stage_bytes<G>(); }
 
-enum : unsigned int { kStatusNormProducer = 1u, kStatusNormConsumer = 2u };
+enum : unsigned int { kStatusNormProducer = 1u, kStatusNormConsumer = 2u, kStatusSelfTest = 4u };
+
+// The bounded wait's failure path, on purpose: one thread waits `polls` rounds on a barrier that nothing arrives at,
+// gives up and reports it in the status word, as a pipeline kernel whose copies never landed would.
+__global__ void __launch_bounds__(32) wait_selftest_kernel(uint32_t polls) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        mbar_fence_init();
+    }
+    __syncwarp();
+    if (threadIdx.x == 0 && !mbar_wait(&bar, 0, polls)) atomicOr(&g_mica_status, kStatusSelfTest);
+}
 
 template <Dtype G, bool kScaled>
 __global__ void __launch_bounds__(kNormThreads, kNormTmaCtasPerSm) norm_tma_kernel(ChunkTable ct, float inv_scale,
@@ -1019,6 +1031,12 @@ int launch_norm(const ChunkTable& ct, Dtype gdt, float inv_scale, double* partia
         e = launch_norm_t<kF32, false>(ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
     count_launches(1);
     return (int)e;
+}
+
+int launch_wait_selftest(uint32_t polls, void* stream) {
+    wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(polls);
+    count_launches(1);
+    return (int)cudaGetLastError();
 }
 
 int read_device_status(unsigned int* status) {

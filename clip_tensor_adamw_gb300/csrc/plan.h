@@ -145,6 +145,9 @@ int launch_norm(const ChunkTable& ct, Dtype gdt, float inv_scale, double* partia
 int launch_scale(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_octs, Dtype dt,
                  float factor, const float* d_factor, void* stream);
 
+// One CTA whose bounded mbarrier wait runs out after `polls` rounds (nothing arrives) and sets the status word.
+int launch_wait_selftest(uint32_t polls, void* stream);
+
 // The device's pipeline status word: nonzero when a kernel's bounded wait on a shared-memory barrier gave up (the
 // kernel then stopped early and its results are not valid). Reads it (synchronously) and clears it.
 int read_device_status(unsigned int* status);

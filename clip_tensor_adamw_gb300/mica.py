@@ -69,6 +69,8 @@ def lib() -> ctypes.CDLL:
         for f in ("mica_scale_tensors", "mica_clip_grad_norms", "mica_adamw_steps", "mica_adamw_steps_grouped",
                   "mica_sgd_steps", "mica_sync", "mica_release_cache"):
             getattr(L, f).restype = ctypes.c_int
+        L.mica_selftest_wait_timeout.argtypes = [ctypes.c_uint32, _P]
+        L.mica_selftest_wait_timeout.restype = ctypes.c_int
         L.mica_sync.argtypes = [_P]
         L.mica_release_cache.argtypes = []
         L.mica_status_string.argtypes = [ctypes.c_int]
@@ -243,6 +245,11 @@ def mica_sgd_steps(w, g, buf=None, *, lr: float, momentum: float = 0.0, zero_gra
 
 def mica_sync(stream=None) -> None:
     _check(lib().mica_sync(_stream(stream)))
+
+
+def mica_selftest_wait_timeout(polls: int = 16, stream=None) -> None:
+    """Queues the self-test kernel whose bounded wait runs out; the next mica_sync raises MicaError (MICA_ERR_CUDA)."""
+    _check(lib().mica_selftest_wait_timeout(int(polls), _stream(stream)))
 
 
 def mica_release_cache() -> None:

@@ -219,6 +219,15 @@ MICA_API mica_status mica_clip_grad_norms_noalloc(const void* const* g, const in
  * MICA_ERR_CUDA, with its results not valid. */
 MICA_API mica_status mica_sync(void* stream);
 
+/*
+ * Self-test of the failure path above, which the method's pages have no counterpart to: queues on `stream` one
+ * one-warp kernel whose bounded mbarrier wait runs out after `polls` polling rounds (1 <= polls <= 2^20, else
+ * MICA_ERR_HYPER) because nothing ever arrives at the barrier; the kernel then ORs 0x4 into the status word and
+ * returns. The next mica_sync(stream) reports MICA_ERR_CUDA ("... gave up (status 0x4)"), the one after it MICA_OK,
+ * and the context stays usable. Nothing faults, traps or hangs.
+ */
+MICA_API mica_status mica_selftest_wait_timeout(uint32_t polls, void* stream);
+
 /* Waits for the current device, then frees every cached per-list device table. Returns MICA_OK or MICA_ERR_CUDA. */
 MICA_API mica_status mica_release_cache(void);
 

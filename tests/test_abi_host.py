@@ -161,6 +161,12 @@ def test_scale_host_validation():
     assert L.mica_scale_tensors(t, N, 0, 0, 1.0, None, None) == OK
 
 
+def test_selftest_host_validation():
+    L = mica.lib()
+    assert L.mica_selftest_wait_timeout(0, None) == HYPER
+    assert L.mica_selftest_wait_timeout((1 << 20) + 1, None) == HYPER
+
+
 def test_no_kernels_without_a_device():
     import torch
     if torch.cuda.is_available():
