@@ -36,7 +36,7 @@ import workloads  # noqa: E402
 METRIC = "clip+AdamW params/sec and achieved HBM GB/s (% of 8 TB/s roofline), 1 GB300"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SRCS = [os.path.join(ROOT, "clip_tensor_adamw_gb300", "csrc", f) for f in ("kernels.cu", "stream.cuh")]
+KERNEL_SRCS = [os.path.join(ROOT, "clip_tensor_adamw_gb300", "csrc", f) for f in ("adamw.cu", "stream.cuh", "plan.h")]
 PROFILE = os.path.join(ROOT, "profiles", "adamw_gpt2_small.md")
 
 
@@ -88,7 +88,7 @@ def hbm_peak() -> tuple[float, str]:
 
 
 def kernel_source_sha() -> str:
-    """The first 16 hex digits of the SHA-256 of the AdamW kernel's sources (kernels.cu, then stream.cuh)."""
+    """The first 16 hex digits of the SHA-256 of the AdamW kernel's sources (adamw.cu, stream.cuh, plan.h)."""
     h = hashlib.sha256()
     for path in KERNEL_SRCS:
         with open(path, "rb") as f:

@@ -1,5 +1,5 @@
-// Internal layout shared by the host side (api.cpp: validation, tables, launches) and the kernels (kernels.cu,
-// sgd.cu).
+// Internal layout shared by the host side (api.cpp: validation, tables, launches) and the kernels (adamw.cu,
+// norm.cu, sgd.cu, scale.cu).
 //
 // A call's tensor list becomes one device table:
 //   TensorRec[T]   the four base pointers and the element count of every tensor;
@@ -126,7 +126,7 @@ inline int32_t persistent_grid(int32_t num_items, int per_sm, int sms) {
     return (int32_t)(num_items < cap ? num_items : cap);
 }
 
-// Kernel launchers (kernels.cu, sgd.cu). Each returns the cudaError_t of its launch as an int.
+// Kernel launchers (adamw.cu, sgd.cu, norm.cu, scale.cu). Each returns the cudaError_t of its launch as an int.
 // AdamW (or, with `coupled`, Adam with the coupled L2 term) over every item. It is launched as a programmatic
 // dependent of the kernel queued before it: it may start and load its tensors while that kernel finishes, and reads
 // d_factor only once that kernel has completed. With `groups`, tensor k takes neg_step, dec and wd from entry

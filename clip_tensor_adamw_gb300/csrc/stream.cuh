@@ -1,4 +1,4 @@
-// Device helpers shared by the streaming kernels (kernels.cu, sgd.cu): 32- and 16-byte streaming accesses,
+// Device helpers shared by the streaming kernels (adamw.cu, norm.cu, sgd.cu, scale.cu): 32- and 16-byte streaming accesses,
 // binary16 widening, programmatic dependent launch, the gradient factor read, L2 prefetch, and the persistent grids'
 // work queue.
 #pragma once
