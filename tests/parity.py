@@ -64,6 +64,15 @@ def exact(a: np.ndarray, b: np.ndarray, what: str) -> None:
         raise AssertionError(f"{what}: {diff.size} of {a.size} differ in bits; first idx {diff[:5].tolist()}")
 
 
+def check_norm(g_norm, o_norm, t) -> None:
+    """The device norm against the oracle's: relative 1e-5, or the same NaN / infinity."""
+    g, o = float(g_norm), float(o_norm)
+    if np.isfinite(o):
+        assert abs(g - o) <= NORM_RTOL * abs(o), (t, g, o)
+    else:
+        assert (np.isnan(g) and np.isnan(o)) or g == o, (t, g, o)
+
+
 def hp_of(wl: workloads.Workload, t: int) -> oracle.Hyper:
     return oracle.Hyper(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps, weight_decay=wl.weight_decay, step=t)
 
@@ -133,10 +142,7 @@ def run_parity(wl: workloads.Workload, sizes=None, steps: int | None = None, zer
         torch.cuda.synchronize()
         g_norm = np.float32(d_norm.item())
         g_factor = np.float32(d_factor.item())
-        if not np.isfinite(o_norm):
-            assert (np.isnan(g_norm) and np.isnan(o_norm)) or g_norm == o_norm, (t, g_norm, o_norm)
-        else:
-            assert abs(float(g_norm) - float(o_norm)) <= NORM_RTOL * abs(float(o_norm)), (t, g_norm, o_norm)
+        check_norm(g_norm, o_norm, t)
         same = g_factor.view(np.uint32) == o_factor.view(np.uint32)
         same_all &= bool(same)
         norms.append((float(g_norm), float(o_norm), float(g_factor), float(o_factor)))
@@ -181,7 +187,7 @@ def run_parity_groups(wl: workloads.Workload, group, sizes=None, steps: int | No
                              step=t) for h in hps]
         ora.adamw_steps_grouped(*host, group, ohps, factor=o_factor, zero_grad=zero_grad)
         torch.cuda.synchronize()
-        assert abs(d_norm.item() - float(o_norm)) <= NORM_RTOL * abs(float(o_norm)), (t, d_norm.item(), o_norm)
+        check_norm(np.float32(d_norm.item()), o_norm, t)
         same = np.float32(d_factor.item()).view(np.uint32) == o_factor.view(np.uint32)
         same_all &= bool(same)
         if check_every_step or t == steps:
@@ -217,11 +223,7 @@ def run_parity_sgd(wl: workloads.Workload, momentum: float, sizes=None, steps: i
         o_norm, o_factor = ora.clip_sgd_step(hw, hg, hb if momentum else None, SGD_LR, momentum, wl.max_norm,
                                              wl.inv_scale, zero_grad=zero_grad, skip_nonfinite=skip_nonfinite)
         torch.cuda.synchronize()
-        g_norm = np.float32(d_norm.item())
-        if np.isfinite(o_norm):
-            assert abs(float(g_norm) - float(o_norm)) <= NORM_RTOL * abs(float(o_norm)), (t, g_norm, o_norm)
-        else:
-            assert (np.isnan(g_norm) and np.isnan(o_norm)) or g_norm == o_norm, (t, g_norm, o_norm)
+        check_norm(np.float32(d_norm.item()), o_norm, t)
         same = np.float32(d_factor.item()).view(np.uint32) == o_factor.view(np.uint32)
         same_all &= bool(same)
         if check_every_step or t == steps:
