@@ -6,6 +6,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdint>
 
 #include "plan.h"
@@ -28,6 +29,13 @@ namespace {
 // infinity or NaN, or nothing but values below 2^-50) is summed again in double by the caller.
 __device__ __forceinline__ float2 neg2(float2 v) { return make_float2(-v.x, -v.y); }
 
+// How a kernel sums the squares of x = g * inv_scale: kSumUnscaled (inv_scale is 1), kSumScaled (each x formed in
+// float32), or kSumHalfPow2 (binary16 g and a power-of-two inv_scale for which every g * inv_scale is an exact
+// normal float32: g^2 then has at most 22 significant bits and lies in [2^-48, 2^32], so each square is exact in
+// float32 and needs neither the error term nor the range check; the sum of g^2 is scaled by inv_scale^2 at the end,
+// exactly).
+enum : int { kSumUnscaled = 0, kSumScaled = 1, kSumHalfPow2 = 2 };
+
 struct SumSq {
     float2 hi, lo;
     float mx;  // the largest |x| seen (NaNs are ignored here and show up in hi instead)
@@ -41,19 +49,31 @@ struct SumSq {
         hi = s;
         lo = __fadd2_rn(lo, __fadd2_rn(err, e));
     }
-    template <bool kScaled>
+    // the same for a pair whose squares are exact in float32 (no rounding error term) and whose |x| need no check
+    __device__ __forceinline__ void add2_exact_squares(float2 x) {
+        const float2 p = __fmul2_rn(x, x);
+        const float2 s = __fadd2_rn(hi, p);
+        const float2 bp = __fadd2_rn(s, neg2(hi));
+        const float2 err = __fadd2_rn(__fadd2_rn(hi, neg2(__fadd2_rn(s, neg2(bp)))), __fadd2_rn(p, neg2(bp)));
+        hi = s;
+        lo = __fadd2_rn(lo, err);
+    }
+    template <int kMode>
     __device__ __forceinline__ void add8(const float (&x)[8], float inv_scale) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             float2 v = make_float2(x[2 * j], x[2 * j + 1]);
-            if constexpr (kScaled) v = __fmul2_rn(v, make_float2(inv_scale, inv_scale));
-            add2(v);
+            if constexpr (kMode == kSumScaled) v = __fmul2_rn(v, make_float2(inv_scale, inv_scale));
+            if constexpr (kMode == kSumHalfPow2) add2_exact_squares(v);
+            else add2(v);
         }
     }
     __device__ __forceinline__ double total() const {
         return ((double)hi.x + (double)lo.x) + ((double)hi.y + (double)lo.y);
     }
+    template <int kMode>
     __device__ __forceinline__ bool exact(double t) const {
+        if constexpr (kMode == kSumHalfPow2) return t < 0x1p100;  // false for an infinity or a NaN
         return mx < 0x1p50f && !(mx < 0x1p-50f && mx > 0.0f) && t < 0x1p100;
     }
 };
@@ -167,6 +187,18 @@ __device__ __noinline__ double sumsq_chunk_double(const ChunkTable& ct, int32_t 
     return t;
 }
 
+// This thread's share of the sum of squares of the unscaled gradient, from its accumulator: in kSumHalfPow2 the
+// squares of the binary16 values themselves were summed, and the power-of-two scale is applied here (exactly). A
+// share the float32 pairs could not hold exactly is summed again in double.
+template <Dtype G, int kMode>
+__device__ __forceinline__ double share_total(const SumSq& acc, const ChunkTable& ct, int32_t k0, int64_t c0,
+                                              int64_t c1, float inv_scale) {
+    const double t = acc.total();
+    if (!acc.exact<kMode>(t)) return sumsq_chunk_double<G>(ct, k0, c0, c1, kMode == kSumUnscaled ? 1.0f : inv_scale);
+    if constexpr (kMode == kSumHalfPow2) return t * ((double)inv_scale * (double)inv_scale);
+    return t;
+}
+
 // Up to kStaged consecutive tensors of a chunk, staged in shared memory: tensor i holds the list's octets
 // [lo[i], lo[i + 1]), its gradient starts at base[i] and has n[i] elements, vec[i] says whether it is aligned for
 // the vector loads.
@@ -216,7 +248,7 @@ __device__ __forceinline__ void load_staged_octet(const StagedSpan& sp, int32_t 
 // chunk's tensors (their octet ranges, bases, sizes) in shared memory up to kStaged at a time; thread t takes the
 // staged span's octets c + t, c + t + 256, ..., four at a time (all four loads in flight before they are summed),
 // finding each octet's tensor by walking the staged table forwards. The rest is as in norm_tma_kernel.
-template <Dtype G, bool kScaled>
+template <Dtype G, int kMode>
 __global__ void __launch_bounds__(kThreads, kNormDirectCtasPerSm) norm_direct_kernel(ChunkTable ct, float inv_scale,
                                                                         double* __restrict__ partials,
                                                                         unsigned int* ticket, float max_norm,
@@ -262,13 +294,12 @@ __global__ void __launch_bounds__(kThreads, kNormDirectCtasPerSm) norm_direct_ke
                 }
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) acc.add8<kScaled>(x[u], inv_scale);
+            for (int u = 0; u < 4; ++u) acc.add8<kMode>(x[u], inv_scale);
         }
         ob = oe;
         k += cnt;
     }
-    double mine = acc.total();
-    if (!acc.exact(mine)) mine = sumsq_chunk_double<G>(ct, k0, c0, c1, kScaled ? inv_scale : 1.0f);
+    double mine = share_total<G, kMode>(acc, ct, k0, c0, c1, inv_scale);
 
     const double part = block_sum(mine, red);
     if (t == 0) {
@@ -364,7 +395,7 @@ __global__ void __launch_bounds__(32) wait_selftest_kernel(uint32_t polls) {
     if (threadIdx.x == 0 && !mbar_wait(&bar, 0, polls)) atomicOr(&g_mica_status, kStatusSelfTest);
 }
 
-template <Dtype G, bool kScaled>
+template <Dtype G, int kMode>
 __global__ void __launch_bounds__(kNormThreads, kNormTmaCtasPerSm) norm_tma_kernel(ChunkTable ct, float inv_scale,
                                                                             double* __restrict__ partials,
                                                                             unsigned int* ticket, float max_norm,
@@ -486,15 +517,14 @@ __global__ void __launch_bounds__(kNormThreads, kNormTmaCtasPerSm) norm_tma_kern
             read_octet(a + t + kThreads, t + kThreads, x1);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);  // this warp is done reading the stage
-            acc.add8<kScaled>(x0, inv_scale);
-            acc.add8<kScaled>(x1, inv_scale);
+            acc.add8<kMode>(x0, inv_scale);
+            acc.add8<kMode>(x1, inv_scale);
             if (++slot == S) {
                 slot = 0;
                 phase ^= 1u;
             }
         }
-        mine = acc.total();
-        if (!acc.exact(mine)) mine = sumsq_chunk_double<G>(ct, k0, c0, c1, kScaled ? inv_scale : 1.0f);
+        mine = share_total<G, kMode>(acc, ct, k0, c0, c1, inv_scale);
         if (!ok) atomicOr(&g_mica_status, kStatusNormConsumer);
     }
 
@@ -514,7 +544,7 @@ __global__ void __launch_bounds__(kNormThreads, kNormTmaCtasPerSm) norm_tma_kern
 
 }  // namespace
 
-template <Dtype G, bool kScaled>
+template <Dtype G, int kMode>
 cudaError_t launch_norm_t(const ChunkTable& ct, cudaStream_t st, float inv_scale, double* partials,
                           unsigned int* ticket, float max_norm, float* d_norm, float* d_factor) {
     cudaLaunchConfig_t cfg = {};
@@ -528,16 +558,16 @@ cudaError_t launch_norm_t(const ChunkTable& ct, cudaStream_t st, float inv_scale
     if (ct.direct) {
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = 0;
-        return cudaLaunchKernelEx(&cfg, norm_direct_kernel<G, kScaled>, ct, inv_scale, partials, ticket, max_norm,
+        return cudaLaunchKernelEx(&cfg, norm_direct_kernel<G, kMode>, ct, inv_scale, partials, ticket, max_norm,
                                   d_norm, d_factor);
     }
     const size_t smem = norm_smem_bytes<G>();
-    cudaError_t e = cudaFuncSetAttribute(norm_tma_kernel<G, kScaled>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(norm_tma_kernel<G, kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
     cfg.blockDim = dim3(kNormThreads);
     cfg.dynamicSmemBytes = smem;
-    return cudaLaunchKernelEx(&cfg, norm_tma_kernel<G, kScaled>, ct, inv_scale, partials, ticket, max_norm, d_norm,
+    return cudaLaunchKernelEx(&cfg, norm_tma_kernel<G, kMode>, ct, inv_scale, partials, ticket, max_norm, d_norm,
                               d_factor);
 }
 
@@ -545,15 +575,18 @@ int launch_norm(const ChunkTable& ct, Dtype gdt, float inv_scale, double* partia
                 float max_norm, float* d_norm, float* d_factor, void* stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool scaled = inv_scale != 1.0f;  // an unscaled list skips the multiply (x * 1 is x)
+    // binary16 times a power of two in [2^-102, 2^111]: every product is an exact normal float32
+    int ex = 0;
+    const bool pow2 = std::frexp(inv_scale, &ex) == 0.5f && inv_scale >= 0x1p-102f && inv_scale <= 0x1p111f;
     cudaError_t e;
-    if (gdt == kF16 && scaled)
-        e = launch_norm_t<kF16, true>(ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
+    if (gdt == kF16 && pow2)
+        e = launch_norm_t<kF16, kSumHalfPow2>(ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
     else if (gdt == kF16)
-        e = launch_norm_t<kF16, false>(ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
+        e = launch_norm_t<kF16, kSumScaled>(ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
     else if (scaled)
-        e = launch_norm_t<kF32, true>(ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
+        e = launch_norm_t<kF32, kSumScaled>(ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
     else
-        e = launch_norm_t<kF32, false>(ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
+        e = launch_norm_t<kF32, kSumUnscaled>(ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
     count_launches(1);
     return (int)e;
 }
