@@ -203,6 +203,15 @@ def time_oracle(wl: workloads.Workload, target_params: int, min_seconds: float, 
     return params, ntens, times
 
 
+def run_config(wl: workloads.Workload, world: int) -> dict:
+    """The `config` of both arms' JSON lines: the workload the metric is quoted on."""
+    bpp = step_bytes_per_param(wl)
+    return {"workload": describe(wl), "params": wl.params, "tensors": len(wl.sizes), "moments": wl.moments,
+            "grad_dtype": wl.grad_dtype, "zero_grad": False, "bytes_per_param": bpp,
+            "l2": f"inputs larger than L2 ({wl.params * bpp / 1e9:.2f} GB moved per step; no flush)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
 def run_reference(args, wl: workloads.Workload) -> None:
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -224,7 +233,7 @@ def run_reference(args, wl: workloads.Workload) -> None:
         "impl": "reference", "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": describe(wl), "params_per_step": params, "oracle": "plain single-threaded C, -O2"},
+        "config": run_config(wl, args.gpus),
         "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -499,10 +508,7 @@ def main():
             "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": main_fig["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": describe(wl), "params": P, "tensors": len(wl.sizes), "moments": wl.moments,
-                       "grad_dtype": wl.grad_dtype, "zero_grad": False, "bytes_per_param": step_bpp,
-                       "l2": f"inputs larger than L2 ({P * step_bpp / 1e9:.2f} GB moved per step; no flush)",
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "config": run_config(wl, world),
             "hbm_gbs": step_gbs, "pct_of_8tbs": 100 * step_gbs / NOMINAL_HBM_GBS,
             "pct_of_measured_copy": 100 * step_gbs / peak if peak_src == "measured" else None,
             "roofline": {"bound": "hbm", "kernel": "adamw_kernel", "achieved": a_gbs, "peak": peak, "unit": "GB/s",
