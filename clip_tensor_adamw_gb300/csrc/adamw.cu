@@ -259,37 +259,55 @@ __device__ __forceinline__ StepScalars group_scalars(const StepScalars& s, const
     return x;
 }
 
-// A pack of small tensors (t .. t+count-1, whole): their octets, concatenated, are spread over the CTA's threads,
-// thread i taking pack octets i, i + 256, ..., so that every thread has work however small the tensors are.
-// pre[0..count] (in the list's pack table, from entry item.o0) holds the first pack octet of each tensor and the
-// pack's total; a thread finds its octet's tensor by binary search from the last one it found.
+// The last j in [j, count) with pre[j] <= q, given pre[j] <= q already (pre non-decreasing).
+__device__ __forceinline__ int32_t pack_search(const int32_t* __restrict__ pre, int32_t j, int32_t count, int32_t q) {
+    int32_t hi = count - 1;
+    while (j < hi) {
+        const int32_t mid = (j + hi + 1) >> 1;
+        if (__ldg(pre + mid) <= q) j = mid;
+        else hi = mid - 1;
+    }
+    return j;
+}
+
+// A pack of small tensors (t .. t+count-1, whole): their octets are spread over the CTA's threads, thread i taking
+// pack octets i, i + 256, ..., so that every thread has work however small the tensors are. The pack numbers the
+// whole octets of its aligned tensors first, then the octets taken element by element (see the pack table in
+// plan.h), so that the two kinds seldom share a warp; a thread finds its octet's tensor by binary search from the
+// last one it found. The CTA first asks L2 for the pack's whole octets.
 template <Dtype G, Dtype M, bool kCoupled, bool kSkip, bool kGrouped>
 __device__ __forceinline__ void adam_pack(const TensorRec* __restrict__ recs, const WorkItem& item,
                                           const int32_t* __restrict__ pack_pre, const StepScalars& s,
                                           const GroupScalars& gs, Factor& fac) {
-    const int32_t* pre = pack_pre + item.o0;
-    // the whole octets of every aligned tensor of the pack into L2 first, one tensor per thread
+    const int32_t* pre_w = pack_pre + item.o0;        // whole octets: count + 1 entries
+    const int32_t* pre_e = pre_w + item.count + 1;   // the others: count + 1 entries
     for (int32_t i = threadIdx.x; i < item.count; i += kThreads) {
         const TensorRec r = recs[item.t + i];
         if (r.vec && r.n >= kOct) prefetch_octets<G, M>(r, 0, r.n / kOct);
     }
-    const int32_t total = __ldg(pre + item.count);
-    int32_t j = 0;
+    const int32_t total_w = __ldg(pre_w + item.count);
+    const int32_t total = total_w + __ldg(pre_e + item.count);
+    int32_t jw = 0, je = 0;
     for (int32_t q = threadIdx.x; q < total; q += kThreads) {
-        int32_t hi = item.count - 1;  // the last j with pre[j] <= q: pre[j] <= q holds already
-        while (j < hi) {
-            const int32_t mid = (j + hi + 1) >> 1;
-            if (__ldg(pre + mid) <= q) j = mid;
-            else hi = mid - 1;
+        const bool whole = q < total_w;
+        int64_t o;
+        TensorRec r;
+        if (whole) {
+            jw = pack_search(pre_w, jw, item.count, q);
+            r = recs[item.t + jw];
+            o = q - __ldg(pre_w + jw);
+        } else {
+            const int32_t qe = q - total_w;
+            je = pack_search(pre_e, je, item.count, qe);
+            r = recs[item.t + je];
+            o = (r.vec ? r.n / kOct : 0) + (qe - __ldg(pre_e + je));
         }
-        const TensorRec r = recs[item.t + j];
-        const int64_t o = q - __ldg(pre + j);
         if constexpr (kGrouped) {
             const StepScalars x = group_scalars<kGrouped>(s, gs, r);
-            if (r.vec && o < r.n / kOct) adam_vec_octet<G, M, kCoupled, kSkip>(r, o, x, fac);
+            if (whole) adam_vec_octet<G, M, kCoupled, kSkip>(r, o, x, fac);
             else adam_oct_elements<G, M, kCoupled, kSkip>(r, o, x, fac);
         } else {
-            if (r.vec && o < r.n / kOct) adam_vec_octet<G, M, kCoupled, kSkip>(r, o, s, fac);
+            if (whole) adam_vec_octet<G, M, kCoupled, kSkip>(r, o, s, fac);
             else adam_oct_elements<G, M, kCoupled, kSkip>(r, o, s, fac);
         }
     }

@@ -249,11 +249,15 @@ static int32_t choose_item_octs(int64_t total_octs, int sms, int32_t base) {
     return io;
 }
 
-// Work items over the tensors' octets (see plan.h), and the pack table: for each pack of two or more tensors, the
-// first pack octet of each of its tensors and the pack's total (its item's o0 says where they start). Tensors of up
-// to 512 octets (and at most io) are packed, up to 1024 octets a pack (and at most 2 io): measured best on GB300 for
-// lists of thousands of small tensors.
-static std::vector<WorkItem> build_items(const int64_t* n, int32_t T, int32_t io, std::vector<int32_t>* pack_pre) {
+// Work items over the tensors' octets (see plan.h), and the pack table. A pack of two or more tensors numbers its
+// octets whole octets of aligned tensors first (tensor by tensor), then the rest (each aligned tensor's partial last
+// octet, every octet of an unaligned tensor), so that the element-by-element octets share warps with each other and
+// not with the vector ones; its row of the pack table (from its item's o0) is the first whole octet of each tensor
+// and the whole octets' total, then the first of each tensor's other octets and their total (2 count + 2 entries).
+// Tensors of up to 512 octets (and at most io) are packed, up to 1024 octets a pack (and at most 2 io): measured
+// best on GB300 for lists of thousands of small tensors.
+static std::vector<WorkItem> build_items(const int64_t* n, const TensorRec* recs, int32_t T, int32_t io,
+                                         std::vector<int32_t>* pack_pre) {
     std::vector<WorkItem> items;
     const int64_t small = std::min<int64_t>(512, io);
     const int64_t pack_cap = std::min<int64_t>(1024, 2 * (int64_t)io);
@@ -264,10 +268,17 @@ static std::vector<WorkItem> build_items(const int64_t* n, int32_t T, int32_t io
         if (!open) return;
         if (pack.count > 1) {
             pack.o0 = (int64_t)pack_pre->size();
+            auto whole = [&](int32_t k) { return recs[k].vec ? n[k] / kOct : (int64_t)0; };
             int32_t at = 0;
             for (int32_t j = 0; j < pack.count; ++j) {
                 pack_pre->push_back(at);
-                at += (int32_t)((n[pack.t + j] + kOct - 1) / kOct);
+                at += (int32_t)whole(pack.t + j);
+            }
+            pack_pre->push_back(at);
+            at = 0;
+            for (int32_t j = 0; j < pack.count; ++j) {
+                pack_pre->push_back(at);
+                at += (int32_t)((n[pack.t + j] + kOct - 1) / kOct - whole(pack.t + j));
             }
             pack_pre->push_back(at);
         }
@@ -484,7 +495,7 @@ static mica_status build_plan(const ListDesc& L, int device, uint64_t h, Plan** 
         plan->chunks.total_octs = total_octs;
     } else {
         plan->item_octs = choose_item_octs(total_octs, sms, base_item_octs(L.kind, L.mdt));
-        items = build_items(L.n, L.T, plan->item_octs, &pack_pre);
+        items = build_items(L.n, recs.data(), L.T, plan->item_octs, &pack_pre);
         if (items.size() > (size_t)INT32_MAX) return fail(MICA_ERR_COUNT, "too many work items (%zu)", items.size());
         plan->num_items = (int32_t)items.size();
     }

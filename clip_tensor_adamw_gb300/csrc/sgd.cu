@@ -129,28 +129,42 @@ __device__ __forceinline__ void sgd_range(const TensorRec& r, int64_t ob, int64_
     }
 }
 
-// A pack of small tensors, its octets spread over the CTA's threads (as the AdamW kernel's packs).
+// The last j in [j, count) with pre[j] <= q, given pre[j] <= q already (pre non-decreasing).
+__device__ __forceinline__ int32_t pack_search(const int32_t* __restrict__ pre, int32_t j, int32_t count, int32_t q) {
+    int32_t hi = count - 1;
+    while (j < hi) {
+        const int32_t mid = (j + hi + 1) >> 1;
+        if (__ldg(pre + mid) <= q) j = mid;
+        else hi = mid - 1;
+    }
+    return j;
+}
+
+// A pack of small tensors, its octets spread over the CTA's threads, whole octets first (as the AdamW kernel's
+// packs).
 template <Dtype G, bool kMomentum, bool kSkip>
 __device__ __forceinline__ void sgd_pack(const TensorRec* __restrict__ recs, const WorkItem& item,
                                          const int32_t* __restrict__ pack_pre, const SgdScalars& s, Factor& fac) {
-    const int32_t* pre = pack_pre + item.o0;
+    const int32_t* pre_w = pack_pre + item.o0;
+    const int32_t* pre_e = pre_w + item.count + 1;
     for (int32_t i = threadIdx.x; i < item.count; i += kThreads) {  // the pack into L2 first, one tensor a thread
         const TensorRec r = recs[item.t + i];
         if (r.vec && r.n >= kOct) sgd_prefetch<G, kMomentum>(r, 0, r.n / kOct);
     }
-    const int32_t total = __ldg(pre + item.count);
-    int32_t j = 0;
+    const int32_t total_w = __ldg(pre_w + item.count);
+    const int32_t total = total_w + __ldg(pre_e + item.count);
+    int32_t jw = 0, je = 0;
     for (int32_t q = threadIdx.x; q < total; q += kThreads) {
-        int32_t hi = item.count - 1;
-        while (j < hi) {
-            const int32_t mid = (j + hi + 1) >> 1;
-            if (__ldg(pre + mid) <= q) j = mid;
-            else hi = mid - 1;
+        if (q < total_w) {
+            jw = pack_search(pre_w, jw, item.count, q);
+            const TensorRec r = recs[item.t + jw];
+            sgd_vec_octet<G, kMomentum, kSkip>(r, q - __ldg(pre_w + jw), s, fac);
+        } else {
+            const int32_t qe = q - total_w;
+            je = pack_search(pre_e, je, item.count, qe);
+            const TensorRec r = recs[item.t + je];
+            sgd_oct_elements<G, kMomentum, kSkip>(r, (r.vec ? r.n / kOct : 0) + (qe - __ldg(pre_e + je)), s, fac);
         }
-        const TensorRec r = recs[item.t + j];
-        const int64_t o = q - __ldg(pre + j);
-        if (r.vec && o < r.n / kOct) sgd_vec_octet<G, kMomentum, kSkip>(r, o, s, fac);
-        else sgd_oct_elements<G, kMomentum, kSkip>(r, o, s, fac);
     }
 }
 
