@@ -370,13 +370,16 @@ struct AdamwLaunch {
 
 template <Dtype G, Dtype M, bool kCoupled, bool kSkip, bool kGrouped>
 cudaError_t launch_adamw_t(const AdamwLaunch& a) {
-    static int per_sm = 0;  // CTAs of this instantiation that fit on one SM
-    if (per_sm <= 0) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, adamw_kernel<G, M, kCoupled, kSkip, kGrouped>,
-                                                          kThreads, 0) != cudaSuccess ||
-            per_sm <= 0)
-            per_sm = 1;
-    }
+    static const int per_sm = [] {  // CTAs of this instantiation that fit on one SM (found once, thread-safely)
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, adamw_kernel<G, M, kCoupled, kSkip, kGrouped>, kThreads,
+                                                          0) != cudaSuccess ||
+            n <= 0) {
+            cudaGetLastError();
+            n = 1;
+        }
+        return n;
+    }();
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.queue ? persistent_grid(a.num_items, per_sm, a.sms) : a.num_items);
     cfg.blockDim = dim3(kThreads);

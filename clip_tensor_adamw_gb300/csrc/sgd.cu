@@ -201,13 +201,16 @@ __global__ void __launch_bounds__(kThreads, 3) sgd_kernel(const TensorRec* __res
 
 template <Dtype G, bool kMomentum, bool kSkip>
 cudaError_t launch_sgd_t(const UpdateLaunch& u, const SgdScalars& s, const float* d_factor, cudaStream_t st) {
-    static int per_sm = 0;  // CTAs of this instantiation that fit on one SM
-    if (per_sm <= 0) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sgd_kernel<G, kMomentum, kSkip>, kThreads, 0) !=
+    static const int per_sm = [] {  // CTAs of this instantiation that fit on one SM (found once, thread-safely)
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sgd_kernel<G, kMomentum, kSkip>, kThreads, 0) !=
                 cudaSuccess ||
-            per_sm <= 0)
-            per_sm = 1;
-    }
+            n <= 0) {
+            cudaGetLastError();
+            n = 1;
+        }
+        return n;
+    }();
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(u.queue ? persistent_grid(u.num_items, per_sm, u.sms) : u.num_items);
     cfg.blockDim = dim3(kThreads);
