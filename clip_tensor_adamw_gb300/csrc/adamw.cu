@@ -314,9 +314,9 @@ __device__ __forceinline__ void adam_pack(const TensorRec* __restrict__ recs, co
 }
 
 // A persistent grid (as many CTAs as fit on the GPU at once) taking the work items one at a time from `queue` (or,
-// with no queue, one CTA per item), in reverse order (the norm reads them forwards, so the gradient it read last may still be in L2 when this kernel
-// starts). Without kGrouped the scalars are read straight from the kernel's parameters; with it each tensor's group
-// picks its own (the parameter array is indexed in place).
+// with no queue, one CTA per item), in reverse order (the norm reads them forwards, so the gradient it read last may
+// still be in L2 when this kernel starts). Without kGrouped the scalars are read straight from the kernel's
+// parameters; with it each tensor's group picks its own (the parameter array is indexed in place).
 template <Dtype G, Dtype M, bool kCoupled, bool kSkip, bool kGrouped>
 __global__ void __launch_bounds__(kThreads, 3) adamw_kernel(const TensorRec* __restrict__ recs,
                                                             const WorkItem* __restrict__ items, int32_t num_items,

@@ -705,7 +705,8 @@ extern "C" mica_status mica_clip_grad_norms(const void* const* g, const int64_t*
                                             void* stream) {
     if (gdt != MICA_F32 && gdt != MICA_F16) return fail(MICA_ERR_DTYPE, "gradients must be float32 or float16");
     if (!d_factor) return fail(MICA_ERR_NULL, "d_factor is NULL");
-    if (std::isnan(max_norm) || !(max_norm > 0.0f)) return fail(MICA_ERR_HYPER, "max_norm %g is not > 0", (double)max_norm);
+    if (std::isnan(max_norm) || !(max_norm > 0.0f))
+        return fail(MICA_ERR_HYPER, "max_norm %g is not > 0", (double)max_norm);
     if (!std::isfinite(inv_scale) || !(inv_scale > 0.0f))
         return fail(MICA_ERR_HYPER, "inv_scale %g is not finite and > 0", (double)inv_scale);
     if (T < 0 || T > MICA_MAX_TENSORS) return fail(MICA_ERR_COUNT, "T = %d is outside [0, %d]", T, MICA_MAX_TENSORS);

@@ -1,11 +1,11 @@
 // mica_clip_grad_norms_noalloc: the joint norm and clip factor without any device allocation.
 //
 // mica_clip_grad_norms keeps a per-list table (tensor records, the octet prefix, chunk starts, one double per CTA
-// and a ticket) in device memory it allocates once per list. Some callers cannot let a library allocate: a runtime that reserves its
-// whole device-memory budget up front and treats any later cudaMalloc as a failure, a caller whose memory is held
-// by another allocator so that cudaMalloc would fail, or a latency-bound loop that cannot afford cudaMalloc's
-// implicit device synchronisation. This entry point runs the same norm kernel with its scratch in one file-scope
-// device array instead, which every GPU that loads this library holds until the process exits.
+// and a ticket) in device memory it allocates once per list. Some callers cannot let a library allocate: a runtime
+// that reserves its whole device-memory budget up front and treats any later cudaMalloc as a failure, a caller whose
+// memory is held by another allocator so that cudaMalloc would fail, or a latency-bound loop that cannot afford
+// cudaMalloc's implicit device synchronisation. This entry point runs the same norm kernel with its scratch in one
+// file-scope device array instead, which every GPU that loads this library holds until the process exits.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -90,7 +90,8 @@ extern "C" mica_status mica_clip_grad_norms_noalloc(const void* const* g, const 
     const size_t es = (gdt == MICA_F16) ? 2 : 4;
     int64_t total_octs = 0;
     for (int32_t k = 0; k < T; ++k) {
-        if (n[k] < 0 || n[k] > ((int64_t)1 << 40)) return noalloc_fail(MICA_ERR_COUNT, "an element count is out of range");
+        if (n[k] < 0 || n[k] > ((int64_t)1 << 40))
+            return noalloc_fail(MICA_ERR_COUNT, "an element count is out of range");
         if (n[k] == 0) continue;
         if (!g[k]) return noalloc_fail(MICA_ERR_NULL, "a gradient with n > 0 is NULL");
         if (reinterpret_cast<uintptr_t>(g[k]) % es) return noalloc_fail(MICA_ERR_ADDRESS, "a gradient is misaligned");

@@ -228,7 +228,8 @@ template <Dtype G>
 cudaError_t launch_sgd_g(const UpdateLaunch& u, bool momentum, bool skip, const SgdScalars& s, const float* d_factor,
                          cudaStream_t st) {
     if (momentum)
-        return skip ? launch_sgd_t<G, true, true>(u, s, d_factor, st) : launch_sgd_t<G, true, false>(u, s, d_factor, st);
+        return skip ? launch_sgd_t<G, true, true>(u, s, d_factor, st)
+                    : launch_sgd_t<G, true, false>(u, s, d_factor, st);
     return skip ? launch_sgd_t<G, false, true>(u, s, d_factor, st) : launch_sgd_t<G, false, false>(u, s, d_factor, st);
 }
 

@@ -1,6 +1,6 @@
-// Device helpers shared by the streaming kernels (adamw.cu, norm.cu, sgd.cu, scale.cu): 32- and 16-byte streaming accesses,
-// binary16 widening, programmatic dependent launch, the gradient factor read, L2 prefetch, and the persistent grids'
-// work queue.
+// Device helpers shared by the streaming kernels (adamw.cu, norm.cu, sgd.cu, scale.cu): 32- and 16-byte streaming
+// accesses, binary16 widening, programmatic dependent launch, the gradient factor read, L2 prefetch, and the
+// persistent grids' work queue.
 #pragma once
 
 #include <cuda_fp16.h>
