@@ -1,4 +1,4 @@
-// ScaleTensors ("Mica 7.7 ...", section "The whole model in one call"): every cell of several tensors times one
+// ScaleTensors ("Mica 7.7 ...", section "The whole model in one call"): each element of each listed tensor times one
 // factor, float32 or binary16 (widened, multiplied, rounded back to nearest-even), one CTA per work item.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>

@@ -4,7 +4,8 @@
  * Three verbs, named for those of the Mica 7.7 release note ("Mica 7.7: a training step on the card, in every float
  * type", section "The whole model in one call"):
  *
- *   mica_scale_tensors    ScaleTensors: every cell of several tensors times one factor (a float16 step's unscale).
+ *   mica_scale_tensors    ScaleTensors: each element of each listed tensor times one factor (a float16 step's
+ *                         unscale).
  *   mica_clip_grad_norms  ClipGradNorms: the joint L2 norm of every listed gradient and the clip factor, both left
  *                         in device memory ("Values that stay on the card"); the gradients are not rewritten.
  *   mica_adamw_steps      AdamWSteps: AdamW over every (w, g, m, v) group in one launch, each group updated exactly

@@ -9,7 +9,7 @@
  *   [MICA]  "Mica 7.7: a training step on the card, in every float type", sections "The whole model in one call"
  *           and "Values that stay on the card": ClipGradNorms caps the joint L2 norm of every listed gradient;
  *           AdamWSteps updates each (w, g, m, v) group exactly as a single-group AdamWStep would; ScaleTensors
- *           multiplies every cell of several tensors by one factor (the unscaling of a float16 step).
+ *           scales each element of each listed tensor by a single factor (a float16 step's unscale).
  *   [OPT]   BendTorch "main.bend", section "Optimizers": AdamW element by element in PyTorch's order of
  *           operations, the gradient written back as zero, c1 = 1 - b1 and c2 = 1 - b2 taken as constants of
  *           their own; the same section's plain SGD (w + (-lr) g) and SGD with momentum (b = b mu + g,
