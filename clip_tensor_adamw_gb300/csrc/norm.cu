@@ -210,36 +210,70 @@ struct StagedSpan {
     int32_t vec[kStaged];
 };
 
+// One gradient octet as loaded, before it is used: binary16 as its 4 words, float32 as its 8 values. Fetching the
+// four octets of a round first and widening them afterwards keeps all four loads in flight at once.
+template <Dtype G>
+struct RawOctet;
+template <>
+struct RawOctet<kF16> {
+    uint4 h;
+};
+template <>
+struct RawOctet<kF32> {
+    float x[8];
+};
+
 // Gradient octet `local` of staged tensor j (zeros past its end): one 32-byte load (16 for binary16) when whole and
 // aligned, else element by element.
 template <Dtype G>
-__device__ __forceinline__ void load_staged_octet(const StagedSpan& sp, int32_t j, int64_t local, float (&x)[8]) {
+__device__ __forceinline__ void fetch_staged_octet(const StagedSpan& sp, int32_t j, int64_t local, RawOctet<G>& r) {
     const char* base = sp.base[j];
     const int64_t n = sp.n[j];
     if (sp.vec[j] && local < n / kOct) {
         if constexpr (G == kF16) {
-            uint4 h;
             asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(h.x), "=r"(h.y), "=r"(h.z), "=r"(h.w)
+                         : "=r"(r.h.x), "=r"(r.h.y), "=r"(r.h.z), "=r"(r.h.w)
                          : "l"(base + local * 16));
-            h8_to(h, x);
         } else {
             asm volatile("ld.global.L1::no_allocate.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                         : "=f"(x[0]), "=f"(x[1]), "=f"(x[2]), "=f"(x[3]), "=f"(x[4]), "=f"(x[5]), "=f"(x[6]),
-                           "=f"(x[7])
+                         : "=f"(r.x[0]), "=f"(r.x[1]), "=f"(r.x[2]), "=f"(r.x[3]), "=f"(r.x[4]), "=f"(r.x[5]),
+                           "=f"(r.x[6]), "=f"(r.x[7])
                          : "l"(base + local * 32));
         }
     } else {
         const int64_t i0 = local * kOct;
+        if constexpr (G == kF16) {
+            const uint16_t* p = reinterpret_cast<const uint16_t*>(base) + i0;
+            uint32_t hv[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            if (i0 + e < n) {
-                x[e] = (G == kF16) ? __half2float(reinterpret_cast<const __half*>(base)[i0 + e])
-                                   : reinterpret_cast<const float*>(base)[i0 + e];
-            } else {
-                x[e] = 0.0f;
-            }
+            for (int e = 0; e < 8; ++e) hv[e] = (i0 + e < n) ? p[e] : 0u;
+            r.h = make_uint4(hv[0] | (hv[1] << 16), hv[2] | (hv[3] << 16), hv[4] | (hv[5] << 16),
+                             hv[6] | (hv[7] << 16));
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) r.x[e] = (i0 + e < n) ? reinterpret_cast<const float*>(base)[i0 + e] : 0.0f;
         }
+    }
+}
+
+template <Dtype G>
+__device__ __forceinline__ void zero_octet(RawOctet<G>& r) {
+    if constexpr (G == kF16) {
+        r.h = make_uint4(0u, 0u, 0u, 0u);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) r.x[e] = 0.0f;
+    }
+}
+
+// The octet's values as float32 (binary16 widened exactly).
+template <Dtype G>
+__device__ __forceinline__ void widen_octet(const RawOctet<G>& r, float (&x)[8]) {
+    if constexpr (G == kF16) {
+        h8_to(r.h, x);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = r.x[e];
     }
 }
 
@@ -281,20 +315,23 @@ __global__ void __launch_bounds__(kThreads, kNormDirectCtasPerSm) norm_direct_ke
         const int64_t oe = sp.lo[cnt] < c1 ? sp.lo[cnt] : c1;
         int32_t j = 0;
         for (int64_t o = ob + t; o < oe; o += 4 * kThreads) {
-            float x[4][8];
+            RawOctet<G> raw[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int64_t q = o + (int64_t)u * kThreads;
                 if (q < oe) {
                     while (q >= sp.lo[j + 1]) ++j;
-                    load_staged_octet<G>(sp, j, q - sp.lo[j], x[u]);
+                    fetch_staged_octet<G>(sp, j, q - sp.lo[j], raw[u]);
                 } else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) x[u][e] = 0.0f;
+                    zero_octet<G>(raw[u]);
                 }
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) acc.add8<kMode>(x[u], inv_scale);
+            for (int u = 0; u < 4; ++u) {
+                float x[8];
+                widen_octet<G>(raw[u], x);
+                acc.add8<kMode>(x, inv_scale);
+            }
         }
         ob = oe;
         k += cnt;
