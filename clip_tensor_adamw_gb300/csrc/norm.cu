@@ -280,8 +280,8 @@ __device__ __forceinline__ void widen_octet(const RawOctet<G>& r, float (&x)[8])
 // The joint norm for lists of many small tensors, where a stage of the TMA pipeline would cross several tensors:
 // CTA b streams its equal, contiguous chunk of the list's octets straight into registers. The CTA stages the
 // chunk's tensors (their octet ranges, bases, sizes) in shared memory up to kStaged at a time; thread t takes the
-// staged span's octets c + t, c + t + 256, ..., four at a time (all four loads in flight before they are summed),
-// finding each octet's tensor by walking the staged table forwards. The rest is as in norm_tma_kernel.
+// staged span's octets c + t, c + t + 256, ..., four at a time (eight for binary16), all their loads in flight
+// before any is widened and summed, finding each octet's tensor by walking the staged table forwards. The rest is as in norm_tma_kernel.
 template <Dtype G, int kMode>
 __global__ void __launch_bounds__(kThreads, kNormDirectCtasPerSm) norm_direct_kernel(ChunkTable ct, float inv_scale,
                                                                         double* __restrict__ partials,
@@ -314,10 +314,11 @@ __global__ void __launch_bounds__(kThreads, kNormDirectCtasPerSm) norm_direct_ke
         __syncthreads();
         const int64_t oe = sp.lo[cnt] < c1 ? sp.lo[cnt] : c1;
         int32_t j = 0;
-        for (int64_t o = ob + t; o < oe; o += 4 * kThreads) {
-            RawOctet<G> raw[4];
+        constexpr int U = (G == kF16) ? 8 : 4;  // octets in flight per thread (a binary16 octet is 4 registers)
+        for (int64_t o = ob + t; o < oe; o += U * kThreads) {
+            RawOctet<G> raw[U];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < U; ++u) {
                 const int64_t q = o + (int64_t)u * kThreads;
                 if (q < oe) {
                     while (q >= sp.lo[j + 1]) ++j;
@@ -327,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, kNormDirectCtasPerSm) norm_direct_ke
                 }
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < U; ++u) {
                 float x[8];
                 widen_octet<G>(raw[u], x);
                 acc.add8<kMode>(x, inv_scale);
