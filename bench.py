@@ -18,6 +18,7 @@ import hashlib
 import json
 import math
 import os
+import platform
 import re
 import statistics
 import subprocess
@@ -203,6 +204,20 @@ def time_oracle(wl: workloads.Workload, target_params: int, min_seconds: float, 
     return params, ntens, times
 
 
+def host_cpu() -> dict:
+    """The host the CPU baseline ran on: its architecture, CPU model (as /proc/cpuinfo names it) and thread count."""
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            fields = dict(line.split(":", 1) for line in f if ":" in line)
+        fields = {k.strip(): v.strip() for k, v in fields.items()}
+        model = fields.get("model name") or (
+            f"implementer {fields.get('CPU implementer', '?')} part {fields.get('CPU part', '?')}")
+    except OSError:
+        pass
+    return {"arch": platform.machine(), "cpu": model, "nproc": os.cpu_count()}
+
+
 def run_config(wl: workloads.Workload, world: int) -> dict:
     """The `config` of both arms' JSON lines: the workload the metric is quoted on."""
     bpp = step_bytes_per_param(wl)
@@ -234,7 +249,8 @@ def run_reference(args, wl: workloads.Workload) -> None:
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": run_config(wl, args.gpus),
-        "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle", "sample": sample,
+                         "host": host_cpu()},
         "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -500,6 +516,7 @@ def main():
                "d2h_bytes_per_step": d2h}
         params, ntens, times = time_oracle(wl, target_params=wl.params, min_seconds=10.0, max_steps=20)
         cpu = {"value": params * len(times) / sum(times), "unit": "params/s", "cores": 1, "kind": "oracle",
+               "host": host_cpu(),
                "sample": f"{len(times)} full steps of the first {ntens} of {len(wl.sizes)} tensors "
                          f"({params:,} params) of {wl.name}, single-threaded C oracle"}
 
