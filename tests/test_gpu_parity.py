@@ -400,3 +400,32 @@ def test_gpt2_xl_sampled(ora):
         else:
             parity.bf16_within_one_ulp(gm, m_s, 2 * gm.size, f"xl m step {t}")
             parity.bf16_within_one_ulp(gv, v_s, 2 * gv.size, f"xl v step {t}")
+
+
+# ------------------------------------------------------------------------------------------------------------------
+# the per-list table cache
+# ------------------------------------------------------------------------------------------------------------------
+
+def test_table_cache_eviction_and_release(ora):
+    """More distinct lists than the cache holds (it is then emptied and refilled), and mica_release_cache between
+    steps: every step's norm and update still match the oracle."""
+    wl = W["tiny"]
+    st = workloads.make_state(wl, "cuda")
+    workloads.fill_grad(st, 1)
+    host_g = workloads.host_lists(st)[1]
+    factor = torch.empty(1, device="cuda")
+    norm = torch.empty(1, device="cuda")
+    # 1,100 distinct one-tensor lists (views at different offsets of the first gradient): each gets its own table
+    g0 = st.g[0]
+    for i in range(1100):
+        view = g0[i:i + 64]
+        mica.mica_clip_grad_norms([view], 1e9, 1.0, norm_out=norm, factor_out=factor)
+        if i % 250 == 0 or i == 1099:
+            o_norm, _, _ = ora.clip_grad_norms([host_g[0][i:i + 64].copy()], 1e9)
+            torch.cuda.synchronize()
+            parity.check_norm(np.float32(norm.item()), o_norm, i)
+    mica.mica_release_cache()
+    # a full step after the release rebuilds its tables and still matches
+    r = parity.run_parity(wl, steps=2, ora=ora)
+    assert r["same_factor_every_step"]
+    mica.mica_sync()
