@@ -75,14 +75,34 @@ def describe(wl: workloads.Workload) -> str:
 # peaks, profiles, clocks
 # ----------------------------------------------------------------------------------------------------------------
 
-def hbm_peak() -> tuple[float, str]:
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+def _hbm_gbs_in(d) -> float | None:
+    """The HBM copy bandwidth in GB/s in a peaks record: the first number whose key path names HBM (or DRAM /
+    memory) and a GB/s or TB/s unit, searched depth-first; a TB/s figure is converted."""
+    found = []
+
+    def walk(x, path):
+        if isinstance(x, dict):
+            for k, v in x.items():
+                walk(v, path + [str(k).lower()])
+        elif isinstance(x, (int, float)) and not isinstance(x, bool) and x > 0:
+            key = "_".join(path)
+            if any(m in key for m in ("hbm", "dram", "mem")) and "bf16" not in key and "tflop" not in key:
+                if any(u in key for u in ("gbs", "gb_s", "gbps", "gb/s")):
+                    found.append(float(x))
+                elif any(u in key for u in ("tbs", "tb_s", "tbps", "tb/s")):
+                    found.append(1e3 * float(x))
+    walk(d, [])
+    return found[0] if found else None
+
+
+def hbm_peak(path: str | None = None) -> tuple[float, str]:
+    """The measured HBM copy peak (GB/s) from MEASURED_PEAKS.json when present, else the fallback figure."""
+    path = path or os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
-            d = json.load(f)
-        for k in ("hbm_gbs", "hbm_copy_gbs", "hbm_GBps"):
-            if k in d and float(d[k]) > 0:
-                return float(d[k]), "measured"
+            v = _hbm_gbs_in(json.load(f))
+        if v is not None and 100.0 < v < 100000.0:
+            return v, "measured"
     except (OSError, ValueError):
         pass
     return FALLBACK_HBM_GBS, "fallback"

@@ -3,6 +3,7 @@
 Every rank steps its own full parameter list (replicas), the job's time is the slowest rank's (a MAX all-reduce),
 and the job's value counts every rank's parameters. The reference arm prints only on rank 0."""
 import io
+import json
 import os
 import socket
 import sys
@@ -56,3 +57,20 @@ def test_reference_arm_prints_on_rank_zero_only(monkeypatch):
         with redirect_stdout(buf):
             bench.run_reference(Args(), wl)
         assert (expect in buf.getvalue()) if expect else buf.getvalue() == ""
+
+
+def test_hbm_peak_from_measured_peaks_file(tmp_path):
+    """The roofline's denominator is read from the peaks record whatever its layout, else the fallback is used."""
+    import bench
+    cases = [({"hbm_gbs": 6781.0}, 6781.0), ({"hbm": {"copy_gbs": 6781.5}}, 6781.5),
+             ({"peaks": {"hbm_copy_GBps": 6700}}, 6700.0), ({"hbm_tbs": 6.781}, 6781.0),
+             ({"bf16_tflops": 1900.0, "hbm_gbs": 6790}, 6790.0), ({"bf16_tflops": 1900.0}, None), ({}, None)]
+    for record, want in cases:
+        p = tmp_path / "peaks.json"
+        p.write_text(json.dumps(record))
+        v, src = bench.hbm_peak(str(p))
+        if want is None:
+            assert src == "fallback" and v == bench.FALLBACK_HBM_GBS, record
+        else:
+            assert src == "measured" and abs(v - want) < 1e-6, (record, v)
+    assert bench.hbm_peak(str(tmp_path / "missing.json"))[1] == "fallback"
