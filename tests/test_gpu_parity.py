@@ -4,6 +4,7 @@ Small cases span many work items and ragged tails and run 10 consecutive steps c
 full-size workloads run in the launch configuration the benchmark times (the same cached tables, item sizes and
 grids), compared in full (GPT-2 small, the loss-scaled list) or on sampled elements (GPT-2 XL)."""
 import dataclasses
+import os
 
 import numpy as np
 import pytest
@@ -429,3 +430,50 @@ def test_table_cache_eviction_and_release(ora):
     r = parity.run_parity(wl, steps=2, ora=ora)
     assert r["same_factor_every_step"]
     mica.mica_sync()
+
+
+# ------------------------------------------------------------------------------------------------------------------
+# resume, and the synchronous debug tier
+# ------------------------------------------------------------------------------------------------------------------
+
+def test_resume_from_saved_state():
+    """The optimizer's state is the caller's buffers and the step count: saving w, m, v to the host after step 3,
+    restoring them into new buffers and going on from t = 4 gives the same bits as six uninterrupted steps."""
+    wl = W["gpt2_small_bf16"]
+    sizes = small_gpt2_sizes()
+    a = workloads.make_state(wl, "cuda", sizes=sizes)
+    la = parity.tensor_lists(a)
+    for t in range(1, 7):
+        workloads.fill_grad(a, t)
+        parity.gpu_step(a, la, t)
+    b = workloads.make_state(wl, "cuda", sizes=sizes)
+    lb = parity.tensor_lists(b)
+    for t in range(1, 4):
+        workloads.fill_grad(b, t)
+        parity.gpu_step(b, lb, t)
+    torch.cuda.synchronize()
+    saved = [x.cpu().clone() for x in (b.w_flat, b.m_flat, b.v_flat)]
+    c = workloads.make_state(wl, "cuda", sizes=sizes, seed=12345)  # other buffers, other initial values
+    for dst, src in zip((c.w_flat, c.m_flat, c.v_flat), saved):
+        dst.copy_(src)
+    lc = parity.tensor_lists(c)
+    for t in range(4, 7):
+        workloads.fill_grad(c, t, seed=wl.seed)
+        parity.gpu_step(c, lc, t)
+    torch.cuda.synchronize()
+    for x, y in ((a.w_flat, c.w_flat), (a.m_flat, c.m_flat), (a.v_flat, c.v_flat)):
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+    mica.mica_sync()
+
+
+def test_sync_debug_tier(tmp_path):
+    """With MICA_SYNC_DEBUG=1 every call waits for its own kernels; a step still matches the oracle."""
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = ("import sys; sys.path[:0] = [%r, %r]; import parity, workloads; "
+            "r = parity.run_parity(workloads.WORKLOADS['tiny'], steps=2); "
+            "assert r['same_factor_every_step']; print('ok')" % (root, os.path.join(root, "tests")))
+    env = dict(os.environ, MICA_SYNC_DEBUG="1")
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0 and "ok" in out.stdout, out.stderr[-2000:]
