@@ -313,6 +313,25 @@ __device__ __forceinline__ void adam_pack(const TensorRec* __restrict__ recs, co
     }
 }
 
+// L2 prefetch of one item's whole octets: the slice's, or every tensor of the pack (one tensor a thread).
+template <Dtype G, Dtype M>
+__device__ __forceinline__ void prefetch_item(const TensorRec* __restrict__ recs, const WorkItem& item,
+                                              int32_t item_octs) {
+    if (item.count == 1) {
+        if (threadIdx.x == 0) {
+            const TensorRec r = recs[item.t];
+            const int64_t full = r.n / kOct;
+            const int64_t oe = item.o0 + item_octs < full ? item.o0 + item_octs : full;
+            if (r.vec && oe > item.o0) prefetch_octets<G, M>(r, item.o0, oe);
+        }
+    } else {
+        for (int32_t i = threadIdx.x; i < item.count; i += kThreads) {
+            const TensorRec r = recs[item.t + i];
+            if (r.vec && r.n >= kOct) prefetch_octets<G, M>(r, 0, r.n / kOct);
+        }
+    }
+}
+
 // A persistent grid (as many CTAs as fit on the GPU at once) taking the work items one at a time from `queue` (or,
 // with no queue, one CTA per item), in reverse order (the norm reads them forwards, so the gradient it read last may
 // still be in L2 when this kernel starts). Without kGrouped the scalars are read straight from the kernel's
@@ -331,6 +350,11 @@ __global__ void __launch_bounds__(kThreads, 3) adamw_kernel(const TensorRec* __r
     const bool persistent = queue != nullptr;  // else one CTA per item: item blockIdx.x
     if (threadIdx.x == 0) s_item[0] = persistent ? queue_take(queue) : (int32_t)blockIdx.x;
     __syncthreads();
+    // Until the kernel queued before this one has finished, its writes to these tensors may still be on their way:
+    // the CTA only asks L2 for its first item's data (L2 keeps global memory coherent, so a prefetch cannot return
+    // stale data to a later load), and every load of w, g, m and v follows the wait.
+    if (s_item[0] < num_items) prefetch_item<G, M>(recs, items[num_items - 1 - s_item[0]], item_octs);
+    fac.get();
     int32_t cur = 0;
     for (int32_t k = s_item[0]; k < num_items; k = s_item[cur]) {
         if (threadIdx.x == 0) s_item[cur ^ 1] = persistent ? queue_take(queue) : num_items;

@@ -290,7 +290,6 @@ __global__ void __launch_bounds__(kThreads, kNormDirectCtasPerSm) norm_direct_ke
     __shared__ double red[kWarps];
     __shared__ int last;
     __shared__ StagedSpan sp;
-    allow_dependents();
     const int t = threadIdx.x;
     const int64_t c0 = ct.total_octs * blockIdx.x / ct.grid;
     const int64_t c1 = ct.total_octs * (blockIdx.x + 1) / ct.grid;
@@ -298,6 +297,7 @@ __global__ void __launch_bounds__(kThreads, kNormDirectCtasPerSm) norm_direct_ke
 
     SumSq acc{{0.f, 0.f}, {0.f, 0.f}, 0.f};
     wait_prerequisite();  // the kernel queued before may still be writing the gradients (zero_grad)
+    allow_dependents();   // the kernel queued next may launch from here (as in the TMA kernel)
     int32_t k = k0;
     int64_t ob = c0;
     while (ob < c1) {
@@ -446,7 +446,6 @@ __global__ void __launch_bounds__(kNormThreads, kNormTmaCtasPerSm) norm_tma_kern
     __shared__ __align__(8) uint64_t empty[S];
     __shared__ double red[kWarps + 1];
     __shared__ int last;
-    allow_dependents();
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int64_t c0 = ct.total_octs * blockIdx.x / ct.grid;
     const int64_t c1 = ct.total_octs * (blockIdx.x + 1) / ct.grid;
@@ -461,6 +460,10 @@ __global__ void __launch_bounds__(kNormThreads, kNormTmaCtasPerSm) norm_tma_kern
     }
     __syncthreads();
     wait_prerequisite();  // the kernel queued before may still be writing the gradients (zero_grad)
+    // The kernel queued next (the update) may launch from here, once every kernel before the norm has finished: so
+    // at most the norm and the update are in flight at once, and the update's early CTAs do not take room on the SMs
+    // from a kernel that is still running.
+    allow_dependents();
 
     double mine = 0.0;
     if (warp == kWarps) {

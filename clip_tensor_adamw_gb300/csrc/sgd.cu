@@ -168,6 +168,25 @@ __device__ __forceinline__ void sgd_pack(const TensorRec* __restrict__ recs, con
     }
 }
 
+// L2 prefetch of one item's whole octets: the slice's, or every tensor of the pack (one tensor a thread).
+template <Dtype G, bool kMomentum>
+__device__ __forceinline__ void sgd_prefetch_item(const TensorRec* __restrict__ recs, const WorkItem& item,
+                                                  int32_t item_octs) {
+    if (item.count == 1) {
+        if (threadIdx.x == 0) {
+            const TensorRec r = recs[item.t];
+            const int64_t full = r.n / kOct;
+            const int64_t oe = item.o0 + item_octs < full ? item.o0 + item_octs : full;
+            if (r.vec && oe > item.o0) sgd_prefetch<G, kMomentum>(r, item.o0, oe);
+        }
+    } else {
+        for (int32_t i = threadIdx.x; i < item.count; i += kThreads) {
+            const TensorRec r = recs[item.t + i];
+            if (r.vec && r.n >= kOct) sgd_prefetch<G, kMomentum>(r, 0, r.n / kOct);
+        }
+    }
+}
+
 // A persistent grid taking the items from `queue` (or, with no queue, one CTA per item), as the AdamW kernel does.
 template <Dtype G, bool kMomentum, bool kSkip>
 __global__ void __launch_bounds__(kThreads, 3) sgd_kernel(const TensorRec* __restrict__ recs,
@@ -181,6 +200,9 @@ __global__ void __launch_bounds__(kThreads, 3) sgd_kernel(const TensorRec* __res
     const bool persistent = queue != nullptr;  // else one CTA per item: item blockIdx.x
     if (threadIdx.x == 0) s_item[0] = persistent ? queue_take(queue) : (int32_t)blockIdx.x;
     __syncthreads();
+    // only an L2 prefetch before the wait for the kernel queued before (as in the AdamW kernel)
+    if (s_item[0] < num_items) sgd_prefetch_item<G, kMomentum>(recs, items[num_items - 1 - s_item[0]], item_octs);
+    fac.get();
     int32_t cur = 0;
     for (int32_t k = s_item[0]; k < num_items; k = s_item[cur]) {
         if (threadIdx.x == 0) s_item[cur ^ 1] = persistent ? queue_take(queue) : num_items;
