@@ -310,6 +310,32 @@ static std::vector<WorkItem> build_items(const int64_t* n, const TensorRec* recs
     return items;
 }
 
+// The order the update kernels take the items in (they walk the array from its end): the packs first, spread
+// evenly over as many slices as there are packs, then the other slices. A pack's CTA waits on memory latency far
+// more than a slice's does (its threads' octets lie in many small tensors), so the packs run while slice CTAs keep
+// HBM busy, and the launch ends on slices, its shortest and most even items, rather than on a wave of packs. Each
+// kind keeps its own order (slices from the end of the list first).
+static void order_items(std::vector<WorkItem>& items) {
+    const size_t N = items.size();
+    std::vector<WorkItem> S, P;  // in the order they are taken
+    for (size_t j = 0; j < N; ++j) {
+        const WorkItem& it = items[N - 1 - j];
+        (it.count > 1 ? P : S).push_back(it);
+    }
+    if (P.empty() || S.empty()) return;
+    const int64_t np = (int64_t)P.size();
+    const int64_t head = std::min<int64_t>((int64_t)S.size(), np);  // slices the packs are spread over
+    std::vector<WorkItem> order;
+    order.reserve(N);
+    int64_t is = 0, ip = 0;
+    while (is < head || ip < np) {
+        if (ip < np && (is >= head || ip * head <= is * np)) order.push_back(P[(size_t)ip++]);
+        else order.push_back(S[(size_t)is++]);
+    }
+    while ((size_t)is < S.size()) order.push_back(S[(size_t)is++]);
+    for (size_t j = 0; j < N; ++j) items[N - 1 - j] = order[j];
+}
+
 static uint64_t ptr_u(const void* p) { return (uint64_t) reinterpret_cast<uintptr_t>(p); }
 
 struct ListDesc {
@@ -496,6 +522,7 @@ static mica_status build_plan(const ListDesc& L, int device, uint64_t h, Plan** 
     } else {
         plan->item_octs = choose_item_octs(total_octs, sms, base_item_octs(L.kind, L.mdt));
         items = build_items(L.n, recs.data(), L.T, plan->item_octs, &pack_pre);
+        order_items(items);
         if (items.size() > (size_t)INT32_MAX) return fail(MICA_ERR_COUNT, "too many work items (%zu)", items.size());
         plan->num_items = (int32_t)items.size();
     }
