@@ -2,7 +2,8 @@
 // parameter groups), over float32, packed BF16 or packed-m / float32-v moments. It streams HBM with no data reuse, so
 // it is built for bandwidth: a persistent grid fed by a work queue, 32-byte vector accesses (sm_100's 256-bit loads
 // and stores) that coalesce across a warp, evict-first cache hints, L2 prefetch ahead of the loads, and a launch as
-// a programmatic dependent of the norm so that its loads start while the norm finishes.
+// a programmatic dependent of the norm, so that its CTAs are resident and have asked L2 for their first data by the
+// time the norm finishes.
 //
 // Per-element arithmetic follows BendTorch "main.bend", section "Optimizers": every float32 operation is a separate
 // correctly rounded intrinsic (__fmul_rn, __fadd_rn, __fdiv_rn, __fsqrt_rn), which the compiler never fuses into an

@@ -128,9 +128,9 @@ inline int32_t persistent_grid(int32_t num_items, int per_sm, int sms) {
 
 // Kernel launchers (adamw.cu, sgd.cu, norm.cu, scale.cu). Each returns the cudaError_t of its launch as an int.
 // AdamW (or, with `coupled`, Adam with the coupled L2 term) over every item. It is launched as a programmatic
-// dependent of the kernel queued before it: it may start and load its tensors while that kernel finishes, and reads
-// d_factor only once that kernel has completed. With `groups`, tensor k takes neg_step, dec and wd from entry
-// recs[k].group of it instead of from s.
+// dependent of the kernel queued before it: it may start while that kernel finishes and ask L2 for its first item's
+// data, but reads w, g, m, v and d_factor only once that kernel has completed. With `groups`, tensor k takes
+// neg_step, dec and wd from entry recs[k].group of it instead of from s.
 int launch_adamw(const UpdateLaunch& u, Dtype gdt, Dtype mdt, bool coupled, const StepScalars& s,
                  const GroupScalars* groups, const float* d_factor, void* stream);
 // SGD (momentum false) or SGD with momentum over every item, launched as AdamW is. `skip`: leave w (and the

@@ -5,9 +5,9 @@
 //
 // Same work items and access scheme as the AdamW kernel: a persistent grid whose CTAs take the items (a slice of a
 // large tensor, or a pack of small tensors whose octets the threads share out) one at a time from a queue, 32-byte
-// streaming loads and stores, L2 prefetch two rounds ahead on the slices, and a programmatic-dependent launch so that
-// the loads start while the norm kernel finishes. Every float operation is a separate correctly rounded intrinsic,
-// in the page's order, so the result is bit-identical to the same step on the CPU.
+// streaming loads and stores, L2 prefetch two rounds ahead on the slices, and a programmatic-dependent launch whose
+// CTAs only ask L2 for their first item before the norm has finished. Every float operation is a separate correctly
+// rounded intrinsic, in the page's order, so the result is bit-identical to the same step on the CPU.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 

@@ -34,6 +34,9 @@
  *     A fault of earlier queued work surfaces as MICA_ERR_CUDA from a later call or from mica_sync(). With the
  *     environment variable MICA_SYNC_DEBUG=1 every call waits for its own kernels, so a fault is reported by the
  *     call that caused it.
+ *   - Two more environment variables tune the update kernels and never change a result: MICA_ITEM_OCTS (a power of
+ *     two from 16 to 2^20, read when a list's table is built) replaces the octets per work item, and
+ *     MICA_UPDATE_GRID=items (read at each call) runs one CTA per work item instead of the persistent grid.
  *   - A tensor with n[i] == 0 is skipped and its pointers may be NULL. T == 0 is allowed.
  *   - mica_last_error_detail() gives a one-line description of the last error on the calling thread.
  */

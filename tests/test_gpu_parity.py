@@ -477,3 +477,26 @@ def test_sync_debug_tier(tmp_path):
     env = dict(os.environ, MICA_SYNC_DEBUG="1")
     out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
     assert out.returncode == 0 and "ok" in out.stdout, out.stderr[-2000:]
+
+
+@pytest.mark.parametrize("env", [{"MICA_ITEM_OCTS": "16"},
+                                 {"MICA_ITEM_OCTS": "64", "MICA_UPDATE_GRID": "items"},
+                                 {"MICA_UPDATE_GRID": "items"}],
+                         ids=["items_16", "items_64_one_cta_each", "one_cta_each"])
+def test_item_size_and_grid_overrides(env):
+    """The tuning overrides change how a list is cut into work items (MICA_ITEM_OCTS: octets per slice, and with it
+    which tensors are packed) and how the update grid takes them (MICA_UPDATE_GRID=items: one CTA per item instead
+    of the persistent queue); every element still matches the oracle, for AdamW (float32, packed BF16, binary16
+    gradients) and SGD with momentum."""
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = ("import sys; sys.path[:0] = [%r, %r]; import parity, workloads\n"
+            "R = %r\n"
+            "for name in ('gpt2_small', 'gpt2_small_bf16', 'fp16_scaled'):\n"
+            "    parity.run_parity(workloads.WORKLOADS[name], sizes=R + R[::-1], steps=3)\n"
+            "parity.run_parity_sgd(workloads.WORKLOADS['gpt2_small'], 0.9, sizes=R, steps=3)\n"
+            "print('ok')\n" % (root, os.path.join(root, "tests"), RAGGED))
+    out = subprocess.run([sys.executable, "-c", code], env=dict(os.environ, **env), capture_output=True, text=True,
+                         timeout=600)
+    assert out.returncode == 0 and "ok" in out.stdout, out.stderr[-2000:]
