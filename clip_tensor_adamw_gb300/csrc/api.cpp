@@ -507,7 +507,7 @@ static mica_status build_plan(const ListDesc& L, int device, uint64_t h, Plan** 
         prefix[0] = 0;
         for (int32_t k = 0; k < L.T; ++k) prefix[k + 1] = prefix[k] + (L.n[k] + kOct - 1) / kOct;
         int32_t grid = 1, direct = 0;
-        choose_norm_shape(total_octs, nonempty, sms, INT32_MAX, &grid, &direct);
+        choose_norm_shape(total_octs, nonempty, L.gdt == kF16 ? 16 : 32, sms, INT32_MAX, &grid, &direct);
         plan->chunks.direct = direct;
         first.resize((size_t)grid);
         for (int32_t b = 0; b < grid; ++b) {

@@ -135,7 +135,7 @@ extern "C" mica_status mica_clip_grad_norms_noalloc(const void* const* g, const 
     int64_t nonempty = 0;
     for (int32_t k = 0; k < T; ++k) nonempty += n[k] > 0;
     int32_t grid = 1, direct = 0;
-    choose_norm_shape(total_octs, nonempty, sms, kNoallocMaxGrid, &grid, &direct);
+    choose_norm_shape(total_octs, nonempty, gdt == MICA_F16 ? 16 : 32, sms, kNoallocMaxGrid, &grid, &direct);
     for (int32_t b = 0; b < grid; ++b) {
         const int64_t c0 = total_octs * b / grid;
         int32_t lo = 0, hi = T;  // the last tensor whose octets start at or before c0
