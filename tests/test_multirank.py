@@ -74,3 +74,23 @@ def test_hbm_peak_from_measured_peaks_file(tmp_path):
         else:
             assert src == "measured" and abs(v - want) < 1e-6, (record, v)
     assert bench.hbm_peak(str(tmp_path / "missing.json"))[1] == "fallback"
+
+
+def test_profiled_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
+    """The roofline's DRAM traffic comes from the committed ncu summary only while that summary names the current
+    AdamW kernel source by its hash; any other hash, a missing figure or a missing file gives null."""
+    import bench
+    monkeypatch.chdir(ROOT)
+    sha = bench.kernel_source_sha()
+    assert len(sha) == 16 and int(sha, 16) >= 0 and sha == bench.kernel_source_sha()
+    p = tmp_path / "profile.md"
+    monkeypatch.setattr(bench, "PROFILE", str(p))
+    p.write_text(f"kernel_source_sha256_16: {sha}\n\ndram_bytes_per_launch_full_size: 3.4577e+09\n")
+    assert bench.profiled_traffic() == 3.4577e9
+    other = ("0" if sha[0] != "0" else "1") + sha[1:]
+    p.write_text(f"kernel_source_sha256_16: {other}\n\ndram_bytes_per_launch_full_size: 3.4577e+09\n")
+    assert bench.profiled_traffic() is None
+    p.write_text(f"kernel_source_sha256_16: {sha}\n")
+    assert bench.profiled_traffic() is None
+    monkeypatch.setattr(bench, "PROFILE", str(tmp_path / "missing.md"))
+    assert bench.profiled_traffic() is None
