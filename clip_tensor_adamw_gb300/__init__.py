@@ -6,8 +6,8 @@ package is its Python binding. Build the library with ``python -m clip_tensor_ad
 """
 from .mica import (GroupIndex, MicaError, TensorList, lib, mica_adamw_steps, mica_adamw_steps_grouped,
                    mica_clip_grad_norms, mica_launch_count, mica_release_cache, mica_scale_tensors,
-                   mica_selftest_wait_timeout, mica_sgd_steps, mica_sync)
+                   mica_selftest_wait_timeout, mica_sgd_steps, mica_sync, mica_work_items)
 
 __all__ = ["GroupIndex", "MicaError", "TensorList", "lib", "mica_adamw_steps", "mica_adamw_steps_grouped",
            "mica_clip_grad_norms", "mica_launch_count", "mica_release_cache", "mica_scale_tensors",
-           "mica_selftest_wait_timeout", "mica_sgd_steps", "mica_sync"]
+           "mica_selftest_wait_timeout", "mica_sgd_steps", "mica_sync", "mica_work_items"]

@@ -948,4 +948,43 @@ extern "C" const char* mica_last_error_detail(void) { return t_detail.c_str(); }
 
 extern "C" uint64_t mica_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
-extern "C" int32_t mica_abi_version(void) { return 2; }
+extern "C" mica_status mica_work_items(const int64_t* n, const int32_t* vec, int32_t T, int32_t item_octs,
+                                       int32_t sms, int64_t* items, int32_t max_items, int32_t* pack,
+                                       int32_t max_pack, int32_t* num_items, int32_t* pack_len,
+                                       int32_t* used_item_octs) {
+    if (!num_items || !pack_len) return fail(MICA_ERR_NULL, "num_items and pack_len must not be NULL");
+    if (T < 0 || T > MICA_MAX_TENSORS) return fail(MICA_ERR_COUNT, "T = %d is outside [0, %d]", T, MICA_MAX_TENSORS);
+    if (T > 0 && (!n || !vec)) return fail(MICA_ERR_NULL, "n and vec must not be NULL");
+    if (max_items < 0 || max_pack < 0) return fail(MICA_ERR_COUNT, "a capacity is negative");
+    if ((max_items > 0 && !items) || (max_pack > 0 && !pack))
+        return fail(MICA_ERR_NULL, "an output array is NULL but its capacity is not 0");
+    if (sms < 1) return fail(MICA_ERR_COUNT, "sms = %d is not >= 1", sms);
+    if (item_octs != 0 && (item_octs < 16 || item_octs > (1 << 20) || (item_octs & (item_octs - 1)) != 0))
+        return fail(MICA_ERR_COUNT, "item_octs = %d is not 0 or a power of two in [16, 2^20]", item_octs);
+    std::vector<TensorRec> recs((size_t)T);
+    int64_t total_octs = 0;
+    for (int32_t k = 0; k < T; ++k) {
+        if (n[k] < 0 || n[k] > ((int64_t)1 << 40))
+            return fail(MICA_ERR_COUNT, "n[%d] = %lld is outside [0, 2^40]", k, (long long)n[k]);
+        recs[(size_t)k] = TensorRec{nullptr, nullptr, nullptr, nullptr, n[k], vec[k] ? 1 : 0, 0};
+        total_octs += (n[k] + kOct - 1) / kOct;
+    }
+    const int32_t io = item_octs ? item_octs : choose_item_octs(total_octs, sms, base_item_octs(kAdamW, kF32));
+    std::vector<int32_t> pre;
+    std::vector<WorkItem> list = build_items(n, recs.data(), T, io, &pre);
+    order_items(list);
+    if (list.size() > (size_t)INT32_MAX || pre.size() > (size_t)INT32_MAX)
+        return fail(MICA_ERR_COUNT, "too many work items (%zu)", list.size());
+    *num_items = (int32_t)list.size();
+    *pack_len = (int32_t)pre.size();
+    if (used_item_octs) *used_item_octs = io;
+    for (size_t i = 0; i < list.size() && i < (size_t)max_items; ++i) {
+        items[3 * i] = list[i].t;
+        items[3 * i + 1] = list[i].count;
+        items[3 * i + 2] = list[i].o0;
+    }
+    for (size_t i = 0; i < pre.size() && i < (size_t)max_pack; ++i) pack[i] = pre[i];
+    return ok();
+}
+
+extern "C" int32_t mica_abi_version(void) { return 3; }

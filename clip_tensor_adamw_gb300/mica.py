@@ -81,6 +81,10 @@ def lib() -> ctypes.CDLL:
         L.mica_launch_count.restype = ctypes.c_uint64
         L.mica_abi_version.argtypes = []
         L.mica_abi_version.restype = ctypes.c_int32
+        _I32P = ctypes.POINTER(ctypes.c_int32)
+        L.mica_work_items.argtypes = [_I64P, _I32P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _I64P,
+                                      ctypes.c_int32, _I32P, ctypes.c_int32, _I32P, _I32P, _I32P]
+        L.mica_work_items.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -241,6 +245,24 @@ def mica_sgd_steps(w, g, buf=None, *, lr: float, momentum: float = 0.0, zero_gra
     hp = _SgdHP(float(lr), float(momentum), int(bool(zero_grad)), MICA_STEP_SKIP_NONFINITE if skip_nonfinite else 0)
     _check(lib().mica_sgd_steps(W.ptrs, G.ptrs, None if B is None else B.ptrs, W.n, W.T, gdt, ctypes.byref(hp),
                                 _ptr(factor), _stream(stream)))
+
+
+def mica_work_items(sizes: Sequence[int], vec: Sequence[bool] | None = None, item_octs: int = 0, sms: int = 152):
+    """The work items an update call cuts a list of ``sizes`` into (no device used): ``(items, pack, item_octs)``
+    with items a list of (first tensor, tensor count, o0) in array order (the kernels take them from the end),
+    pack the pack table, and the octets per slice used. ``vec``: which tensors take the vector path (default all)."""
+    T = len(sizes)
+    n = (ctypes.c_int64 * max(T, 1))(*[int(x) for x in sizes])
+    v = (ctypes.c_int32 * max(T, 1))(*[1 if x else 0 for x in (vec if vec is not None else [True] * T)])
+    num, plen, used = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().mica_work_items(n, v, T, int(item_octs), int(sms), None, 0, None, 0, ctypes.byref(num),
+                                 ctypes.byref(plen), ctypes.byref(used)))
+    items = (ctypes.c_int64 * max(3 * num.value, 1))()
+    pack = (ctypes.c_int32 * max(plen.value, 1))()
+    _check(lib().mica_work_items(n, v, T, int(item_octs), int(sms), items, num.value, pack, plen.value,
+                                 ctypes.byref(num), ctypes.byref(plen), ctypes.byref(used)))
+    out = [(items[3 * i], items[3 * i + 1], items[3 * i + 2]) for i in range(num.value)]
+    return out, list(pack[:plen.value]), used.value
 
 
 def mica_sync(stream=None) -> None:

@@ -245,7 +245,26 @@ MICA_API const char* mica_last_error_detail(void);
 /* How many kernels this library has queued since it was loaded, over all threads. */
 MICA_API uint64_t mica_launch_count(void);
 
-/* The ABI version of this header: 2 (1 had neither mica_adamw_steps_grouped nor mica_sgd_steps). */
+/* The work items an update call (AdamWSteps, SGD) cuts a list into, for inspection and tests; no device is used and
+ * nothing is cached. The list is n[T] (element counts) and vec[T] (nonzero where a tensor's buffers are aligned for
+ * the vector path: 32 bytes for float32 streams, 16 for binary16 and packed ones). item_octs is the octets (8
+ * elements) per slice of a large tensor, a power of two from 16 to 2^20, or 0 for what an AdamW call with float32
+ * moments chooses on a GPU of `sms` SMs (`*used_item_octs` gets the value used; it may be NULL).
+ * Output, in array order (the kernels take the items from the end of the array): item i as three int64 values in
+ * items[3i .. 3i+2]: its first tensor t, its tensor count c, and o0. A slice has c == 1; it covers octets
+ * [o0, min(o0 + item_octs, ceil(n[t]/8))) of tensor t. A pack has c > 1; it covers tensors t .. t+c-1 whole, and its
+ * row of the pack table starts at pack[o0]: c + 1 running counts of the tensors' whole octets (those of vec
+ * tensors' first floor(n/8) octets), then c + 1 running counts of their other octets. Up to max_items items and
+ * max_pack table entries are written; *num_items and *pack_len get the full counts either way.
+ * Errors: MICA_ERR_NULL (num_items, pack_len, n or vec NULL where needed, or an output NULL with a nonzero
+ * capacity), MICA_ERR_COUNT (T, an n[i], item_octs, sms or a capacity out of range). This is a description of this
+ * library's own scheduling, with no counterpart in the method's pages. */
+MICA_API mica_status mica_work_items(const int64_t* n, const int32_t* vec, int32_t T, int32_t item_octs, int32_t sms,
+                                     int64_t* items, int32_t max_items, int32_t* pack, int32_t max_pack,
+                                     int32_t* num_items, int32_t* pack_len, int32_t* used_item_octs);
+
+/* The ABI version of this header: 3 (2 had no mica_work_items; 1 had neither mica_adamw_steps_grouped nor
+ * mica_sgd_steps). */
 MICA_API int32_t mica_abi_version(void);
 
 #ifdef __cplusplus

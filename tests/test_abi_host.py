@@ -29,7 +29,7 @@ def test_exports_every_declared_symbol():
     assert len(names) >= 9
     for name in names:
         assert hasattr(L, name), name
-    assert L.mica_abi_version() == 2
+    assert L.mica_abi_version() == 3
 
 
 def test_status_strings():
