@@ -676,10 +676,39 @@ def pin_printed_beta_rounding(o: oracle.Oracle) -> None:
     assert s["c2"] == np.float32(0.001)
 
 
+def pin_adamw_op_order(o: oracle.Oracle) -> None:
+    """Single elements worked out by hand in the pages' order, one float32 operation per line
+    (``tests/golden/adamw_op_order.txt``, each line re-derived exactly by ``golden_steps``): the oracle must end on
+    the derivations' bits for w, m and v. Each element is one where a plausible other order (the weighted-sum
+    moment, c2 (gh gh), (-step) (m / denom), bc2 inside the root, eps before the division, the decay after the
+    update, or step, bc2 or dec taken in float32) rounds differently, so this pins the order to the bit."""
+    import golden_steps
+    for case in golden_steps.read_cases():
+        x = {k: np.array([b], np.uint32).view(np.float32) for k, b in case.inputs.items()}
+        w, g = x["w"].copy(), x["g"].copy()
+        if case.moments == "bf16x2":
+            assert (case.inputs["m"] & 0xFFFF) == 0 and (case.inputs["v"] & 0xFFFF) == 0, case.name
+            m = np.array([case.inputs["m"] >> 16], np.uint32)
+            v = np.array([case.inputs["v"] >> 16], np.uint32)
+        else:
+            m, v = x["m"].copy(), x["v"].copy()
+        o.adamw_steps([w], [g], [m], [v], Hyper(**case.hp), factor=x["factor"][0])
+        want = {k: case.bits[name] for k, name in case.output.items()}
+        assert int(w.view(np.uint32)[0]) == want["w"], (case.name, "w", hex(int(w.view(np.uint32)[0])))
+        if case.moments == "bf16x2":
+            got_m, got_v = int(m[0]) & 0xFFFF, int(v[0]) & 0xFFFF
+            assert got_m == want["m"] >> 16 and got_v == want["v"] >> 16, (case.name, hex(got_m), hex(got_v))
+            assert (int(m[0]) >> 16) == 0 and (int(v[0]) >> 16) == 0, case.name  # n = 1: the high half untouched
+        else:
+            assert int(m.view(np.uint32)[0]) == want["m"], (case.name, "m")
+            assert int(v.view(np.uint32)[0]) == want["v"], (case.name, "v")
+
+
 ALL_PINS = [
     pin_bf16_rounding, pin_bf16_printed, pin_f16, pin_norm_fsum, pin_norm_closed_forms, pin_clip_factor,
     pin_torch_adamw, pin_torch_adam_l2, pin_first_step_closed_form, pin_constant_gradient,
     pin_packed_reads_rounded_moments, pin_odd_tail_untouched, pin_zero_grad, pin_list_equals_groups,
     pin_scale_tensors, pin_printed_beta_rounding, pin_packed_m_float_v, pin_skip_nonfinite_vs_gradscaler,
     pin_torch_adamw_param_groups, pin_torch_sgd, pin_sgd_dyadic_closed_form, pin_sgd_skip_vs_gradscaler,
+    pin_adamw_op_order,
 ]

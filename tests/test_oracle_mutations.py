@@ -58,6 +58,22 @@ MUTATIONS = {
     "sgd_ignores_factor": ("float gh = grad_at(g, gdt, i) * factor;\n        if (buf) {",
                            "float gh = grad_at(g, gdt, i);\n        if (buf) {"),
     "sgd_skip_ignored": ("const int skipped = (flags & 1u) && !(factor > 0.0f);", "const int skipped = 0;"),
+    # orders of the per-element arithmetic and of the scalars that a reader could take for the page's
+    "lerp_as_weighted_sum": ("float m_new = mi + s->c1 * (gh - mi);",
+                             "float m_new = (1.0f - s->c1) * mi + s->c1 * gh;"),
+    "v_groups_gh_squared": ("float v_new = vi * s->b2 + (s->c2 * gh) * gh;",
+                            "float v_new = vi * s->b2 + s->c2 * (gh * gh);"),
+    "w_divides_m_first": ("w[i] = wdec + (neg_step * m_new) / denom;", "w[i] = wdec + neg_step * (m_new / denom);"),
+    "bc2_inside_sqrt": ("float denom = sqrtf(v_new) / s->bc2 + s->eps;",
+                        "float denom = sqrtf(v_new / (s->bc2 * s->bc2)) + s->eps;"),
+    "eps_before_bc2": ("float denom = sqrtf(v_new) / s->bc2 + s->eps;",
+                       "float denom = (sqrtf(v_new) + s->eps) / s->bc2;"),
+    "decay_after_update": ("w[i] = wdec + (neg_step * m_new) / denom;",
+                           "w[i] = (wi + (neg_step * m_new) / denom) * (decoupled ? s->dec : 1.0f);"),
+    "step_in_f32": ("s->step = (float)(lr / (1.0 - pow(b1, tt)));",
+                    "s->step = (float)lr / (float)(1.0 - pow(b1, tt));"),
+    "bc2_in_f32": ("s->bc2 = (float)sqrt(1.0 - pow(b2, tt));", "s->bc2 = sqrtf((float)(1.0 - pow(b2, tt)));"),
+    "decay_in_f32": ("s->dec = (float)(1.0 - lr * wd);", "s->dec = 1.0f - (float)lr * (float)wd;"),
     "odd_tail_clobbered": ("if (i & 1) return (word & 0x0000FFFFu) | ((uint32_t)h << 16);\n    return (word & 0xFFFF0000u) | (uint32_t)h;",
                            "if (i & 1) return (word & 0x0000FFFFu) | ((uint32_t)h << 16);\n    return (uint32_t)h;"),
 }
