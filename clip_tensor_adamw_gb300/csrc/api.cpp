@@ -15,6 +15,7 @@
 #include <unordered_map>
 #include <vector>
 
+#include "host.h"
 #include "mica_optim.h"
 #include "plan.h"
 
@@ -100,9 +101,7 @@ static MemGetAddressRange address_range_fn() {
     return fn;
 }
 
-// `p` must be device (or managed) memory of `device`, aligned to `align`, and [p, p + bytes) must lie inside the
-// allocation that holds p when the driver can tell its extent.
-static mica_status check_device_span(const void* p, size_t bytes, size_t align, int device, const char* what,
+mica_status check_device_span(const void* p, size_t bytes, size_t align, int device, const char* what,
                                      int64_t index) {
     if (reinterpret_cast<uintptr_t>(p) % align != 0)
         return fail(MICA_ERR_ADDRESS, "%s[%lld] = %p is not %zu-byte aligned", what, (long long)index, p, align);
@@ -923,6 +922,7 @@ extern "C" mica_status mica_release_cache(void) {
     if (g_plan_count) e = cudaDeviceSynchronize();
     g_plans.clear();
     g_plan_count = 0;
+    noalloc_forget_addresses();
     if (e != cudaSuccess) return cuda_fail(e, "mica_release_cache");
     return ok();
 }
@@ -940,6 +940,7 @@ extern "C" const char* mica_status_string(mica_status s) {
         case MICA_ERR_ADDRESS: return "MICA_ERR_ADDRESS";
         case MICA_ERR_CUDA: return "MICA_ERR_CUDA";
         case MICA_ERR_NOMEM: return "MICA_ERR_NOMEM";
+        case MICA_ERR_CAPTURE: return "MICA_ERR_CAPTURE";
     }
     return "MICA_ERR_UNKNOWN";
 }

@@ -13,6 +13,7 @@
 #include <cstdio>
 #include <mutex>
 
+#include "host.h"
 #include "mica_optim.h"
 #include "plan.h"
 
@@ -27,6 +28,7 @@ constexpr size_t kFirstBytes = (size_t)kNoallocMaxGrid * sizeof(int32_t);
 constexpr size_t kPartialBytes = (size_t)kNoallocMaxGrid * sizeof(double);
 constexpr size_t kTableBytes = kRecBytes + kPrefixBytes + kFirstBytes;  // what each call uploads
 constexpr size_t kScratchBytes = kTableBytes + kPartialBytes + 256;     // + the ticket: 930,304 bytes
+static_assert(kScratchBytes == 930304, "the size the header states");
 
 // The scratch: tensor records | octet prefix | chunk starts | per-CTA partials | ticket. Shared by every call on a
 // device; each call overwrites the tables and the ticket before its kernel runs.
@@ -60,16 +62,13 @@ mica_status scratch_address(int device, unsigned char** out) {
     return MICA_OK;
 }
 
-bool device_pointer(const void* p, int device) {
-    cudaPointerAttributes a{};
-    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
-        cudaGetLastError();
-        return false;
-    }
-    return (a.type == cudaMemoryTypeDevice && a.device == device) || a.type == cudaMemoryTypeManaged;
+}  // namespace
+
+void noalloc_forget_addresses() {
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (int d = 0; d < kMaxDevices; ++d) g_addr[d] = nullptr;
 }
 
-}  // namespace
 }  // namespace mica
 
 using namespace mica;
@@ -100,20 +99,32 @@ extern "C" mica_status mica_clip_grad_norms_noalloc(const void* const* g, const 
     if (reinterpret_cast<uintptr_t>(d_factor) % 4 || (d_norm && reinterpret_cast<uintptr_t>(d_norm) % 4))
         return noalloc_fail(MICA_ERR_ADDRESS, "d_norm or d_factor is misaligned");
 
+    // The tables reach the device by a copy from g_host, which the next call overwrites: a copy recorded into a
+    // CUDA graph would replay whatever list was passed last. So a capturing stream is refused before any other
+    // CUDA call, and the capture is left as it was.
+    cudaStreamCaptureStatus capturing = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &capturing) != cudaSuccess) {
+        cudaGetLastError();
+        return noalloc_fail(MICA_ERR_CUDA, "cudaStreamIsCapturing failed on the stream");
+    }
+    if (capturing != cudaStreamCaptureStatusNone)
+        return noalloc_fail(MICA_ERR_CAPTURE, "the stream is capturing a CUDA graph: this call copies its tables "
+                            "from a host buffer every call reuses, so it is not recorded (nothing was queued)");
+
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();
         return noalloc_fail(MICA_ERR_DEVICE, "no usable CUDA device");
     }
-    if (!device_pointer(d_factor, dev) || (d_norm && !device_pointer(d_norm, dev)))
-        return noalloc_fail(MICA_ERR_ADDRESS, "d_norm or d_factor is not device memory of the current device");
-    for (int32_t k = 0; k < T; ++k)
-        if (n[k] > 0 && !device_pointer(g[k], dev))
-            return noalloc_fail(MICA_ERR_ADDRESS, "a gradient is not device memory of the current device");
+    // every buffer: device memory of this device, and each gradient's n elements inside its allocation
+    mica_status s = check_device_span(d_factor, 4, 4, dev, "d_factor", 0);
+    if (s == MICA_OK && d_norm) s = check_device_span(d_norm, 4, 4, dev, "d_norm", 0);
+    for (int32_t k = 0; s == MICA_OK && k < T; ++k)
+        if (n[k] > 0) s = check_device_span(g[k], (size_t)n[k] * es, es, dev, "g", k);
+    if (s != MICA_OK) return s;
     std::lock_guard<std::mutex> lock(g_mu);
     unsigned char* scratch = nullptr;
-    mica_status s = scratch_address(dev, &scratch);
-    if (s != MICA_OK) return s;
+    if ((s = scratch_address(dev, &scratch)) != MICA_OK) return s;
 
     // The chunk layout the allocating entry point uses: the octet prefix of the list, equal contiguous chunks (as
     // many as the allocating entry point's, capped by this scratch), each chunk's first tensor.
@@ -126,14 +137,14 @@ extern "C" mica_status mica_clip_grad_norms_noalloc(const void* const* g, const 
     int64_t* prefix = reinterpret_cast<int64_t*>(g_host + kRecBytes);
     int32_t* first = reinterpret_cast<int32_t*>(g_host + kRecBytes + kPrefixBytes);
     prefix[0] = 0;
+    int64_t nonempty = 0;
     for (int32_t k = 0; k < T; ++k) {
         const void* gp = n[k] > 0 ? g[k] : nullptr;
         recs[k] = TensorRec{nullptr, const_cast<void*>(gp), nullptr, nullptr, n[k], 0, 0};
         recs[k].vec = (reinterpret_cast<uintptr_t>(gp) % (gdt == MICA_F16 ? 16 : 32)) == 0;
         prefix[k + 1] = prefix[k] + (n[k] + kOct - 1) / kOct;
+        nonempty += n[k] > 0;
     }
-    int64_t nonempty = 0;
-    for (int32_t k = 0; k < T; ++k) nonempty += n[k] > 0;
     int32_t grid = 1, direct = 0;
     choose_norm_shape(total_octs, nonempty, gdt == MICA_F16 ? 16 : 32, sms, kNoallocMaxGrid, &grid, &direct);
     for (int32_t b = 0; b < grid; ++b) {

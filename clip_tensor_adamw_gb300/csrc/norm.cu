@@ -531,13 +531,17 @@ __global__ void __launch_bounds__(kNormThreads, kNormTmaCtasPerSm) norm_tma_kern
                 const int64_t local = o - cc.lo;
                 if (cc.vec && local < cc.full) {
                     const unsigned char* src = stages + (size_t)slot * kStageBytes + (size_t)pos * kOctBytes;
-                    const float4 p0 = *reinterpret_cast<const float4*>(src);
                     if constexpr (G == kF16) {
-                        h8_to(*reinterpret_cast<const uint4*>(&p0), x);
+                        h8_to(*reinterpret_cast<const uint4*>(src), x);
                     } else {
-                        const float4 p1 = *reinterpret_cast<const float4*>(src + 16);
-                        x[0] = p0.x; x[1] = p0.y; x[2] = p0.z; x[3] = p0.w;
-                        x[4] = p1.x; x[5] = p1.y; x[6] = p1.z; x[7] = p1.w;
+                        // the octet's two halves, lanes whose bit 2 is set reading the upper half first: each
+                        // 16-byte read of the warp then covers all 32 banks four times, not half of them eight
+                        const int h = (lane >> 2) & 1;
+                        const float4 p = *reinterpret_cast<const float4*>(src + 16 * h);
+                        const float4 q = *reinterpret_cast<const float4*>(src + 16 * (h ^ 1));
+                        const float4 lo4 = h ? q : p, hi4 = h ? p : q;
+                        x[0] = lo4.x; x[1] = lo4.y; x[2] = lo4.z; x[3] = lo4.w;
+                        x[4] = hi4.x; x[5] = hi4.y; x[6] = hi4.z; x[7] = hi4.w;
                     }
                 } else {  // a tensor's partial last octet, or an unaligned tensor
                     load_elements<G>(cc, local, x);

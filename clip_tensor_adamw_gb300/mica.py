@@ -20,7 +20,8 @@ LIB_PATH = os.environ.get("MICA_LIB") or os.path.join(_PKG, "libmica_optim.so")
 MICA_F32, MICA_F16, MICA_BF16X2, MICA_BF16X2_M = 0, 1, 2, 3
 MICA_STEP_SKIP_NONFINITE, MICA_STEP_COUPLED_L2 = 1, 2
 STATUS = ["MICA_OK", "MICA_ERR_NULL", "MICA_ERR_COUNT", "MICA_ERR_DTYPE", "MICA_ERR_HYPER", "MICA_ERR_BETA",
-          "MICA_ERR_OVERLAP", "MICA_ERR_DEVICE", "MICA_ERR_ADDRESS", "MICA_ERR_CUDA", "MICA_ERR_NOMEM"]
+          "MICA_ERR_OVERLAP", "MICA_ERR_DEVICE", "MICA_ERR_ADDRESS", "MICA_ERR_CUDA", "MICA_ERR_NOMEM",
+          "MICA_ERR_CAPTURE"]
 
 
 class MicaError(RuntimeError):

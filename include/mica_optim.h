@@ -67,7 +67,9 @@ typedef enum {
     MICA_ERR_ADDRESS = 8,  /* a pointer is not device memory of the current device, is not aligned to its element,
                               or its extent runs past the end of its allocation */
     MICA_ERR_CUDA = 9,     /* a CUDA call failed, including a fault of earlier queued work */
-    MICA_ERR_NOMEM = 10    /* the per-list device table could not be allocated */
+    MICA_ERR_NOMEM = 10,   /* the per-list device table could not be allocated */
+    MICA_ERR_CAPTURE = 11  /* the call was refused because `stream` is capturing work into a CUDA graph (only
+                              mica_clip_grad_norms_noalloc refuses this; see there) */
 } mica_status;
 
 /* Element types.
@@ -201,17 +203,26 @@ MICA_API mica_status mica_sgd_steps(float* const* w, void* const* g, float* cons
  * by another allocator, or a loop that cannot afford cudaMalloc's implicit synchronisation. The method's pages have
  * no counterpart to this entry point; it is an addition of this library.
  *
- * Arguments, results and errors are those of mica_clip_grad_norms (same kernel, same arithmetic). The difference is
- * where the scratch lives: instead of a per-list table allocated on first use, every call copies its tables into
- * one fixed device array of this library (930,304 bytes, held by every GPU that loads the library until the
- * process exits) and launches on `stream`. Limits: at most 16,384 tensors (MICA_ERR_COUNT beyond, with a detail
- * naming the limit). The call allocates nothing: no cudaMalloc, no cudaFree, no host heap.
+ * Arguments, results and errors are those of mica_clip_grad_norms (same kernel and arithmetic; the same bits too,
+ * unless a list of more than about 2 GB of gradient asks for more than 1,024 CTAs, which this entry point caps, so
+ * that its partial sums are grouped differently: the norm then agrees to ~1e-13 relative). The difference is where
+ * the scratch lives: instead of a per-list table allocated on first use, every call copies its tables into one
+ * fixed device array of this library (930,304 bytes, held by every GPU that loads the library until the process
+ * exits) and launches on `stream`. The call allocates nothing: no cudaMalloc, no cudaFree, no host heap.
+ *   - Limit: at most 16,384 tensors (MICA_ERR_COUNT beyond, with a detail naming the limit).
+ *   - Every call checks every gradient as a table build of mica_clip_grad_norms does (device memory of the current
+ *     device, n elements inside its allocation, else MICA_ERR_ADDRESS), and uploads its tables: its host cost grows
+ *     linearly with T (two driver queries per tensor and up to 1 MB copied from host memory).
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with that device
- *     current; make that first call before any stream capture.
+ *     current, and keeps it; make that first call before any stream capture. mica_release_cache() forgets the
+ *     address, so that the next call looks it up again: call mica_release_cache() after a cudaDeviceReset before
+ *     using this entry point again.
+ *   - The tables are copied from a host buffer that every call reuses, so a call on a stream that is capturing a
+ *     CUDA graph is refused with MICA_ERR_CAPTURE before anything is queued (the capture is left intact).
  *   - The array is shared by every call and keeps the last call's contents; each call rewrites what it reads, so
  *     calls ordered on one stream are safe, while calls that overlap on the GPU (other streams, other threads'
  *     streams) race on it.
- *   - The table copies come from a static host buffer, so the host side of concurrent calls is serialised.
+ *   - The host side of concurrent calls is serialised (one static staging buffer).
  */
 MICA_API mica_status mica_clip_grad_norms_noalloc(const void* const* g, const int64_t* n, int32_t T, mica_dtype gdt,
                                                   float max_norm, float inv_scale, float* d_norm, float* d_factor,

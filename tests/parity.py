@@ -4,7 +4,8 @@ on the same seeded inputs, and compare them element by element.
 Tolerances (the optimizer-step benchmark's):
 * joint norm: relative 1e-5;
 * weights and float32 moments: |gpu - oracle| <= 1e-6 * |oracle| + 1e-7;
-* packed BF16 moments: bit-exact, or one BF16 ulp apart where the float32 values before rounding differ.
+* packed BF16 moments: bit-exact, or one BF16 ulp apart where the float32 values before rounding differ; with the
+  same factor on both sides, every packed word identical (a NaN moment must carry the pages' code 0xFFFF).
 The kernels are written to be bit-identical to the oracle, so on top of those tolerances every test also requires
 identical bits wherever both sides used the same clip factor (the factor is a float32; the two sides compute it
 from square sums that agree to ~1e-13, so in practice it always has the same bits).
@@ -53,7 +54,9 @@ def bf16_within_one_ulp(a_words: np.ndarray, b_words: np.ndarray, n: int, what: 
 
 
 def exact(a: np.ndarray, b: np.ndarray, what: str) -> None:
-    """Identical bits; two NaNs count as equal whatever their payloads (the CPU and the GPU make different NaNs)."""
+    """Identical bits. For float arrays two NaNs count as equal whatever their payloads (the pages fix no float32
+    NaN code, and the CPU and the GPU make different ones); integer arrays (packed BF16 words) must match bit for
+    bit, NaN codes included."""
     bits = {2: np.uint16, 4: np.uint32}[a.dtype.itemsize]
     au, bu = a.view(bits), b.view(bits)
     neq = au != bu
@@ -108,9 +111,11 @@ def compare_state(st: workloads.State, host, same_factor: bool, tag: str) -> Non
             exact(gg[k], og[k], f"{tag} g[{k}] bits")
         for name, gx, ox, packed in (("m", gm[k], om[k], st.m_packed), ("v", gv[k], ov[k], st.packed)):
             if packed:
-                d = bf16_within_one_ulp(gx, ox, n, f"{tag} {name}[{k}]")
+                bf16_within_one_ulp(gx, ox, n, f"{tag} {name}[{k}]")
                 if same_factor:
-                    assert not d.any(), f"{tag}: packed {name}[{k}] differs with the same factor"
+                    # the same factor: every packed word identical, NaN codes included (a NaN moment is stored as
+                    # the pages' 0xFFFF, not as a canonical NaN)
+                    exact(gx, ox, f"{tag} packed {name}[{k}] words")
             else:
                 f32_close(gx, ox, f"{tag} {name}[{k}]")
                 if same_factor:
