@@ -1,8 +1,9 @@
 #!/usr/bin/env python3
 """Benchmark of the clip + AdamW optimizer step: parameters per second and achieved HBM bandwidth on one GB300.
 
-One step = ClipGradNorms (norm partials + fixed-order finalize) and AdamWSteps over the whole parameter list, both
-through the C ABI (via the Python binding), inputs resident in HBM. Prints one JSON line.
+One step = ClipGradNorms (norm partials + fixed-order finalize) and AdamWSteps over the whole parameter list, through
+the C ABI's one-step entry point mica_clip_adamw_step (via the Python binding), inputs resident in HBM. Prints one
+JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload gpt2_small] [--impl mica|reference]
 
@@ -37,7 +38,8 @@ import workloads  # noqa: E402
 METRIC = "clip+AdamW params/sec and achieved HBM GB/s (% of 8 TB/s roofline), 1 GB300"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SRCS = [os.path.join(ROOT, "clip_tensor_adamw_gb300", "csrc", f) for f in ("adamw.cu", "stream.cuh", "plan.h")]
+KERNEL_SRCS = [os.path.join(ROOT, "clip_tensor_adamw_gb300", "csrc", f)
+               for f in ("adamw.cu", "adam.cuh", "stream.cuh", "plan.h")]
 PROFILE = os.path.join(ROOT, "profiles", "adamw_gpt2_small.md")
 
 
@@ -109,7 +111,7 @@ def hbm_peak(path: str | None = None) -> tuple[float, str]:
 
 
 def kernel_source_sha() -> str:
-    """The first 16 hex digits of the SHA-256 of the AdamW kernel's sources (adamw.cu, stream.cuh, plan.h)."""
+    """The first 16 hex digits of the SHA-256 of the AdamW kernel's sources (adamw.cu, adam.cuh, stream.cuh, plan.h)."""
     h = hashlib.sha256()
     for path in KERNEL_SRCS:
         with open(path, "rb") as f:
@@ -301,9 +303,17 @@ def decay_groups(wl: workloads.Workload):
 
 SGD_LR, SGD_MOMENTUM = 0.1, 0.9
 
+MIN_STEPS_EXTRA, MIN_MS_EXTRA = 200, 50.0
+
+
+def extra_steps(est_ms_per_step: float) -> int:
+    """Timed steps for a secondary workload: at least MIN_STEPS_EXTRA and at least MIN_MS_EXTRA of GPU time, so that
+    short steps are not timed on a region of a few milliseconds."""
+    return max(MIN_STEPS_EXTRA, math.ceil(MIN_MS_EXTRA / max(est_ms_per_step, 1e-4)))
+
 
 def measure(wl: workloads.Workload, steps: int, warmup: int, zero_grad: bool, dist=None, sampler=None,
-            coupled_l2: bool = False, opt: str = "adamw"):
+            coupled_l2: bool = False, opt: str = "adamw", per_kernel: bool = True):
     """Times `steps` steps of the whole hot path on the device (inputs resident): the norm and clip factor, then the
     update (``opt``: "adamw", "adamw_groups", "sgd" or "momentum"). Returns a dict of figures."""
     import clip_tensor_adamw_gb300 as mica
@@ -336,7 +346,14 @@ def measure(wl: workloads.Workload, steps: int, warmup: int, zero_grad: bool, di
         def update(t):
             mica.mica_adamw_steps(W, G, M, V, step=t, **kw)
 
+    step_kw = dict(max_norm=wl.max_norm, inv_scale=wl.inv_scale, lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps,
+                   weight_decay=wl.weight_decay, zero_grad=zero_grad, norm_out=norm, factor_out=factor,
+                   coupled_l2=coupled_l2)
+
     def step(t, ev_mid=None):
+        if ev_mid is None and opt == "adamw":  # the whole step through the one-step entry point
+            mica.mica_clip_adamw_step(W, G, M, V, step=t, **step_kw)
+            return
         mica.mica_clip_grad_norms(G, wl.max_norm, wl.inv_scale, norm_out=norm, factor_out=factor)
         if ev_mid is not None:
             ev_mid.record(stream)
@@ -365,7 +382,7 @@ def measure(wl: workloads.Workload, steps: int, warmup: int, zero_grad: bool, di
         total_ms = slowest_rank_ms(total_ms, dist, "cuda")
     # each kernel's own duration, from events around each launch (a separate loop: events between the two
     # launches of a step keep them from overlapping)
-    k2 = min(steps, 50)
+    k2 = min(steps, 50) if per_kernel else 0
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(k2)]
     for i in range(k2):
@@ -373,11 +390,11 @@ def measure(wl: workloads.Workload, steps: int, warmup: int, zero_grad: bool, di
         step(warmup + steps + 1 + i, ev[i][1])
         ev[i][2].record(stream)
     torch.cuda.synchronize()
-    adamw_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    clip_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    out = {"total_ms": total_ms, "ms_per_step": total_ms / steps, "adamw_ms": statistics.mean(adamw_ms),
-           "clip_ms": statistics.mean(clip_ms), "launches": launches, "t_wall": (t_wall0, t_wall1),
-           "norm": float(norm.item())}
+    adamw_ms = [e[1].elapsed_time(e[2]) for e in ev] or [float("nan")]
+    clip_ms = [e[0].elapsed_time(e[1]) for e in ev] or [float("nan")]
+    out = {"total_ms": total_ms, "ms_per_step": total_ms / steps, "steps": steps,
+           "adamw_ms": statistics.mean(adamw_ms), "clip_ms": statistics.mean(clip_ms), "launches": launches,
+           "t_wall": (t_wall0, t_wall1), "norm": float(norm.item())}
     mica.mica_sync()
     del st
     return out, (W, G, M, V, norm, factor, kw)
@@ -403,7 +420,8 @@ def measure_e2e(wl: workloads.Workload, steps: int, warmup: int):
     V = mica.TensorList(st.v, W.counts)
     norm = torch.empty(1, device="cuda")
     factor = torch.empty(1, device="cuda")
-    kw = dict(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps, weight_decay=wl.weight_decay, factor=factor)
+    kw = dict(max_norm=wl.max_norm, inv_scale=wl.inv_scale, lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps,
+              weight_decay=wl.weight_decay, norm_out=norm, factor_out=factor)
     compute = torch.cuda.current_stream()
     copier = torch.cuda.Stream()
     copied = [torch.cuda.Event(), torch.cuda.Event()]
@@ -418,8 +436,7 @@ def measure_e2e(wl: workloads.Workload, steps: int, warmup: int):
             g_flat[x].copy_(g_host, non_blocking=True)
             copied[x].record(copier)
         compute.wait_event(copied[x])
-        mica.mica_clip_grad_norms(g_lists[x], wl.max_norm, wl.inv_scale, norm_out=norm, factor_out=factor)
-        mica.mica_adamw_steps(W, g_lists[x], M, V, step=t, **kw)
+        mica.mica_clip_adamw_step(W, g_lists[x], M, V, step=t, **kw)
         released[x].record(compute)
         norm_host[x:x + 1].copy_(norm, non_blocking=True)
 
@@ -503,35 +520,59 @@ def main():
     e2e = None
     cpu = None
     if not args.no_extras and rank == 0:
-        zg, _ = measure(wl, max(20, args.steps // 4), args.warmup, zero_grad=True)
-        extras["zero_grad"] = {"ms_per_step": zg["ms_per_step"],
+        zg, _ = measure(wl, extra_steps(main_fig["ms_per_step"]), args.warmup, zero_grad=True)
+        extras["zero_grad"] = {"ms_per_step": zg["ms_per_step"], "steps": zg["steps"],
                                "hbm_gbs_model": P * step_bytes_per_param(wl) / (zg["ms_per_step"] / 1e3) / 1e9,
                                "hbm_gbs_actual": P * step_bytes_per_param(wl, True) / (zg["ms_per_step"] / 1e3) / 1e9,
                                "bytes_per_param_actual": step_bytes_per_param(wl, True)}
         small = workloads.WORKLOADS["gpt2_small"]
-        others = [(n, workloads.WORKLOADS[n], False, "adamw")
+        others = [(n, workloads.WORKLOADS[n], False, "adamw", None)
                   for n in ("gpt2_small_bf16", "gpt2_xl", "fp16_scaled", "tiny")]
-        others += [("gpt2_small_bf16_m", dataclasses.replace(small, name="gpt2_small_bf16_m", moments="bf16x2_m"),
-                    False, "adamw"),
-                   ("gpt2_small_adam_l2", small, True, "adamw"),
-                   ("gpt2_small_param_groups", small, False, "adamw_groups"),
-                   ("gpt2_small_sgd", small, False, "sgd"),
-                   ("gpt2_small_sgd_momentum", small, False, "momentum")]
-        for other, owl, coupled, opt in others:
+        others += [("fp16_scaled_cooperative", workloads.WORKLOADS["fp16_scaled"], False, "adamw", "1"),
+                   ("gpt2_small_bf16_m", dataclasses.replace(small, name="gpt2_small_bf16_m", moments="bf16x2_m"),
+                    False, "adamw", None),
+                   ("gpt2_small_adam_l2", small, True, "adamw", None),
+                   ("gpt2_small_param_groups", small, False, "adamw_groups", None),
+                   ("gpt2_small_sgd", small, False, "sgd", None),
+                   ("gpt2_small_sgd_momentum", small, False, "momentum", None)]
+        for other, owl, coupled, opt, fused in others:
             if other == wl.name:
                 continue
-            k = 40 if other == "gpt2_xl" else max(20, args.steps // 4)
-            f, _ = measure(owl, k, args.warmup, zero_grad=False, coupled_l2=coupled, opt=opt)
+            if fused is not None:
+                os.environ["MICA_FUSED"] = fused
+            est, _ = measure(owl, 10, args.warmup, zero_grad=False, coupled_l2=coupled, opt=opt, per_kernel=False)
+            f, _ = measure(owl, extra_steps(est["ms_per_step"]), args.warmup, zero_grad=False, coupled_l2=coupled,
+                           opt=opt)
+            os.environ.pop("MICA_FUSED", None)
             torch.cuda.empty_cache()
             bpp = step_bytes_per_param(owl, opt=opt)
-            extras[other] = {"params": owl.params, "ms_per_step": f["ms_per_step"],
+            ubpp = adamw_bytes_per_param(owl, opt=opt)
+            extras[other] = {"params": owl.params, "steps": f["steps"], "ms_per_step": f["ms_per_step"],
                              "params_per_s": owl.params / (f["ms_per_step"] / 1e3),
                              "hbm_gbs": owl.params * bpp / (f["ms_per_step"] / 1e3) / 1e9,
                              "pct_of_8tbs": 100 * owl.params * bpp / (f["ms_per_step"] / 1e3) / 1e9 / NOMINAL_HBM_GBS,
                              "update_ms": f["adamw_ms"], "clip_ms": f["clip_ms"], "bytes_per_param": bpp,
-                             "update_gbs": owl.params * adamw_bytes_per_param(owl, opt=opt) / (f["adamw_ms"] / 1e3)
-                             / 1e9}
-        ms, h2d, d2h = measure_e2e(wl, max(20, args.steps // 4), args.warmup)
+                             "update_gbs": owl.params * ubpp / (f["adamw_ms"] / 1e3) / 1e9,
+                             "roofline": {"bound": "hbm", "kernel": "sgd_kernel" if opt in ("sgd", "momentum")
+                                          else "adamw_kernel", "achieved": owl.params * ubpp / f["adamw_ms"] / 1e6,
+                                          "peak": peak, "unit": "GB/s",
+                                          "frac": owl.params * ubpp / f["adamw_ms"] / 1e6 / peak,
+                                          "peak_source": peak_src, "bytes_per_param": ubpp,
+                                          "launch_ms": f["adamw_ms"]}}
+            if fused is not None:
+                extras[other]["path"] = "one cooperative launch (MICA_FUSED=1)"
+            if other == "gpt2_xl":
+                ms, h2d, d2h = measure_e2e(owl, 10, args.warmup)
+                extras[other]["e2e"] = {"value": owl.params / (ms / 1e3), "unit": "params/s", "ms_per_step": ms,
+                                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+                params, ntens, times = time_oracle(owl, target_params=owl.params // 8, min_seconds=5.0, max_steps=5)
+                extras[other]["cpu_baseline"] = {
+                    "value": params * len(times) / sum(times), "unit": "params/s", "cores": 1, "kind": "oracle",
+                    "host": host_cpu(),
+                    "sample": f"{len(times)} steps of the first {ntens} of {len(owl.sizes)} tensors ({params:,} of "
+                              f"{owl.params:,} params) of {owl.name}, single-threaded C oracle"}
+                torch.cuda.empty_cache()
+        ms, h2d, d2h = measure_e2e(wl, extra_steps(main_fig["ms_per_step"]), args.warmup)
         e2e = {"value": P / (ms / 1e3), "unit": "params/s", "ms_per_step": ms, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h}
         params, ntens, times = time_oracle(wl, target_params=wl.params, min_seconds=10.0, max_steps=20)

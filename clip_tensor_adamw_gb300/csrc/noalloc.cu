@@ -87,7 +87,7 @@ extern "C" mica_status mica_clip_grad_norms_noalloc(const void* const* g, const 
         return noalloc_fail(MICA_ERR_COUNT, "more than 16384 tensors: beyond this entry point's scratch");
     if (T > 0 && (!g || !n)) return noalloc_fail(MICA_ERR_NULL, "a pointer array is NULL");
     const size_t es = (gdt == MICA_F16) ? 2 : 4;
-    int64_t total_octs = 0;
+    int64_t total_octs = 0, total = 0;
     for (int32_t k = 0; k < T; ++k) {
         if (n[k] < 0 || n[k] > ((int64_t)1 << 40))
             return noalloc_fail(MICA_ERR_COUNT, "an element count is out of range");
@@ -95,6 +95,7 @@ extern "C" mica_status mica_clip_grad_norms_noalloc(const void* const* g, const 
         if (!g[k]) return noalloc_fail(MICA_ERR_NULL, "a gradient with n > 0 is NULL");
         if (reinterpret_cast<uintptr_t>(g[k]) % es) return noalloc_fail(MICA_ERR_ADDRESS, "a gradient is misaligned");
         total_octs += (n[k] + kOct - 1) / kOct;
+        total += n[k];
     }
     if (reinterpret_cast<uintptr_t>(d_factor) % 4 || (d_norm && reinterpret_cast<uintptr_t>(d_norm) % 4))
         return noalloc_fail(MICA_ERR_ADDRESS, "d_norm or d_factor is misaligned");
@@ -182,7 +183,9 @@ extern "C" mica_status mica_clip_grad_norms_noalloc(const void* const* g, const 
         cudaGetLastError();
         return noalloc_fail(MICA_ERR_CUDA, "uploading the tables into the scratch failed");
     }
-    const int err = launch_norm(ct, (Dtype)gdt, inv_scale, d_part, d_ticket, max_norm, d_norm, d_factor, stream);
+    const bool keep_l2 = total * (int64_t)es <= kKeepL2MaxGradBytes;  // as the allocating entry point chooses
+    const int err = launch_norm(ct, (Dtype)gdt, inv_scale, d_part, d_ticket, max_norm, d_norm, d_factor, keep_l2,
+                                stream);
     if (err != (int)cudaSuccess) return noalloc_fail(MICA_ERR_CUDA, "the norm kernel failed to launch");
     return MICA_OK;
 }

@@ -151,17 +151,40 @@ int launch_sgd(const UpdateLaunch& u, Dtype gdt, bool momentum, bool skip, const
 // The joint norm in one launch of ct.grid CTAs: one partial square sum per CTA into `partials` (ct.grid doubles),
 // and the CTA that finishes last sums them in a fixed order and writes norm and factor. `ticket` must be 0 before
 // the launch; the kernel leaves it 0.
+// keep_l2: the gradient's loads (and bulk copies) carry an evict-last L2 policy, so that the update that follows
+// reads the gradient from L2 (for gradients that fit in it, see kKeepL2MaxGradBytes).
 int launch_norm(const ChunkTable& ct, Dtype gdt, float inv_scale, double* partials, unsigned int* ticket,
-                float max_norm, float* d_norm, float* d_factor, void* stream);
+                float max_norm, float* d_norm, float* d_factor, bool keep_l2, void* stream);
+// Gradient bytes up to which the norm asks L2 to keep the gradient for the update (GB300 has 126 MB of L2; the
+// update's own streams pass through it with evict-first hints). Larger gradients would only push the update's
+// other streams out.
+constexpr int64_t kKeepL2MaxGradBytes = (int64_t)96 << 20;
 int launch_scale(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_octs, Dtype dt,
                  float factor, const float* d_factor, void* stream);
 
+// The norm and the AdamW update in one cooperative launch of ct.grid CTAs (fused.cu): CTA b sums the squares of
+// chunk b of ct (the register-streaming layout, ct.first holding ct.grid entries) into partials[b]; the CTAs meet
+// at a bounded grid-wide wait on `bar` (two words, zero before the first launch, left ready by each); every CTA then
+// computes norm and factor from the partials in a fixed order (CTA 0 writes them to d_norm, when not null, and
+// d_factor), and the grid runs the update's items from u's queue (not null) with that factor. Returns
+// cudaErrorCooperativeLaunchTooLarge, having queued nothing, when ct.grid CTAs of the instantiation cannot all be
+// resident at once.
+int launch_clip_adamw(const ChunkTable& ct, double* partials, unsigned int* bar, const UpdateLaunch& u, Dtype gdt,
+                      Dtype mdt, bool coupled, const StepScalars& s, float max_norm, float inv_scale, float* d_norm,
+                      float* d_factor, void* stream);
+constexpr int kFusedCtasPerSm = 3;
+
 // One CTA whose bounded mbarrier wait runs out after `polls` rounds (nothing arrives) and sets the status word.
 int launch_wait_selftest(uint32_t polls, void* stream);
+// One CTA whose grid-wide wait for a second CTA (never launched) runs out after `polls` polls and sets the fused
+// kernels' status word.
+int launch_grid_wait_selftest(uint32_t polls, void* stream);
 
 // The device's pipeline status word: nonzero when a kernel's bounded wait on a shared-memory barrier gave up (the
 // kernel then stopped early and its results are not valid). Reads it (synchronously) and clears it.
 int read_device_status(unsigned int* status);
+// The same for the fused kernels' grid-wide waits.
+int read_fused_status(unsigned int* status);
 
 // kernels queued so far (incremented by the launchers)
 void count_launches(uint64_t k);

@@ -67,11 +67,14 @@ def lib() -> ctypes.CDLL:
                                                ctypes.c_int32, _P, ctypes.POINTER(_HP), ctypes.c_int32, _P, _P]
         L.mica_sgd_steps.argtypes = [_P, _P, _P, _I64P, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(_SgdHP),
                                      _P, _P]
+        L.mica_clip_adamw_step.argtypes = [_P, _P, _P, _P, _I64P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                           ctypes.POINTER(_HP), ctypes.c_float, ctypes.c_float, _P, _P, _P]
         for f in ("mica_scale_tensors", "mica_clip_grad_norms", "mica_adamw_steps", "mica_adamw_steps_grouped",
-                  "mica_sgd_steps", "mica_sync", "mica_release_cache"):
+                  "mica_sgd_steps", "mica_clip_adamw_step", "mica_sync", "mica_release_cache"):
             getattr(L, f).restype = ctypes.c_int
-        L.mica_selftest_wait_timeout.argtypes = [ctypes.c_uint32, _P]
-        L.mica_selftest_wait_timeout.restype = ctypes.c_int
+        for f in ("mica_selftest_wait_timeout", "mica_selftest_grid_wait_timeout"):
+            getattr(L, f).argtypes = [ctypes.c_uint32, _P]
+            getattr(L, f).restype = ctypes.c_int
         L.mica_sync.argtypes = [_P]
         L.mica_release_cache.argtypes = []
         L.mica_status_string.argtypes = [ctypes.c_int]
@@ -197,6 +200,37 @@ def mica_adamw_steps(w, g, m, v, *, lr: float, beta1: float, beta2: float, eps: 
                                   _stream(stream)))
 
 
+def mica_clip_adamw_step(w, g, m, v, *, max_norm: float, inv_scale: float = 1.0, lr: float, beta1: float,
+                         beta2: float, eps: float, weight_decay: float, step: int, zero_grad: bool = False,
+                         norm_out: torch.Tensor | None = None, factor_out: torch.Tensor | None = None, stream=None,
+                         skip_nonfinite: bool = False, coupled_l2: bool = False):
+    """One whole step: ClipGradNorms then AdamWSteps on the same list (one cooperative launch when the gradient
+    fits in L2). Arguments as mica_clip_grad_norms and mica_adamw_steps; returns the device (norm, factor)."""
+    W = _as_list(w)
+    sizes = W.counts
+    G = _as_list(g)
+    M = _as_list(m, sizes)
+    V = _as_list(v, sizes)
+    if not (W.T == G.T == M.T == V.T):
+        raise ValueError("w, g, m and v must list the same number of tensors")
+    dev = G.tensors[0].device if G.T else torch.device("cuda", torch.cuda.current_device())
+    if norm_out is None:
+        norm_out = torch.empty(1, dtype=torch.float32, device=dev)
+    if factor_out is None:
+        factor_out = torch.empty(1, dtype=torch.float32, device=dev)
+    gdt = _dtype_code(G.tensors[0] if G.T else None, "g")
+    mdt = _dtype_code(M.tensors[0] if M.T else None, "m")
+    if mdt == MICA_BF16X2 and V.T and _dtype_code(V.tensors[0], "v") == MICA_F32:
+        mdt = MICA_BF16X2_M
+    flags = (MICA_STEP_SKIP_NONFINITE if skip_nonfinite else 0) | (MICA_STEP_COUPLED_L2 if coupled_l2 else 0)
+    hp = _HP(float(lr), float(beta1), float(beta2), float(eps), float(weight_decay), int(step), int(bool(zero_grad)),
+             flags)
+    _check(lib().mica_clip_adamw_step(W.ptrs, G.ptrs, M.ptrs, V.ptrs, W.n, W.T, gdt, mdt, ctypes.byref(hp),
+                                      float(max_norm), float(inv_scale), _ptr(norm_out), _ptr(factor_out),
+                                      _stream(stream)))
+    return norm_out, factor_out
+
+
 class GroupIndex:
     """The per-tensor group indices of mica_adamw_steps_grouped as a host int32 array, built once and reusable."""
 
@@ -273,6 +307,11 @@ def mica_sync(stream=None) -> None:
 def mica_selftest_wait_timeout(polls: int = 16, stream=None) -> None:
     """Queues the self-test kernel whose bounded wait runs out; the next mica_sync raises MicaError (MICA_ERR_CUDA)."""
     _check(lib().mica_selftest_wait_timeout(int(polls), _stream(stream)))
+
+
+def mica_selftest_grid_wait_timeout(polls: int = 16, stream=None) -> None:
+    """Queues the self-test kernel whose grid-wide wait runs out; the next mica_sync raises MicaError."""
+    _check(lib().mica_selftest_grid_wait_timeout(int(polls), _stream(stream)))
 
 
 def mica_release_cache() -> None:

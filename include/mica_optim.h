@@ -172,6 +172,33 @@ MICA_API mica_status mica_adamw_steps_grouped(float* const* w, void* const* g, v
                                               const int32_t* group, const mica_adamw_hp* hp, int32_t num_groups,
                                               const float* d_factor, void* stream);
 
+/*
+ * One whole step of the hot path: ClipGradNorms followed by AdamWSteps on the same list, with the results of
+ *   mica_clip_grad_norms(g, n, T, gdt, max_norm, inv_scale, d_norm, d_factor, stream);
+ *   mica_adamw_steps(w, g, m, v, n, T, gdt, mdt, hp, d_factor, stream);
+ * (the same arguments, checks and errors as those two calls, and the same results: the update bit for bit given
+ * the factor; the norm within its rounding, see below). Source: "Mica 7.7 ...", sections "The whole model in one
+ * call" (ClipGradNorms then AdamWSteps) and "Values that stay on the card" (the norm measured, decided and applied on
+ * the card, never copied to the host).
+ *
+ * By default the two run as those two launches, the update a programmatic dependent of the norm; for a gradient
+ * of at most 96 MB the norm's loads ask L2 to keep the gradient (an evict-last policy), so that the update reads it
+ * from L2 rather than HBM (mica_clip_grad_norms does the same). With MICA_FUSED=1 (read at each call) they run as
+ * ONE cooperative launch instead: each CTA sums its chunk of the gradient, keeping the lines in L2, the CTAs meet at
+ * one grid-wide wait, every CTA derives the same norm and factor from the partial sums in a fixed order, and the
+ * update follows in the same kernel. That launch's partial sums are grouped by its own CTAs, so its norm may differ
+ * from mica_clip_grad_norms's in the last bit when the exact sum lies within ~1e-13 of a float32 rounding boundary
+ * (both are within the norm's 1e-5 of the exact value). On GB300 it is the slower of the two (a cooperative launch
+ * cannot overlap the steps around it). Its grid-wide wait is bounded: if it gives up (only a GPU that did not keep
+ * the launch's CTAs resident could make it), the kernel stops, mica_sync() reports MICA_ERR_CUDA and the list's
+ * cached table must be released (mica_release_cache) before it is used again.
+ * Errors: those of mica_clip_grad_norms and mica_adamw_steps.
+ */
+MICA_API mica_status mica_clip_adamw_step(float* const* w, void* const* g, void* const* m, void* const* v,
+                                          const int64_t* n, int32_t T, mica_dtype gdt, mica_dtype mdt,
+                                          const mica_adamw_hp* hp, float max_norm, float inv_scale, float* d_norm,
+                                          float* d_factor, void* stream);
+
 /* One SGD step's hyperparameters. */
 typedef struct {
     double lr;          /* finite, >= 0 */
@@ -243,6 +270,16 @@ MICA_API mica_status mica_sync(void* stream);
  */
 MICA_API mica_status mica_selftest_wait_timeout(uint32_t polls, void* stream);
 
+/*
+ * Self-test of the fused launch's grid-wide wait (mica_clip_adamw_step), which the method's pages have no
+ * counterpart to: queues on `stream` one one-CTA kernel that waits for a second CTA that is never launched; its
+ * bounded wait gives up after `polls` polls (1 <= polls <= 2^20, else MICA_ERR_HYPER; each poll sleeps ~128 ns or
+ * more) and ORs 0x10 into the fused kernels' status word. The next mica_sync(stream) reports MICA_ERR_CUDA
+ * ("... grid-wide wait gave up (status 0x10)"), the one after it MICA_OK, and the context stays usable. Nothing
+ * faults, traps or hangs.
+ */
+MICA_API mica_status mica_selftest_grid_wait_timeout(uint32_t polls, void* stream);
+
 /* Waits for the current device, then frees every cached per-list device table. Returns MICA_OK or MICA_ERR_CUDA. */
 MICA_API mica_status mica_release_cache(void);
 
@@ -274,8 +311,8 @@ MICA_API mica_status mica_work_items(const int64_t* n, const int32_t* vec, int32
                                      int64_t* items, int32_t max_items, int32_t* pack, int32_t max_pack,
                                      int32_t* num_items, int32_t* pack_len, int32_t* used_item_octs);
 
-/* The ABI version of this header: 3 (2 had no mica_work_items; 1 had neither mica_adamw_steps_grouped nor
- * mica_sgd_steps). */
+/* The ABI version of this header: 4 (3 had neither mica_clip_adamw_step, mica_selftest_grid_wait_timeout nor
+ * MICA_ERR_CAPTURE; 2 had no mica_work_items; 1 had neither mica_adamw_steps_grouped nor mica_sgd_steps). */
 MICA_API int32_t mica_abi_version(void);
 
 #ifdef __cplusplus

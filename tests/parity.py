@@ -81,10 +81,18 @@ def hp_of(wl: workloads.Workload, t: int) -> oracle.Hyper:
 
 
 def gpu_step(st: workloads.State, lists, t: int, zero_grad: bool = False, max_norm: float | None = None,
-             norm_out=None, factor_out=None, coupled_l2: bool = False, skip_nonfinite: bool = False):
-    """One clip + AdamW step of the hot path on the device, through the binding (one C-ABI call each)."""
+             norm_out=None, factor_out=None, coupled_l2: bool = False, skip_nonfinite: bool = False,
+             fused: bool = False):
+    """One clip + AdamW step of the hot path on the device, through the binding: one C-ABI call each for the norm
+    and the update, or (``fused``) the one call of mica_clip_adamw_step."""
     wl = st.wl
     W, G, M, V = lists
+    if fused:
+        return mica.mica_clip_adamw_step(W, G, M, V, max_norm=wl.max_norm if max_norm is None else max_norm,
+                                         inv_scale=wl.inv_scale, lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2,
+                                         eps=wl.eps, weight_decay=wl.weight_decay, step=t, zero_grad=zero_grad,
+                                         norm_out=norm_out, factor_out=factor_out, coupled_l2=coupled_l2,
+                                         skip_nonfinite=skip_nonfinite)
     norm, factor = mica.mica_clip_grad_norms(G, wl.max_norm if max_norm is None else max_norm, wl.inv_scale,
                                              norm_out=norm_out, factor_out=factor_out)
     mica.mica_adamw_steps(W, G, M, V, lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps,
@@ -124,7 +132,7 @@ def compare_state(st: workloads.State, host, same_factor: bool, tag: str) -> Non
 
 def run_parity(wl: workloads.Workload, sizes=None, steps: int | None = None, zero_grad: bool = False,
                seed: int | None = None, ora: oracle.Oracle | None = None, check_every_step: bool = True,
-               grad_hook=None, coupled_l2: bool = False, skip_nonfinite: bool = False) -> dict:
+               grad_hook=None, coupled_l2: bool = False, skip_nonfinite: bool = False, fused: bool = False) -> dict:
     """Both sides from the same initial state for ``steps`` steps, each step's gradient drawn on the device and
     copied to the oracle. Compares the norm every step and the state every step (or only at the end)."""
     ora = ora or oracle.Oracle()
@@ -141,7 +149,7 @@ def run_parity(wl: workloads.Workload, sizes=None, steps: int | None = None, zer
         host_g = [x.copy() for x in workloads.host_lists(st)[1]]
         host = (host[0], host_g, host[2], host[3])
         d_norm, d_factor = gpu_step(st, lists, t, zero_grad=zero_grad, coupled_l2=coupled_l2,
-                                    skip_nonfinite=skip_nonfinite)
+                                    skip_nonfinite=skip_nonfinite, fused=fused)
         o_norm, o_factor = ora.clip_adamw_step(*host, hp_of(wl, t), wl.max_norm, wl.inv_scale, zero_grad=zero_grad,
                                                decoupled=not coupled_l2, skip_nonfinite=skip_nonfinite)
         torch.cuda.synchronize()

@@ -29,7 +29,7 @@ def test_exports_every_declared_symbol():
     assert len(names) >= 9
     for name in names:
         assert hasattr(L, name), name
-    assert L.mica_abi_version() == 3
+    assert L.mica_abi_version() == 4
 
 
 def test_status_strings():
@@ -150,6 +150,28 @@ def test_clip_host_validation():
     assert L.mica_clip_grad_norms(G, N, -2, 0, 1.0, 1.0, None, f, None) == COUNT
 
 
+def test_clip_adamw_step_host_validation():
+    """The fused step checks the norm's arguments and the update's, on the host, before anything is queued."""
+    L = mica.lib()
+    P = _arr(ctypes.c_void_p, [0x1000])
+    N = _arr(ctypes.c_int64, [4])
+    f = ctypes.c_void_p(0x2000)
+
+    def step(hp=None, gdt=0, mdt=0, mx=1.0, inv=1.0, factor=f, T=1, n=N):
+        hp_ref = ctypes.byref(hp) if hp is not None else None
+        return L.mica_clip_adamw_step(P, P, P, P, n, T, gdt, mdt, hp_ref, mx, inv, None, factor, None)
+    assert step(hp=_hp(), factor=None) == NULL
+    assert step(hp=None) == NULL
+    assert step(hp=_hp(), gdt=2) == DTYPE
+    assert step(hp=_hp(), mdt=1) == DTYPE
+    for mx, inv in ((0.0, 1.0), (math.nan, 1.0), (1.0, 0.0), (1.0, math.inf)):
+        assert step(hp=_hp(), mx=mx, inv=inv) == HYPER, (mx, inv)
+    assert step(hp=_hp(lr=-1.0)) == HYPER
+    assert step(hp=_hp(beta2=1.0)) == BETA
+    assert step(hp=_hp(), T=-1) == COUNT
+    assert step(hp=_hp(), n=_arr(ctypes.c_int64, [-4])) == COUNT
+
+
 def test_scale_host_validation():
     L = mica.lib()
     t = _arr(ctypes.c_void_p, [0x1000])
@@ -163,8 +185,9 @@ def test_scale_host_validation():
 
 def test_selftest_host_validation():
     L = mica.lib()
-    assert L.mica_selftest_wait_timeout(0, None) == HYPER
-    assert L.mica_selftest_wait_timeout((1 << 20) + 1, None) == HYPER
+    for fn in (L.mica_selftest_wait_timeout, L.mica_selftest_grid_wait_timeout):
+        assert fn(0, None) == HYPER
+        assert fn((1 << 20) + 1, None) == HYPER
 
 
 def test_no_kernels_without_a_device():
