@@ -396,8 +396,10 @@ def measure(wl: workloads.Workload, steps: int, warmup: int, zero_grad: bool, di
            "adamw_ms": statistics.mean(adamw_ms), "clip_ms": statistics.mean(clip_ms), "launches": launches,
            "t_wall": (t_wall0, t_wall1), "norm": float(norm.item())}
     mica.mica_sync()
-    del st
-    return out, (W, G, M, V, norm, factor, kw)
+    del st, W, G, M, V
+    mica.mica_release_cache()  # the list's tables go with its tensors
+    torch.cuda.empty_cache()
+    return out
 
 
 def measure_e2e(wl: workloads.Workload, steps: int, warmup: int):
@@ -452,7 +454,9 @@ def measure_e2e(wl: workloads.Workload, steps: int, warmup: int):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
     h2d = st.g_flat.numel() * st.g_flat.element_size()
-    del st, g_flat, views
+    del st, g_flat, views, g_lists, W, M, V, g_host
+    mica.mica_release_cache()
+    torch.cuda.empty_cache()
     return ms, h2d, 4
 
 
@@ -502,7 +506,7 @@ def main():
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if sampler:
         sampler.start()
-    main_fig, _ = measure(wl, args.steps, args.warmup, zero_grad=False, dist=dist)
+    main_fig = measure(wl, args.steps, args.warmup, zero_grad=False, dist=dist)
     if sampler:
         sampler.stop()
     clocks = sampler.summary(*main_fig["t_wall"]) if sampler else None
@@ -520,7 +524,7 @@ def main():
     e2e = None
     cpu = None
     if not args.no_extras and rank == 0:
-        zg, _ = measure(wl, extra_steps(main_fig["ms_per_step"]), args.warmup, zero_grad=True)
+        zg = measure(wl, extra_steps(main_fig["ms_per_step"]), args.warmup, zero_grad=True)
         extras["zero_grad"] = {"ms_per_step": zg["ms_per_step"], "steps": zg["steps"],
                                "hbm_gbs_model": P * step_bytes_per_param(wl) / (zg["ms_per_step"] / 1e3) / 1e9,
                                "hbm_gbs_actual": P * step_bytes_per_param(wl, True) / (zg["ms_per_step"] / 1e3) / 1e9,
@@ -540,8 +544,8 @@ def main():
                 continue
             if fused is not None:
                 os.environ["MICA_FUSED"] = fused
-            est, _ = measure(owl, 10, args.warmup, zero_grad=False, coupled_l2=coupled, opt=opt, per_kernel=False)
-            f, _ = measure(owl, extra_steps(est["ms_per_step"]), args.warmup, zero_grad=False, coupled_l2=coupled,
+            est = measure(owl, 10, args.warmup, zero_grad=False, coupled_l2=coupled, opt=opt, per_kernel=False)
+            f = measure(owl, extra_steps(est["ms_per_step"]), args.warmup, zero_grad=False, coupled_l2=coupled,
                            opt=opt)
             os.environ.pop("MICA_FUSED", None)
             torch.cuda.empty_cache()

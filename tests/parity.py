@@ -146,7 +146,7 @@ def run_parity(wl: workloads.Workload, sizes=None, steps: int | None = None, zer
         workloads.fill_grad(st, t, seed=seed)
         if grad_hook is not None:
             grad_hook(st, t)
-        host_g = [x.copy() for x in workloads.host_lists(st)[1]]
+        host_g = [x.detach().cpu().numpy().copy() for x in st.g]  # this step's gradient, for the oracle
         host = (host[0], host_g, host[2], host[3])
         d_norm, d_factor = gpu_step(st, lists, t, zero_grad=zero_grad, coupled_l2=coupled_l2,
                                     skip_nonfinite=skip_nonfinite, fused=fused)
