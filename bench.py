@@ -9,7 +9,8 @@ JSON line.
 
 --impl reference times the CPU oracle (the plain single-threaded C step) on the host cores instead, on a bounded
 sample of the same workload. Under torchrun with N > 1 every rank runs the whole step on its own GPU (each rank a
-replica, as data-parallel training steps its replicated parameters); the time is the slowest rank's.
+replica, as data-parallel training steps its replicated parameters); the time is the slowest rank's. With --shard
+the ranks split the list instead (each steps its own part after one all-gather of the norm's square sums).
 """
 from __future__ import annotations
 
@@ -402,6 +403,66 @@ def measure(wl: workloads.Workload, steps: int, warmup: int, zero_grad: bool, di
     return out
 
 
+def measure_sharded(wl: workloads.Workload, steps: int, warmup: int, dist, world: int, rank: int):
+    """The sharded step (the list split over the ranks, ZeRO-style): each rank's square sum of its own part
+    (mica_grad_sumsq), an all-gather of one double per rank, the factor from the sums in rank order
+    (mica_clip_factor_from_sumsq), and each rank's update of its own part. Times `steps` steps as measure() does."""
+    import clip_tensor_adamw_gb300 as mica
+    from clip_tensor_adamw_gb300.shard import piece_views, shard_pieces
+    st = workloads.make_state(wl, "cuda")
+    workloads.fill_grad(st, 1)
+    pieces = shard_pieces(st.sizes, world, rank)
+    counts = [b - a for _, a, b in pieces]
+    W = mica.TensorList(piece_views(st.w, pieces))
+    G = mica.TensorList(piece_views(st.g, pieces))
+    M = mica.TensorList(piece_views(st.m, pieces, st.m_packed), counts)
+    V = mica.TensorList(piece_views(st.v, pieces, st.packed), counts)
+    mine = torch.zeros(1, dtype=torch.float64, device="cuda")
+    parts = torch.zeros(world, dtype=torch.float64, device="cuda")
+    norm = torch.empty(1, device="cuda")
+    factor = torch.empty(1, device="cuda")
+    kw = dict(lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps, weight_decay=wl.weight_decay, factor=factor)
+    stream = torch.cuda.current_stream()
+
+    def step(t):
+        mica.mica_grad_sumsq(G, wl.inv_scale, out=mine)
+        if dist is not None:
+            dist.all_gather_into_tensor(parts, mine)
+        else:
+            parts.copy_(mine)
+        mica.mica_clip_factor_from_sumsq(parts, wl.max_norm, wl.inv_scale, norm_out=norm, factor_out=factor)
+        mica.mica_adamw_steps(W, G, M, V, step=t, **kw)
+
+    for t in range(1, warmup + 1):
+        step(t)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = mica.mica_launch_count()
+    t_wall0 = time.time()
+    start.record(stream)
+    for i in range(steps):
+        step(warmup + 1 + i)
+    end.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    launches = mica.mica_launch_count() - launches0
+    total_ms = start.elapsed_time(end)
+    if dist is not None:
+        dist.barrier()
+        total_ms = slowest_rank_ms(total_ms, dist, "cuda")
+    out = {"total_ms": total_ms, "ms_per_step": total_ms / steps, "steps": steps, "launches": launches,
+           "t_wall": (t_wall0, t_wall1), "norm": float(norm.item()),
+           "part_params": sum(counts), "pieces": len(pieces)}
+    mica.mica_sync()
+    del st, W, G, M, V
+    mica.mica_release_cache()
+    torch.cuda.empty_cache()
+    return out
+
+
 def measure_e2e(wl: workloads.Workload, steps: int, warmup: int):
     """The same step through the public API, fed from the host: every step copies its whole gradient from pinned host
     memory into one of two device gradient buffers (on a copy stream, so that step t+1's copy overlaps step t's
@@ -468,6 +529,9 @@ def main():
     ap.add_argument("--workload", default="gpt2_small", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="mica", choices=["mica", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="skip the other workloads, e2e and the CPU baseline")
+    ap.add_argument("--shard", action="store_true",
+                    help="split the list over the ranks (each steps its own part; one all-gather of the norm's "
+                         "square sums a step) instead of stepping a replica on every rank")
     ap.add_argument("--subset-params", type=int, default=0,
                     help="keep only the workload's first tensors up to this many parameters (small profiling case)")
     args = ap.parse_args()
@@ -506,10 +570,31 @@ def main():
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if sampler:
         sampler.start()
-    main_fig = measure(wl, args.steps, args.warmup, zero_grad=False, dist=dist)
+    if args.shard:
+        main_fig = measure_sharded(wl, args.steps, args.warmup, dist, world, rank)
+    else:
+        main_fig = measure(wl, args.steps, args.warmup, zero_grad=False, dist=dist)
     if sampler:
         sampler.stop()
     clocks = sampler.summary(*main_fig["t_wall"]) if sampler else None
+    if args.shard:
+        if rank == 0:
+            P = wl.params
+            sec = main_fig["total_ms"] / 1e3
+            gbs = P * step_bytes_per_param(wl) * args.steps / sec / 1e9
+            print(json.dumps({
+                "metric": METRIC, "value": P * args.steps / sec, "unit": "params/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": main_fig["ms_per_step"],
+                "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "f32",
+                "data": "synthetic",
+                "config": {**run_config(wl, world), "parallelism": f"sharded x{world} (one all-gather a step)"},
+                "hbm_gbs": gbs, "pct_of_8tbs": 100 * gbs / NOMINAL_HBM_GBS, "clocks": clocks,
+                "gpu_launches": main_fig["launches"], "norm": main_fig["norm"],
+                "rank0_part_params": main_fig["part_params"]}), flush=True)
+        if dist is not None:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
 
     P = wl.params
     sec = main_fig["total_ms"] / 1e3

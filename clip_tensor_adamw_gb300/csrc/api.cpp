@@ -820,8 +820,55 @@ extern "C" mica_status mica_clip_grad_norms(const void* const* g, const int64_t*
     if ((s = check_scalars(p, dev, d_factor, d_norm, "a gradient")) != MICA_OK) return s;
     const bool keep_l2 = p->total * (int64_t)elem_bytes((Dtype)gdt) <= kKeepL2MaxGradBytes;
     return after_launch(launch_norm(p->chunks, (Dtype)gdt, inv_scale, p->partials, p->ticket, max_norm, d_norm,
-                                    d_factor, keep_l2, stream),
+                                    d_factor, nullptr, keep_l2, stream),
                         stream, "ClipGradNorms launch");
+}
+
+extern "C" mica_status mica_grad_sumsq(const void* const* g, const int64_t* n, int32_t T, mica_dtype gdt,
+                                       float inv_scale, double* d_sumsq, void* stream) {
+    if (gdt != MICA_F32 && gdt != MICA_F16) return fail(MICA_ERR_DTYPE, "gradients must be float32 or float16");
+    if (!d_sumsq) return fail(MICA_ERR_NULL, "d_sumsq is NULL");
+    if (!std::isfinite(inv_scale) || !(inv_scale > 0.0f))
+        return fail(MICA_ERR_HYPER, "inv_scale %g is not finite and > 0", (double)inv_scale);
+    if (T < 0 || T > MICA_MAX_TENSORS) return fail(MICA_ERR_COUNT, "T = %d is outside [0, %d]", T, MICA_MAX_TENSORS);
+    if (T > 0 && (!g || !n)) return fail(MICA_ERR_NULL, "a pointer array is NULL");
+    mica_status s;
+    int dev = 0;
+    ListDesc L{kNorm, T, n, nullptr, const_cast<void* const*>(reinterpret_cast<const void* const*>(g)), nullptr,
+               nullptr, (Dtype)gdt, kF32};
+    Plan* p = nullptr;
+    if (T > 0 && current_device(&dev) == MICA_OK) p = cached_plan(L, dev);
+    if (!p) {
+        int64_t total = 0;
+        if ((s = check_list(T, n, {g}, &total)) != MICA_OK) return s;
+        if ((s = current_device(&dev)) != MICA_OK) return s;
+        if (total == 0) L.T = 0;  // an empty list still gets its sum (0) written
+        if ((s = get_plan(L, dev, &p, stream)) != MICA_OK) return s;
+    }
+    if ((s = check_device_span(d_sumsq, 8, 8, dev, "d_sumsq", 0)) != MICA_OK) return s;
+    if (overlaps_any(p->spans, d_sumsq, 8)) return fail(MICA_ERR_OVERLAP, "d_sumsq lies inside a gradient");
+    const bool keep_l2 = p->total * (int64_t)elem_bytes((Dtype)gdt) <= kKeepL2MaxGradBytes;
+    return after_launch(launch_norm(p->chunks, (Dtype)gdt, inv_scale, p->partials, p->ticket, 1.0f, nullptr, nullptr,
+                                    d_sumsq, keep_l2, stream),
+                        stream, "square-sum launch");
+}
+
+extern "C" mica_status mica_clip_factor_from_sumsq(const double* d_parts, int32_t count, float max_norm,
+                                                   float inv_scale, float* d_norm, float* d_factor, void* stream) {
+    if (!d_parts || !d_factor) return fail(MICA_ERR_NULL, "d_parts or d_factor is NULL");
+    if (count < 1 || count > (1 << 16)) return fail(MICA_ERR_COUNT, "count = %d is outside [1, 65536]", count);
+    if (std::isnan(max_norm) || !(max_norm > 0.0f))
+        return fail(MICA_ERR_HYPER, "max_norm %g is not > 0", (double)max_norm);
+    if (!std::isfinite(inv_scale) || !(inv_scale > 0.0f))
+        return fail(MICA_ERR_HYPER, "inv_scale %g is not finite and > 0", (double)inv_scale);
+    int dev = 0;
+    mica_status s = current_device(&dev);
+    if (s != MICA_OK) return s;
+    if ((s = check_device_span(d_parts, (size_t)count * 8, 8, dev, "d_parts", 0)) != MICA_OK) return s;
+    if ((s = check_device_span(d_factor, 4, 4, dev, "d_factor", 0)) != MICA_OK) return s;
+    if (d_norm && (s = check_device_span(d_norm, 4, 4, dev, "d_norm", 0)) != MICA_OK) return s;
+    return after_launch(launch_factor_from_sumsq(d_parts, count, max_norm, inv_scale, d_norm, d_factor, stream), stream,
+                        "factor launch");
 }
 
 namespace mica {

@@ -184,8 +184,8 @@ extern "C" mica_status mica_clip_grad_norms_noalloc(const void* const* g, const 
         return noalloc_fail(MICA_ERR_CUDA, "uploading the tables into the scratch failed");
     }
     const bool keep_l2 = total * (int64_t)es <= kKeepL2MaxGradBytes;  // as the allocating entry point chooses
-    const int err = launch_norm(ct, (Dtype)gdt, inv_scale, d_part, d_ticket, max_norm, d_norm, d_factor, keep_l2,
-                                stream);
+    const int err = launch_norm(ct, (Dtype)gdt, inv_scale, d_part, d_ticket, max_norm, d_norm, d_factor, nullptr,
+                                keep_l2, stream);
     if (err != (int)cudaSuccess) return noalloc_fail(MICA_ERR_CUDA, "the norm kernel failed to launch");
     return MICA_OK;
 }

@@ -22,7 +22,8 @@ template <Dtype G, int kMode, bool kKeepL2>
 __global__ void __launch_bounds__(kThreads, kNormDirectCtasPerSm) norm_direct_kernel(ChunkTable ct, float inv_scale,
                                                                         double* __restrict__ partials,
                                                                         unsigned int* ticket, float max_norm,
-                                                                        float* d_norm, float* d_factor) {
+                                                                        float* d_norm, float* d_factor,
+                                                                        double* d_sumsq) {
     __shared__ double red[kWarps];
     __shared__ int last;
     __shared__ StagedSpan sp;
@@ -40,7 +41,7 @@ __global__ void __launch_bounds__(kThreads, kNormDirectCtasPerSm) norm_direct_ke
     __syncthreads();
     if (last) {  // every other CTA's partial is written: sum them all, in order
         __threadfence();
-        finalize_norm(partials, ct.grid, max_norm, inv_scale, d_norm, d_factor, red);
+        finalize_norm(partials, ct.grid, max_norm, inv_scale, d_norm, d_factor, d_sumsq, red);
         if (t == 0) *ticket = 0u;  // ready for the next launch on this list
     }
 }
@@ -138,7 +139,7 @@ template <Dtype G, int kMode, bool kKeepL2>
 __global__ void __launch_bounds__(kNormThreads, kNormTmaCtasPerSm) norm_tma_kernel(ChunkTable ct, float inv_scale,
                                                                             double* __restrict__ partials,
                                                                             unsigned int* ticket, float max_norm,
-                                                                            float* d_norm, float* d_factor) {
+                                                                            float* d_norm, float* d_factor, double* d_sumsq) {
     constexpr int S = kNormStages;
     constexpr int kOctBytes = (G == kF16) ? 16 : 32;
     constexpr int kStageBytes = norm_stage_bytes<G>();
@@ -288,7 +289,7 @@ __global__ void __launch_bounds__(kNormThreads, kNormTmaCtasPerSm) norm_tma_kern
     __syncthreads();
     if (last) {  // every other CTA's partial is written: sum them all, in order
         __threadfence();
-        finalize_norm(partials, ct.grid, max_norm, inv_scale, d_norm, d_factor, red);
+        finalize_norm(partials, ct.grid, max_norm, inv_scale, d_norm, d_factor, d_sumsq, red);
         if (t == 0) *ticket = 0u;  // ready for the next launch on this list
     }
 }
@@ -297,7 +298,7 @@ __global__ void __launch_bounds__(kNormThreads, kNormTmaCtasPerSm) norm_tma_kern
 
 template <Dtype G, int kMode, bool kKeepL2>
 cudaError_t launch_norm_t(const ChunkTable& ct, cudaStream_t st, float inv_scale, double* partials,
-                          unsigned int* ticket, float max_norm, float* d_norm, float* d_factor) {
+                          unsigned int* ticket, float max_norm, float* d_norm, float* d_factor, double* d_sumsq) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ct.grid > 0 ? ct.grid : 1);
     cfg.stream = st;
@@ -310,7 +311,7 @@ cudaError_t launch_norm_t(const ChunkTable& ct, cudaStream_t st, float inv_scale
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = 0;
         return cudaLaunchKernelEx(&cfg, norm_direct_kernel<G, kMode, kKeepL2>, ct, inv_scale, partials, ticket,
-                                  max_norm, d_norm, d_factor);
+                                  max_norm, d_norm, d_factor, d_sumsq);
     }
     const size_t smem = norm_smem_bytes<G>();
     cudaError_t e = cudaFuncSetAttribute(norm_tma_kernel<G, kMode, kKeepL2>,
@@ -319,18 +320,33 @@ cudaError_t launch_norm_t(const ChunkTable& ct, cudaStream_t st, float inv_scale
     cfg.blockDim = dim3(kNormThreads);
     cfg.dynamicSmemBytes = smem;
     return cudaLaunchKernelEx(&cfg, norm_tma_kernel<G, kMode, kKeepL2>, ct, inv_scale, partials, ticket, max_norm,
-                              d_norm, d_factor);
+                              d_norm, d_factor, d_sumsq);
 }
 
 template <Dtype G, int kMode>
 cudaError_t launch_norm_k(bool keep_l2, const ChunkTable& ct, cudaStream_t st, float inv_scale, double* partials,
-                          unsigned int* ticket, float max_norm, float* d_norm, float* d_factor) {
-    return keep_l2 ? launch_norm_t<G, kMode, true>(ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor)
-                   : launch_norm_t<G, kMode, false>(ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
+                          unsigned int* ticket, float max_norm, float* d_norm, float* d_factor, double* d_sumsq) {
+    return keep_l2 ? launch_norm_t<G, kMode, true>(ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor,
+                                                   d_sumsq)
+                   : launch_norm_t<G, kMode, false>(ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor,
+                                                    d_sumsq);
+}
+
+// The norm and factor of rank-ordered partial square sums: one thread adds parts[0], parts[1], ... in double.
+static __global__ void __launch_bounds__(32) factor_from_sumsq_kernel(const double* __restrict__ parts, int32_t count,
+                                                               float max_norm, float inv_scale, float* d_norm,
+                                                               float* d_factor) {
+    if (threadIdx.x != 0) return;
+    double S = 0.0;
+    for (int32_t i = 0; i < count; ++i) S += __ldcg(parts + i);
+    float norm, factor;
+    norm_and_factor(S, max_norm, inv_scale, &norm, &factor);
+    if (d_norm) *d_norm = norm;
+    *d_factor = factor;
 }
 
 int launch_norm(const ChunkTable& ct, Dtype gdt, float inv_scale, double* partials, unsigned int* ticket,
-                float max_norm, float* d_norm, float* d_factor, bool keep_l2, void* stream) {
+                float max_norm, float* d_norm, float* d_factor, double* d_sumsq, bool keep_l2, void* stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool scaled = inv_scale != 1.0f;  // an unscaled list skips the multiply (x * 1 is x)
     // binary16 times a power of two in [2^-102, 2^111]: every product is an exact normal float32
@@ -339,16 +355,26 @@ int launch_norm(const ChunkTable& ct, Dtype gdt, float inv_scale, double* partia
     cudaError_t e;
     if (gdt == kF16 && pow2)
         e = launch_norm_k<kF16, kSumHalfPow2>(keep_l2, ct, st, inv_scale, partials, ticket, max_norm, d_norm,
-                                              d_factor);
+                                              d_factor, d_sumsq);
     else if (gdt == kF16)
-        e = launch_norm_k<kF16, kSumScaled>(keep_l2, ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
+        e = launch_norm_k<kF16, kSumScaled>(keep_l2, ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor,
+                                            d_sumsq);
     else if (scaled)
-        e = launch_norm_k<kF32, kSumScaled>(keep_l2, ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
+        e = launch_norm_k<kF32, kSumScaled>(keep_l2, ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor,
+                                            d_sumsq);
     else
         e = launch_norm_k<kF32, kSumUnscaled>(keep_l2, ct, st, inv_scale, partials, ticket, max_norm, d_norm,
-                                              d_factor);
+                                              d_factor, d_sumsq);
     count_launches(1);
     return (int)e;
+}
+
+int launch_factor_from_sumsq(const double* parts, int32_t count, float max_norm, float inv_scale, float* d_norm,
+                             float* d_factor, void* stream) {
+    factor_from_sumsq_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(parts, count, max_norm, inv_scale,
+                                                                             d_norm, d_factor);
+    count_launches(1);
+    return (int)cudaGetLastError();
 }
 
 int launch_wait_selftest(uint32_t polls, void* stream) {

@@ -168,16 +168,17 @@ __device__ __forceinline__ void norm_and_factor(double S, float max_norm, float 
     *factor_out = __fmul_rn(inv_scale, clip);
 }
 
-// The finalize of a norm launch: the partials summed in a fixed order, and norm and factor written to device
-// memory (norm only when d_norm is not null).
+// The finalize of a norm launch: the partials summed in a fixed order; the square sum itself written to d_sumsq
+// when that is not null, and norm and factor to d_norm and d_factor when those are not null.
 __device__ void finalize_norm(const double* partials, int32_t num, float max_norm, float inv_scale, float* d_norm,
-                              float* d_factor, double* red) {
+                              float* d_factor, double* d_sumsq, double* red) {
     const double S = sum_partials(partials, num, red);
     if (threadIdx.x == 0) {
         float norm, factor;
         norm_and_factor(S, max_norm, inv_scale, &norm, &factor);
         if (d_norm) *d_norm = norm;
-        *d_factor = factor;
+        if (d_factor) *d_factor = factor;
+        if (d_sumsq) *d_sumsq = S;
     }
 }
 

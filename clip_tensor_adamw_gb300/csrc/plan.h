@@ -151,10 +151,15 @@ int launch_sgd(const UpdateLaunch& u, Dtype gdt, bool momentum, bool skip, const
 // The joint norm in one launch of ct.grid CTAs: one partial square sum per CTA into `partials` (ct.grid doubles),
 // and the CTA that finishes last sums them in a fixed order and writes norm and factor. `ticket` must be 0 before
 // the launch; the kernel leaves it 0.
-// keep_l2: the gradient's loads (and bulk copies) carry an evict-last L2 policy, so that the update that follows
-// reads the gradient from L2 (for gradients that fit in it, see kKeepL2MaxGradBytes).
+// d_norm, d_factor and d_sumsq (the square sum itself, in double) are each written when not null. keep_l2: the
+// gradient's loads (and bulk copies) carry an evict-last L2 policy, so that the update that follows reads the
+// gradient from L2 (for gradients that fit in it, see kKeepL2MaxGradBytes).
 int launch_norm(const ChunkTable& ct, Dtype gdt, float inv_scale, double* partials, unsigned int* ticket,
-                float max_norm, float* d_norm, float* d_factor, bool keep_l2, void* stream);
+                float max_norm, float* d_norm, float* d_factor, double* d_sumsq, bool keep_l2, void* stream);
+// Norm and factor from `count` partial square sums (one per rank of a sharded list), added in index order in double;
+// one thread of one CTA.
+int launch_factor_from_sumsq(const double* parts, int32_t count, float max_norm, float inv_scale, float* d_norm,
+                             float* d_factor, void* stream);
 // Gradient bytes up to which the norm asks L2 to keep the gradient for the update (GB300 has 126 MB of L2; the
 // update's own streams pass through it with evict-first hints). Larger gradients would only push the update's
 // other streams out.

@@ -69,8 +69,11 @@ def lib() -> ctypes.CDLL:
                                      _P, _P]
         L.mica_clip_adamw_step.argtypes = [_P, _P, _P, _P, _I64P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                            ctypes.POINTER(_HP), ctypes.c_float, ctypes.c_float, _P, _P, _P]
+        L.mica_grad_sumsq.argtypes = [_P, _I64P, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, _P, _P]
+        L.mica_clip_factor_from_sumsq.argtypes = [_P, ctypes.c_int32, ctypes.c_float, ctypes.c_float, _P, _P, _P]
         for f in ("mica_scale_tensors", "mica_clip_grad_norms", "mica_adamw_steps", "mica_adamw_steps_grouped",
-                  "mica_sgd_steps", "mica_clip_adamw_step", "mica_sync", "mica_release_cache"):
+                  "mica_sgd_steps", "mica_clip_adamw_step", "mica_grad_sumsq", "mica_clip_factor_from_sumsq",
+                  "mica_sync", "mica_release_cache"):
             getattr(L, f).restype = ctypes.c_int
         for f in ("mica_selftest_wait_timeout", "mica_selftest_grid_wait_timeout"):
             getattr(L, f).argtypes = [ctypes.c_uint32, _P]
@@ -163,6 +166,34 @@ def mica_clip_grad_norms(grads, max_norm: float, inv_scale: float = 1.0, norm_ou
     gdt = _dtype_code(L.tensors[0] if L.T else None, "grads")
     _check(lib().mica_clip_grad_norms(L.ptrs, L.n, L.T, gdt, float(max_norm), float(inv_scale), _ptr(norm_out),
                                       _ptr(factor_out), _stream(stream)))
+    return norm_out, factor_out
+
+
+def mica_grad_sumsq(grads, inv_scale: float = 1.0, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The sum of squares of the unscaled gradients, exactly as the norm sums it, as a one-element float64 device
+    tensor (``out`` when given): one rank's share of a sharded list's joint norm."""
+    L = _as_list(grads)
+    dev = L.tensors[0].device if L.T else torch.device("cuda", torch.cuda.current_device())
+    if out is None:
+        out = torch.empty(1, dtype=torch.float64, device=dev)
+    gdt = _dtype_code(L.tensors[0] if L.T else None, "grads")
+    _check(lib().mica_grad_sumsq(L.ptrs, L.n, L.T, gdt, float(inv_scale), _ptr(out), _stream(stream)))
+    return out
+
+
+def mica_clip_factor_from_sumsq(parts: torch.Tensor, max_norm: float, inv_scale: float = 1.0,
+                                norm_out: torch.Tensor | None = None, factor_out: torch.Tensor | None = None,
+                                stream=None):
+    """Norm and clip factor from the ranks' square sums ``parts`` (a float64 device tensor, in rank order), added
+    in that order: every rank passing the same parts gets the same bits. Returns the device (norm, factor)."""
+    if parts.dtype != torch.float64 or not parts.is_contiguous():
+        raise TypeError("parts must be a contiguous float64 tensor")
+    if norm_out is None:
+        norm_out = torch.empty(1, dtype=torch.float32, device=parts.device)
+    if factor_out is None:
+        factor_out = torch.empty(1, dtype=torch.float32, device=parts.device)
+    _check(lib().mica_clip_factor_from_sumsq(_ptr(parts), parts.numel(), float(max_norm), float(inv_scale),
+                                             _ptr(norm_out), _ptr(factor_out), _stream(stream)))
     return norm_out, factor_out
 
 

@@ -136,6 +136,30 @@ MICA_API mica_status mica_clip_grad_norms(const void* const* g, const int64_t* n
                                  float inv_scale, float* d_norm, float* d_factor, void* stream);
 
 /*
+ * The joint norm of a list sharded over several GPUs (each rank holding a contiguous part of the parameters, as a
+ * ZeRO-style partition does), in two calls around one exchange that the caller makes (an all-gather of one double
+ * per rank): ClipGradNorms's joint norm ("Mica 7.7 ...", section "The whole model in one call") is that of every
+ * gradient of every rank, so each rank sums its own part and the sums are added in rank order.
+ *
+ * mica_grad_sumsq: writes *d_sumsq (a device double) = the sum over the list of x^2, x = f32(g * inv_scale), summed
+ * exactly as mica_clip_grad_norms sums it (the same kernel and work split; an empty list gives 0).
+ * Errors: NULL / COUNT / DTYPE / HYPER (inv_scale) / ADDRESS / OVERLAP (d_sumsq inside a gradient) / DEVICE / CUDA /
+ * NOMEM.
+ */
+MICA_API mica_status mica_grad_sumsq(const void* const* g, const int64_t* n, int32_t T, mica_dtype gdt, float inv_scale,
+                                     double* d_sumsq, void* stream);
+
+/*
+ * mica_clip_factor_from_sumsq: from `count` per-rank square sums d_parts[0 .. count-1] (device doubles, in rank
+ * order), S = d_parts[0] + d_parts[1] + ... in double, in that order, and then, as mica_clip_grad_norms:
+ * *d_norm = f32(sqrt(S)) (when d_norm is not NULL) and *d_factor = inv_scale * min(1, max_norm / (norm + 1e-6)). Every
+ * rank that passes the same d_parts gets the same bits. 1 <= count <= 65536.
+ * Errors: NULL / COUNT / HYPER / ADDRESS / DEVICE / CUDA.
+ */
+MICA_API mica_status mica_clip_factor_from_sumsq(const double* d_parts, int32_t count, float max_norm, float inv_scale,
+                                                 float* d_norm, float* d_factor, void* stream);
+
+/*
  * AdamWSteps. For every group k and element i < n[k], in float32, each operation rounded on its own:
  *   gh = g * f                          f = *d_factor (device float32) or 1 when d_factor is NULL
  *   w' = w * (1 - lr*wd)
@@ -311,8 +335,9 @@ MICA_API mica_status mica_work_items(const int64_t* n, const int32_t* vec, int32
                                      int64_t* items, int32_t max_items, int32_t* pack, int32_t max_pack,
                                      int32_t* num_items, int32_t* pack_len, int32_t* used_item_octs);
 
-/* The ABI version of this header: 4 (3 had neither mica_clip_adamw_step, mica_selftest_grid_wait_timeout nor
- * MICA_ERR_CAPTURE; 2 had no mica_work_items; 1 had neither mica_adamw_steps_grouped nor mica_sgd_steps). */
+/* The ABI version of this header: 4 (3 had none of mica_clip_adamw_step, mica_grad_sumsq,
+ * mica_clip_factor_from_sumsq, mica_selftest_grid_wait_timeout and MICA_ERR_CAPTURE; 2 had no mica_work_items; 1 had
+ * neither mica_adamw_steps_grouped nor mica_sgd_steps). */
 MICA_API int32_t mica_abi_version(void);
 
 #ifdef __cplusplus
