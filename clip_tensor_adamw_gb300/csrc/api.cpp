@@ -992,7 +992,7 @@ static mica_status adamw_steps(float* const* w, void* const* g, void* const* m, 
 // 0.021 ms), because a cooperative launch cannot overlap the steps before and after it, and its norm phase runs at
 // the update's 3 CTAs per SM; the two launches get the L2 re-read too, from the norm's evict-last policy on
 // gradients that fit in L2.
-static bool use_fused(const Plan*) {
+static bool use_fused() {
     const char* e = std::getenv("MICA_FUSED");
     return e && std::strcmp(e, "1") == 0;
 }
@@ -1029,28 +1029,24 @@ extern "C" mica_status mica_clip_adamw_step(float* const* w, void* const* g, voi
     AdamCall a;
     mica_status s = prepare_adamw(w, g, m, v, n, T, gdt, mdt, nullptr, hp, 1, d_factor, d_norm, stream, &a);
     if (s != MICA_OK) return s;
-    if (!a.p || !use_fused(a.p)) {
-        // an empty list (its norm is 0 and its factor inv_scale) or a gradient larger than the L2 budget: the two
-        // launches of mica_clip_grad_norms and mica_adamw_steps
-        s = mica_clip_grad_norms(const_cast<const void* const*>(g), n, T, gdt, max_norm, inv_scale, d_norm, d_factor,
-                                 stream);
-        if (s != MICA_OK || !a.p) return s;
+    // the two launches of mica_clip_grad_norms and mica_adamw_steps (an empty list only gets its norm, 0, and its
+    // factor, inv_scale)
+    auto two_launches = [&]() -> mica_status {
+        mica_status r = mica_clip_grad_norms(const_cast<const void* const*>(g), n, T, gdt, max_norm, inv_scale, d_norm,
+                                             d_factor, stream);
+        if (r != MICA_OK || !a.p) return r;
         return after_launch(launch_adamw(update_launch(a.p, true), (Dtype)gdt, (Dtype)mdt, a.coupled, a.sc, nullptr,
                                          d_factor, stream),
                             stream, "AdamWSteps launch");
-    }
+    };
+    if (!a.p || !use_fused()) return two_launches();
     if ((s = ensure_fused_table(a.p, stream)) != MICA_OK) return s;
     const int e = launch_clip_adamw(a.p->fchunks, a.p->fpartials, a.p->fbar, update_launch(a.p, true, true),
                                     (Dtype)gdt, (Dtype)mdt, a.coupled, a.sc, max_norm, inv_scale, d_norm, d_factor,
                                     stream);
-    if (e == (int)cudaErrorCooperativeLaunchTooLarge) {  // not one wave on this GPU: the two launches instead
+    if (e == (int)cudaErrorCooperativeLaunchTooLarge) {  // not one wave on this GPU: nothing queued, two launches
         cudaGetLastError();
-        s = mica_clip_grad_norms(const_cast<const void* const*>(g), n, T, gdt, max_norm, inv_scale, d_norm, d_factor,
-                                 stream);
-        if (s != MICA_OK) return s;
-        return after_launch(launch_adamw(update_launch(a.p, true), (Dtype)gdt, (Dtype)mdt, a.coupled, a.sc, nullptr,
-                                         d_factor, stream),
-                            stream, "AdamWSteps launch");
+        return two_launches();
     }
     return after_launch(e, stream, "fused ClipGradNorms + AdamWSteps launch");
 }
