@@ -12,7 +12,11 @@ import workloads
 pytestmark = pytest.mark.gpu
 
 
-def test_captured_step_replays(ora):
+@pytest.mark.parametrize("entry", ["separate", "one_step"])
+def test_captured_step_replays(ora, entry, monkeypatch):
+    """The norm and the update captured as two calls, or as the one call of mica_clip_adamw_step (its default
+    path: the same two launches)."""
+    monkeypatch.delenv("MICA_FUSED", raising=False)
     wl = workloads.WORKLOADS["gpt2_small"]
     sizes = [int(np.prod(s)) for s in workloads._gpt2_shapes(90, 2, 1003, 67)]
     st = workloads.make_state(wl, "cuda", sizes=sizes)
@@ -27,6 +31,10 @@ def test_captured_step_replays(ora):
     host = workloads.host_lists(st)
     mica.mica_clip_grad_norms(G, wl.max_norm, wl.inv_scale, norm_out=norm, factor_out=factor)
     mica.mica_adamw_steps(W, G, M, V, **kw)
+    if entry == "one_step":  # its scalar-output check (norm and factor together) also happens once, outside
+        mica.mica_clip_adamw_step(W, G, M, V, max_norm=wl.max_norm, inv_scale=wl.inv_scale, norm_out=norm,
+                                  factor_out=factor, **{k: v for k, v in kw.items() if k != "factor"})
+        ora.clip_adamw_step(*host, parity.hp_of(wl, t_fixed), wl.max_norm, wl.inv_scale)
     hp = parity.hp_of(wl, t_fixed)
     ora.clip_adamw_step(*host, hp, wl.max_norm, wl.inv_scale)
     torch.cuda.synchronize()
@@ -36,8 +44,13 @@ def test_captured_step_replays(ora):
     stream.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(stream):
         graph.capture_begin()
-        mica.mica_clip_grad_norms(G, wl.max_norm, wl.inv_scale, norm_out=norm, factor_out=factor, stream=stream)
-        mica.mica_adamw_steps(W, G, M, V, stream=stream, **kw)
+        if entry == "separate":
+            mica.mica_clip_grad_norms(G, wl.max_norm, wl.inv_scale, norm_out=norm, factor_out=factor, stream=stream)
+            mica.mica_adamw_steps(W, G, M, V, stream=stream, **kw)
+        else:
+            one = {k: v for k, v in kw.items() if k != "factor"}
+            mica.mica_clip_adamw_step(W, G, M, V, max_norm=wl.max_norm, inv_scale=wl.inv_scale, norm_out=norm,
+                                      factor_out=factor, stream=stream, **one)
         graph.capture_end()
     torch.cuda.current_stream().wait_stream(stream)
     torch.cuda.synchronize()
