@@ -264,13 +264,13 @@ static int32_t choose_item_octs(int64_t total_octs, int sms, int32_t base) {
 // octet, every octet of an unaligned tensor), so that the element-by-element octets share warps with each other and
 // not with the vector ones; its row of the pack table (from its item's o0) is the first whole octet of each tensor
 // and the whole octets' total, then the first of each tensor's other octets and their total (2 count + 2 entries).
-// Tensors of up to 512 octets (and at most io) are packed, up to 1024 octets a pack (and at most 2 io): measured
+// Tensors of up to 512 octets (and at most io) are packed, up to 1536 octets a pack (and at most 3 io): measured
 // best on GB300 for lists of thousands of small tensors.
 static std::vector<WorkItem> build_items(const int64_t* n, const TensorRec* recs, int32_t T, int32_t io,
                                          std::vector<int32_t>* pack_pre) {
     std::vector<WorkItem> items;
     const int64_t small = std::min<int64_t>(512, io);
-    const int64_t pack_cap = std::min<int64_t>(1024, 2 * (int64_t)io);
+    const int64_t pack_cap = std::min<int64_t>(1536, 3 * (int64_t)io);
     bool open = false;
     WorkItem pack{};
     int64_t pack_o = 0;

@@ -10,7 +10,7 @@
 //
 // Work items are counted in octets (8 consecutive elements: one 32-byte float32 vector, one 16-byte vector of
 // binary16 values or of 4 packed BF16 words). A large tensor is cut into slices of `item_octs` octets; runs of
-// consecutive small tensors (each at most min(512, item_octs) octets, at most min(1024, 2 item_octs) octets a pack)
+// consecutive small tensors (each at most min(512, item_octs) octets, at most min(1536, 3 item_octs) octets a pack)
 // are packed into one item whose octets the CTA's threads share out one by one (the list's pack table holds, per
 // pack, the first pack octet of each of its tensors and the pack's total; ScaleTensors instead gives each warp whole
 // tensors). Every element belongs to exactly one item, so each element is read and written by exactly one thread per

@@ -20,7 +20,7 @@ def check_items(sizes, vec, io):
     if io:
         assert used == io
     io = used
-    small, cap = min(512, io), min(1024, 2 * io)
+    small, cap = min(512, io), min(1536, 3 * io)
     covered = [np.zeros(octs(n), np.int32) for n in sizes]
     packs = []
     for t, c, o0 in items:
@@ -140,9 +140,10 @@ def test_work_items_host_validation():
 
 
 def test_more_packs_than_slices():
-    """250 packs of eight 30-element tensors and one tensor of 40 slices (16-octet items): the packs are spread
-    evenly over the slices, and the launch still takes every octet once."""
+    """167 packs of 30-element tensors (twelve a pack at 16-octet items, the last of eight) and one tensor of 40
+    slices: the packs are spread evenly over the slices, and the launch still takes every octet once."""
     sizes = [30] * 2000 + [5000]
     items, _, _ = check_items(sizes, [True] * len(sizes), 16)
     kinds = ["P" if c > 1 else "S" for _, c, _ in items[::-1]]
-    assert kinds.count("P") == 250 and kinds.count("S") == 40
+    assert kinds.count("P") == 167 and kinds.count("S") == 40
+    assert sorted(c for _, c, _ in items if c > 1) == [8] + [12] * 166
