@@ -222,10 +222,29 @@ __device__ __forceinline__ void adam_vec_octet(const TensorRec& r, int64_t o, co
 
 // Octets [ob, oe) of one tensor: octet ob + lane first, then every `stride`-th. With `prefetch` (a whole CTA on
 // one slice: lane is the thread index and stride the CTA size) thread 0 asks L2 for the rounds one and two ahead,
-// so that the other threads' loads of those rounds find their data in L2 rather than waiting on DRAM.
+// so that the other threads' loads of those rounds find their data in L2 rather than waiting on DRAM, and, at the
+// slice's second-to-last round, for the first round of `nx`, the slice the CTA takes next.
+// The item a CTA takes after the current one, whose first round of octets (when it is a slice) the CTA's thread 0
+// asks L2 for while the CTA works on the current slice's last round, as it does for the current slice's own rounds.
+struct NextSlice {
+    const TensorRec* recs;
+    const WorkItem* item;  // null: none, or no prefetch of the next item
+};
+
+template <Dtype G, Dtype M>
+__device__ __noinline__ void prefetch_next_round(const NextSlice& nx, int32_t round) {
+    const WorkItem it = *nx.item;
+    if (it.count != 1) return;
+    const TensorRec r = nx.recs[it.t];
+    const int64_t full = r.n / kOct;
+    const int64_t oe = it.o0 + round < full ? it.o0 + round : full;
+    if (r.vec && oe > it.o0) prefetch_octets<G, M>(r, it.o0, oe);
+}
+
 template <Dtype G, Dtype M, bool kCoupled, bool kSkip>
 __device__ __forceinline__ void adam_range(const TensorRec& r, int64_t ob, int64_t oe, int lane, int stride,
-                                           const StepScalars& s, Factor& fac, bool prefetch = false) {
+                                           const StepScalars& s, Factor& fac, bool prefetch = false,
+                                           NextSlice nx = NextSlice{nullptr, nullptr}) {
     using L = MomentLayout<M>;
     const int64_t full = r.n / kOct;  // octets with all eight elements
     if (r.vec) {
@@ -234,8 +253,13 @@ __device__ __forceinline__ void adam_range(const TensorRec& r, int64_t ob, int64
         if (prefetch && lane == 0 && ob + round < vend)
             prefetch_octets<G, M>(r, ob + round, ob + 2 * round < vend ? ob + 2 * round : vend);
         for (int64_t o = ob + lane; o < vend; o += round) {
-            if (prefetch && lane == 0 && o + 2 * round < vend)
-                prefetch_octets<G, M>(r, o + 2 * round, o + 3 * round < vend ? o + 3 * round : vend);
+            if (prefetch && lane == 0) {
+                if (o + 2 * round < vend) {
+                    prefetch_octets<G, M>(r, o + 2 * round, o + 3 * round < vend ? o + 3 * round : vend);
+                } else if (nx.item && o + round < vend) {  // the second-to-last round: the next slice's first
+                    prefetch_next_round<G, M>(nx, (int32_t)round);
+                }
+            }
             adam_vec_octet<G, M, kCoupled, kSkip>(r, o, s, fac);
         }
         // the last, partial octet (n % 8 != 0), when it lies in this range
@@ -334,7 +358,8 @@ __device__ __forceinline__ void prefetch_item(const TensorRec* __restrict__ recs
 
 // The items of a persistent grid (or, with no queue, the CTA's one item), the first index already in s_item[0]:
 // taken one at a time from the end of the item array (the norm reads the list forwards, so the gradient it read
-// last may still be in L2), thread 0 taking the next index while the CTA works on the current item. Without
+// last may still be in L2), thread 0 taking the next index while the CTA works on the current item (and, with both
+// moments packed, asking L2 for that item's first round before the current slice ends). Without
 // kGrouped the scalars come straight from s; with it each tensor's group picks its own from gs.
 template <Dtype G, Dtype M, bool kCoupled, bool kSkip, bool kGrouped>
 __device__ __forceinline__ void adamw_item_loop(const TensorRec* __restrict__ recs, const WorkItem* __restrict__ items,
@@ -345,7 +370,15 @@ __device__ __forceinline__ void adamw_item_loop(const TensorRec* __restrict__ re
     const bool persistent = queue != nullptr;
     int32_t cur = 0;
     for (int32_t k = s_item[0]; k < num_items; k = s_item[cur]) {
-        if (threadIdx.x == 0) s_item[cur ^ 1] = persistent ? queue_take(queue) : num_items;
+        NextSlice nx{recs, nullptr};
+        if (threadIdx.x == 0) {
+            const int32_t nk = persistent ? queue_take(queue) : num_items;
+            s_item[cur ^ 1] = nk;
+            // measured on GB300: with both moments packed (160-byte octets) the next slice's first round is asked
+            // for early (GPT-2 small's step 0.465 -> 0.458 ms, GPT-2 XL's 5.41 -> 5.32 ms); with float32 moments
+            // (224-byte octets) the extra data in L2 made the step slower, and with m packed alone it changed nothing
+            if (MomentLayout<M>::kVPacked && nk < num_items) nx.item = items + (num_items - 1 - nk);
+        }
         const WorkItem item = items[num_items - 1 - k];
         if (item.count == 1) {
             const TensorRec r = recs[item.t];
@@ -353,9 +386,9 @@ __device__ __forceinline__ void adamw_item_loop(const TensorRec* __restrict__ re
             const int64_t oe = item.o0 + item_octs < no ? item.o0 + item_octs : no;
             if constexpr (kGrouped) {
                 const StepScalars x = group_scalars<kGrouped>(s, gs, r);
-                adam_range<G, M, kCoupled, kSkip>(r, item.o0, oe, threadIdx.x, kThreads, x, fac, true);
+                adam_range<G, M, kCoupled, kSkip>(r, item.o0, oe, threadIdx.x, kThreads, x, fac, true, nx);
             } else {
-                adam_range<G, M, kCoupled, kSkip>(r, item.o0, oe, threadIdx.x, kThreads, s, fac, true);
+                adam_range<G, M, kCoupled, kSkip>(r, item.o0, oe, threadIdx.x, kThreads, s, fac, true, nx);
             }
         } else {
             adam_pack<G, M, kCoupled, kSkip, kGrouped>(recs, item, pack_pre, s, gs, fac);
