@@ -91,6 +91,12 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.ora_clip_grad_norms.restype = None
     lib.ora_scale_tensors.argtypes = [_P, _I64P, ctypes.c_int32, ctypes.c_int32, ctypes.c_float]
     lib.ora_scale_tensors.restype = None
+    lib.ora_accumulate_grads.argtypes = [_P, _P, _I64P, ctypes.c_int32, ctypes.c_int32]
+    lib.ora_accumulate_grads.restype = None
+    lib.ora_accumulate_clip_grad_norms.argtypes = [_P, _P, _I64P, ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
+                                                   ctypes.c_float, ctypes.POINTER(ctypes.c_float),
+                                                   ctypes.POINTER(ctypes.c_float)]
+    lib.ora_accumulate_clip_grad_norms.restype = None
     return lib
 
 
@@ -274,6 +280,25 @@ class Oracle:
             return
         dt = _gdt(ts[0])
         self.lib.ora_scale_tensors(_ptrs(ts), _sizes([t.size for t in ts]), len(ts), dt, np.float32(factor))
+
+    # ---- the gradient's last write (an add) with the norm of its result ----
+    def accumulate_grads(self, gs, adds) -> None:
+        """gs[k] += adds[k] in place, each sum rounded to the gradients' type."""
+        if not gs:
+            return
+        dt = _gdt(gs[0])
+        assert all(a.dtype == g.dtype and a.size == g.size for g, a in zip(gs, adds))
+        self.lib.ora_accumulate_grads(_ptrs(gs), _ptrs(adds), _sizes([g.size for g in gs]), len(gs), dt)
+
+    def accumulate_clip_grad_norms(self, gs, adds, max_norm: float, inv_scale: float = 1.0):
+        """gs[k] += adds[k], then the joint norm and factor of the result. Returns ``(norm, factor)``."""
+        gdt = _gdt(gs[0]) if gs else F32
+        assert all(a.dtype == g.dtype and a.size == g.size for g, a in zip(gs, adds))
+        norm, factor = ctypes.c_float(), ctypes.c_float()
+        self.lib.ora_accumulate_clip_grad_norms(_ptrs(gs), _ptrs(adds), _sizes([g.size for g in gs]), len(gs), gdt,
+                                                np.float32(max_norm), np.float32(inv_scale), ctypes.byref(norm),
+                                                ctypes.byref(factor))
+        return np.float32(norm.value), np.float32(factor.value)
 
     # ---- the whole hot path ----
     def clip_adamw_step(self, ws, gs, ms, vs, hp: Hyper, max_norm: float, inv_scale: float = 1.0,

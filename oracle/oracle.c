@@ -22,6 +22,9 @@
  *   [SUM]   BendTorch "main.bend", section "Losses over arrays": a running F32 sum of many squares drifts, so the
  *           joint norm here is summed in double over exactly formed squares.
  *   [PREC]  "Precision and numerics", section "bf16 regions": rounding to nearest-even is the one cast.
+ *   [TAPE]  "Mica 7.7", section "Values that stay on the card": the tape walks the recorded steps backwards and
+ *           hands each operand its gradient; an operand read by more than one step gets the sum of what each
+ *           step hands it (the chain rule), so the last write to such a gradient is an element-wise add.
  *
  * Readings where the pages leave a step open (each is listed in the design notes):
  *   - The step's scalars are PyTorch's: every one is computed in double and rounded once to float32 (c1, c2, b2,
@@ -33,6 +36,11 @@
  *     inside the update; the gradient is never rewritten by the clip.
  *   - Parameter groups (PyTorch's param_groups: a list split into groups with their own lr and weight decay, e.g.
  *     no decay on biases and norm gains) step every tensor exactly as a call over its group alone would.
+ *   - A gradient's last write when it has several contributions (a weight read twice, micro-batches summed) is
+ *     g + a rounded once to the gradient's type, as PyTorch's add_ does: float32 cells add in float32; binary16
+ *     cells are widened, added in float32 and rounded back to nearest-even (float32 holds at least 2 * 11 + 2
+ *     significant bits, so this is the correctly rounded binary16 sum). The norm fused into that write is the
+ *     norm of the list after the add.
  *
  * Build with -O2 -ffp-contract=off and without -ffast-math: every float operation below rounds on its own, with no
  * fused multiply-add, exactly in the order written.
@@ -402,6 +410,34 @@ void ora_scale_tensors(void* const* t, const int64_t* n, int32_t T, int32_t dt, 
             }
         }
     }
+}
+
+/* ------------------------------------------------------------------------------------------------------------ */
+/* the gradient's last write, an add, with the joint norm of its result [TAPE], [MICA], [SUM]                      */
+/* ------------------------------------------------------------------------------------------------------------ */
+
+/* Every cell of every listed gradient plus the same cell of its addend, in place. */
+void ora_accumulate_grads(void* const* g, const void* const* a, const int64_t* n, int32_t T, int32_t gdt) {
+    for (int32_t k = 0; k < T; ++k) {
+        for (int64_t i = 0; i < n[k]; ++i) {
+            if (gdt == ORA_F16) {
+                uint16_t* p = (uint16_t*)g[k];
+                const uint16_t* q = (const uint16_t*)a[k];
+                p[i] = ora_f16_from_f32(ora_f32_from_f16(p[i]) + ora_f32_from_f16(q[i]));
+            } else {
+                float* p = (float*)g[k];
+                const float* q = (const float*)a[k];
+                p[i] = p[i] + q[i];
+            }
+        }
+    }
+}
+
+/* The add, then ClipGradNorms over the list it leaves: what one pass over g and a computes. */
+void ora_accumulate_clip_grad_norms(void* const* g, const void* const* a, const int64_t* n, int32_t T, int32_t gdt,
+                                    float max_norm, float inv_scale, float* norm_out, float* factor_out) {
+    ora_accumulate_grads(g, a, n, T, gdt);
+    ora_clip_grad_norms((const void* const*)g, n, T, gdt, max_norm, inv_scale, norm_out, factor_out, 0);
 }
 
 /* The whole step of the hot path: the joint norm and its factor, then AdamW over every group. */

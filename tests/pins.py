@@ -8,7 +8,8 @@ What the pins hold the oracle to (no pin re-types the oracle's own formula):
 
 * library routines: PyTorch's CPU ``torch.optim.AdamW`` / ``torch.optim.Adam`` (also with two param_groups),
   ``torch.optim.SGD`` (plain and with momentum), ``GradScaler`` and ``clip_grad_norm_``, PyTorch's
-  float32 -> bfloat16 conversion, numpy's binary16 conversions, Python's exactly rounded ``math.fsum``;
+  float32 -> bfloat16 conversion, numpy's binary16 conversions and float32 add, Python's exactly rounded
+  ``math.fsum``;
 * closed forms: the first step from zero moments, a constant gradient over many steps (also for SGD and momentum in
   dyadic values, where every operation is exact), norms of all-ones and Pythagorean vectors, and the b1 = b2 = eps = 0 step whose weight update is lr * m / sqrt(v) of rounded moments;
 * the pages' printed values (``tests/golden/printed_values.txt``): the F32 rounding of 1 - 0.999 and the BF16 codes
@@ -421,6 +422,47 @@ def pin_scale_tensors(o: oracle.Oracle) -> None:
         np.testing.assert_array_equal(a.view(np.uint16), b.view(np.uint16))
 
 
+def pin_accumulate(o: oracle.Oracle) -> None:
+    """The gradient's last write, g + a rounded once to the gradient's type: float32 cells against numpy's float32
+    add (random bit patterns and the edge cases: zeros, infinities, NaNs, subnormals, the largest values);
+    binary16 cells against the exact sum (exact in float64 for two binary16 values) rounded to binary16 by numpy's
+    float64 -> float16 conversion, on random bit-pattern pairs and on every pair of a set of edge values."""
+    rng = _rng(31)
+    x = edge_f32_bits(rng, 1 << 16).view(np.float32)
+    y = rng.permutation(edge_f32_bits(rng, 1 << 16)).view(np.float32)[: x.size]
+    g, a = [x.copy(), x[:7].copy()], [y.copy(), y[:7].copy()]
+    o.accumulate_grads(g, a)
+    with np.errstate(over="ignore", invalid="ignore"):
+        want = x + y
+    for got, w in ((g[0], want), (g[1], want[:7])):
+        nan = np.isnan(w)
+        np.testing.assert_array_equal(got.view(np.uint32)[~nan], w.view(np.uint32)[~nan])
+        assert np.isnan(got[nan]).all()
+    edge16 = np.array([0x0000, 0x8000, 0x0001, 0x8001, 0x03FF, 0x0400, 0x3C00, 0xBC00, 0x3C01, 0x7BFF, 0xFBFF,
+                       0x7C00, 0xFC00, 0x7E00, 0x5800, 0x1400, 0x6BFF, 0xEBFF, 0x0200], np.uint16)
+    ex, ey = np.meshgrid(edge16, edge16)
+    hx = np.concatenate([rng.integers(0, 1 << 16, size=1 << 18).astype(np.uint16), ex.ravel()])
+    hy = np.concatenate([rng.integers(0, 1 << 16, size=1 << 18).astype(np.uint16), ey.ravel()])
+    g16, a16 = [hx.view(np.float16).copy()], [hy.view(np.float16).copy()]
+    o.accumulate_grads(g16, a16)
+    with np.errstate(over="ignore", invalid="ignore"):
+        exact = hx.view(np.float16).astype(np.float64) + hy.view(np.float16).astype(np.float64)
+        want16 = exact.astype(np.float16)
+    nan = np.isnan(exact)
+    np.testing.assert_array_equal(g16[0].view(np.uint16)[~nan], want16.view(np.uint16)[~nan])
+    assert np.isnan(g16[0][nan]).all()
+    # the norm fused into the write is that of the list the add leaves
+    grads = [rng.normal(0, 1e-3, size=n).astype(np.float32) for n in (50_000, 3)]
+    adds = [rng.normal(0, 1e-3, size=gr.size).astype(np.float32) for gr in grads]
+    sums = [gr + ad for gr, ad in zip(grads, adds)]
+    norm, factor = o.accumulate_clip_grad_norms(grads, adds, 0.01)
+    for gr, sm in zip(grads, sums):
+        np.testing.assert_array_equal(gr, sm)
+    ref = math.sqrt(_exact_sumsq(sums, 1.0))
+    assert abs(float(norm) - ref) <= f32_ulp(np.float32(ref)), (norm, ref)
+    assert factor == np.float32(np.float32(0.01) / (norm + np.float32(1e-6)))
+
+
 def pin_packed_m_float_v(o: oracle.Oracle) -> None:
     """m packed, v float32 (the page's CAdamWBF16 with v16 false). With b1 = b2 = eps = 0 and t = 1, m = bf16(g)
     and v = g*g unrounded, so the weight moves by exactly lr * bf16(g) / sqrt(g*g) (PyTorch's bfloat16 rounding
@@ -710,5 +752,5 @@ ALL_PINS = [
     pin_packed_reads_rounded_moments, pin_odd_tail_untouched, pin_zero_grad, pin_list_equals_groups,
     pin_scale_tensors, pin_printed_beta_rounding, pin_packed_m_float_v, pin_skip_nonfinite_vs_gradscaler,
     pin_torch_adamw_param_groups, pin_torch_sgd, pin_sgd_dyadic_closed_form, pin_sgd_skip_vs_gradscaler,
-    pin_adamw_op_order,
+    pin_adamw_op_order, pin_accumulate,
 ]

@@ -74,6 +74,13 @@ MUTATIONS = {
                     "s->step = (float)lr / (float)(1.0 - pow(b1, tt));"),
     "bc2_in_f32": ("s->bc2 = (float)sqrt(1.0 - pow(b2, tt));", "s->bc2 = sqrtf((float)(1.0 - pow(b2, tt)));"),
     "decay_in_f32": ("s->dec = (float)(1.0 - lr * wd);", "s->dec = 1.0f - (float)lr * (float)wd;"),
+    # the gradient's last write (an add) and the norm fused into it
+    "accumulate_f16_rounds_down": ("p[i] = ora_f16_from_f32(ora_f32_from_f16(p[i]) + ora_f32_from_f16(q[i]));",
+                                   "p[i] = ora_f16_from_f32(nextafterf(ora_f32_from_f16(p[i]) + ora_f32_from_f16(q[i]), 0.0f));"),
+    "accumulate_f32_ignores_addend": ("p[i] = p[i] + q[i];", "p[i] = p[i];"),
+    "accumulate_subtracts": ("p[i] = p[i] + q[i];", "p[i] = p[i] - q[i];"),
+    "accumulate_norm_before_add": ("    ora_accumulate_grads(g, a, n, T, gdt);\n    ora_clip_grad_norms((const void* const*)g, n, T, gdt, max_norm, inv_scale, norm_out, factor_out, 0);",
+                                   "    ora_clip_grad_norms((const void* const*)g, n, T, gdt, max_norm, inv_scale, norm_out, factor_out, 0);\n    ora_accumulate_grads(g, a, n, T, gdt);"),
     "odd_tail_clobbered": ("if (i & 1) return (word & 0x0000FFFFu) | ((uint32_t)h << 16);\n    return (word & 0xFFFF0000u) | (uint32_t)h;",
                            "if (i & 1) return (word & 0x0000FFFFu) | ((uint32_t)h << 16);\n    return (uint32_t)h;"),
 }
