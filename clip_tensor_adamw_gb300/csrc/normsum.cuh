@@ -219,6 +219,7 @@ __device__ __forceinline__ double share_total(const SumSq& acc, const ChunkTable
 // [lo[i], lo[i + 1]), its gradient starts at base[i] and has n[i] elements, vec[i] says whether it is aligned for
 // the vector loads.
 constexpr int kStaged = 256;
+static_assert((kThreads & (kThreads - 1)) == 0, "a thread's octets are found with a mask of kThreads - 1");
 struct StagedSpan {
     int64_t lo[kStaged + 1];
     const char* base[kStaged];
@@ -314,9 +315,11 @@ __device__ __forceinline__ void widen_octet(const RawOctet<G>& r, float (&x)[8])
 // This thread's share of the sum of squares of chunk b of `grid` equal contiguous chunks of the list's octets, for
 // lists of many small tensors, where a stage of the TMA pipeline would cross several tensors: the CTA streams the
 // chunk straight into registers, staging the chunk's tensors (their octet ranges, bases, sizes) in `sp` up to
-// kStaged at a time; thread t takes the staged span's octets c + t, c + t + 256, ..., four at a time (eight for
-// binary16), all their loads in flight before any is widened and summed, finding each octet's tensor by walking the
-// staged table forwards. Every thread of the CTA calls it (it meets the others at barriers).
+// kStaged at a time; thread t takes the chunk's octets c0 + t, c0 + t + 256, ... (in every staged span, those of
+// them that lie in it: the same octets that its double-precision re-sum in share_total takes, however many spans
+// the chunk has), four at a time (eight for binary16), all their loads in flight before any is widened and summed,
+// finding each octet's tensor by walking the staged table forwards. Every thread of the CTA calls it (it meets the
+// others at barriers).
 template <Dtype G, int kMode, bool kKeepL2 = false>
 __device__ __forceinline__ double direct_chunk_share(const ChunkTable& ct, int32_t b, int32_t grid, float inv_scale,
                                                      StagedSpan& sp) {
@@ -343,7 +346,9 @@ __device__ __forceinline__ double direct_chunk_share(const ChunkTable& ct, int32
         const int64_t oe = sp.lo[cnt] < c1 ? sp.lo[cnt] : c1;
         int32_t j = 0;
         constexpr int U = (G == kF16) ? 8 : 4;  // octets in flight per thread (a binary16 octet is 4 registers)
-        for (int64_t o = ob + t; o < oe; o += U * kThreads) {
+        // this thread's first octet of the span: the first at or after ob that is c0 + t plus a multiple of 256
+        const int64_t first = ob + ((t - (int32_t)((ob - c0) & (kThreads - 1))) & (kThreads - 1));
+        for (int64_t o = first; o < oe; o += U * kThreads) {
             RawOctet<G> raw[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {

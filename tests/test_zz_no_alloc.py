@@ -172,3 +172,22 @@ def test_noalloc_after_release_cache():
     b = _call(fn, st.g, wl.max_norm, wl.inv_scale, 1)
     torch.cuda.synchronize()
     assert _bits(a[0]) == _bits(b[0]) and _bits(a[1]) == _bits(b[1])
+
+
+@pytest.mark.parametrize("values,at", [([float("inf")], [64]), ([1e30, -3e25], [64, 130])], ids=["inf", "two_huge"])
+def test_noalloc_norm_over_many_staged_spans(ora, values, at):
+    """The list of 4,096 tensors whose register-norm chunks span four staged runs of 256 tensors each, a value that
+    the float32 pairs cannot hold planted in a later span (see test_gpu_norm_spans.py): the same norm as the oracle
+    and the same bits as the allocating entry point."""
+    from test_gpu_norm_spans import spanning_list
+    host, dev, _ = spanning_list(values, at)
+    o_norm, o_factor, _ = ora.clip_grad_norms(host, 1.0)
+    norm, factor = _call(_noalloc(), dev, 1.0, 1.0, 0)
+    a_norm, a_factor = mica.mica_clip_grad_norms(dev, 1.0, 1.0)
+    torch.cuda.synchronize()
+    assert _bits(norm) == _bits(a_norm) and _bits(factor) == _bits(a_factor)
+    if np.isinf(o_norm):
+        assert np.isinf(norm.item()) and factor.item() == 0.0
+    else:
+        assert abs(norm.item() - float(o_norm)) <= NORM_RTOL * float(o_norm)
+        assert np.float32(factor.item()).view(np.uint32) == o_factor.view(np.uint32)
