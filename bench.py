@@ -64,8 +64,11 @@ def adamw_bytes_per_param(wl: workloads.Workload, zero_grad: bool = False, opt: 
 
 def step_bytes_per_param(wl: workloads.Workload, zero_grad: bool = False, opt: str = "adamw") -> float:
     """The whole step: the norm's read of g plus the update kernel (AdamW: 28 / 20 B + 4 B with float32
-    gradients)."""
+    gradients). With opt "accumulate" the norm is fused into the gradient's last write, g += a: that kernel reads
+    g and a and writes g (12 B with float32 gradients), and the norm reads nothing more."""
     g = 2.0 if wl.grad_dtype == "f16" else 4.0
+    if opt == "accumulate":
+        return 3 * g + adamw_bytes_per_param(wl, zero_grad, "adamw")
     return g + adamw_bytes_per_param(wl, zero_grad, opt)
 
 
@@ -316,7 +319,8 @@ def extra_steps(est_ms_per_step: float) -> int:
 def measure(wl: workloads.Workload, steps: int, warmup: int, zero_grad: bool, dist=None, sampler=None,
             coupled_l2: bool = False, opt: str = "adamw", per_kernel: bool = True):
     """Times `steps` steps of the whole hot path on the device (inputs resident): the norm and clip factor, then the
-    update (``opt``: "adamw", "adamw_groups", "sgd" or "momentum"). Returns a dict of figures."""
+    update (``opt``: "adamw", "adamw_groups", "sgd" or "momentum"; "accumulate": each step first adds a second
+    gradient contribution into g with the norm fused into that add, then AdamW). Returns a dict of figures."""
     import clip_tensor_adamw_gb300 as mica
     st = workloads.make_state(wl, "cuda")
     workloads.fill_grad(st, 1)
@@ -346,6 +350,12 @@ def measure(wl: workloads.Workload, steps: int, warmup: int, zero_grad: bool, di
     else:
         def update(t):
             mica.mica_adamw_steps(W, G, M, V, step=t, **kw)
+    if opt == "accumulate":  # a second contribution to every gradient, laid out as g
+        a_flat = torch.empty_like(st.g_flat)
+        a_flat.normal_(0.0, wl.g_std, generator=torch.Generator(device="cuda").manual_seed(wl.seed + 1))
+        es = st.g_flat.element_size()
+        A = mica.TensorList([a_flat.narrow(0, (x.data_ptr() - st.g_flat.data_ptr()) // es, x.numel())
+                             if x.numel() else a_flat[:0] for x in st.g])
 
     step_kw = dict(max_norm=wl.max_norm, inv_scale=wl.inv_scale, lr=wl.lr, beta1=wl.beta1, beta2=wl.beta2, eps=wl.eps,
                    weight_decay=wl.weight_decay, zero_grad=zero_grad, norm_out=norm, factor_out=factor,
@@ -355,7 +365,10 @@ def measure(wl: workloads.Workload, steps: int, warmup: int, zero_grad: bool, di
         if ev_mid is None and opt == "adamw":  # the whole step through the one-step entry point
             mica.mica_clip_adamw_step(W, G, M, V, step=t, **step_kw)
             return
-        mica.mica_clip_grad_norms(G, wl.max_norm, wl.inv_scale, norm_out=norm, factor_out=factor)
+        if opt == "accumulate":
+            mica.mica_accumulate_clip_grad_norms(G, A, wl.max_norm, wl.inv_scale, norm_out=norm, factor_out=factor)
+        else:
+            mica.mica_clip_grad_norms(G, wl.max_norm, wl.inv_scale, norm_out=norm, factor_out=factor)
         if ev_mid is not None:
             ev_mid.record(stream)
         update(t)
@@ -397,6 +410,8 @@ def measure(wl: workloads.Workload, steps: int, warmup: int, zero_grad: bool, di
            "adamw_ms": statistics.mean(adamw_ms), "clip_ms": statistics.mean(clip_ms), "launches": launches,
            "t_wall": (t_wall0, t_wall1), "norm": float(norm.item())}
     mica.mica_sync()
+    if opt == "accumulate":
+        del A, a_flat
     del st, W, G, M, V
     mica.mica_release_cache()  # the list's tables go with its tensors
     torch.cuda.empty_cache()
@@ -622,6 +637,7 @@ def main():
                     False, "adamw", None),
                    ("gpt2_small_adam_l2", small, True, "adamw", None),
                    ("gpt2_small_param_groups", small, False, "adamw_groups", None),
+                   ("gpt2_small_accumulate", small, False, "accumulate", None),
                    ("gpt2_small_sgd", small, False, "sgd", None),
                    ("gpt2_small_sgd_momentum", small, False, "momentum", None)]
         for other, owl, coupled, opt, fused in others:
@@ -650,6 +666,13 @@ def main():
                                           "launch_ms": f["adamw_ms"]}}
             if fused is not None:
                 extras[other]["path"] = "one cooperative launch (MICA_FUSED=1)"
+            if opt == "accumulate":  # the add + norm kernel: reads g and a, writes g
+                abpp = 3 * (2.0 if owl.grad_dtype == "f16" else 4.0)
+                extras[other]["path"] = "g += a with the norm fused into the add, then AdamWSteps"
+                extras[other]["accumulate_kernel"] = {
+                    "kernel": "accumulate_norm_kernel", "launch_ms": f["clip_ms"], "bytes_per_param": abpp,
+                    "achieved": owl.params * abpp / f["clip_ms"] / 1e6, "peak": peak, "unit": "GB/s",
+                    "frac": owl.params * abpp / f["clip_ms"] / 1e6 / peak, "peak_source": peak_src}
             if other == "gpt2_xl":
                 ms, h2d, d2h = measure_e2e(owl, 10, args.warmup)
                 extras[other]["e2e"] = {"value": owl.params / (ms / 1e3), "unit": "params/s", "ms_per_step": ms,

@@ -15,7 +15,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmica_optim.so")
-SOURCES = ["adamw.cu", "fused.cu", "norm.cu", "sgd.cu", "scale.cu", "api.cpp", "noalloc.cu"]
+SOURCES = ["adamw.cu", "fused.cu", "norm.cu", "accnorm.cu", "sgd.cu", "scale.cu", "api.cpp", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")
 CFLAGS = [*ARCH, "-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC,-O2,-fvisibility=hidden",

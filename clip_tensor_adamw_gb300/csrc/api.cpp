@@ -141,7 +141,7 @@ struct Span {
 };
 
 static const char* span_name(int32_t kind) {
-    static const char* names[] = {"w", "g", "m", "v", "t", "buf"};
+    static const char* names[] = {"w", "g", "m", "v", "t", "buf", "a"};
     return names[kind];
 }
 
@@ -167,7 +167,7 @@ static bool overlaps_any(const std::vector<Span>& sorted, const void* p, size_t 
 // per-list device tables
 // ------------------------------------------------------------------------------------------------------------------
 
-enum Kind : uint64_t { kAdamW = 1, kNorm = 2, kScale = 3, kSGD = 4, kMomentum = 5 };
+enum Kind : uint64_t { kAdamW = 1, kNorm = 2, kScale = 3, kSGD = 4, kMomentum = 5, kAccNorm = 6 };
 
 struct Plan {
     // the list it was built for (compared in full on every lookup)
@@ -354,7 +354,7 @@ struct ListDesc {
     const int64_t* n;
     float* const* w;     // adamw: weights; scale: the tensors
     void* const* g;      // adamw, norm
-    void* const* m;      // adamw
+    void* const* m;      // adamw; accumulate: the addends
     void* const* v;      // adamw
     Dtype gdt, mdt;      // scale: gdt is the tensors' type
     const int32_t* group = nullptr;  // AdamW over parameter groups: T group indices (validated by the caller)
@@ -370,6 +370,11 @@ static int list_arrays(const ListDesc& L, const void* const* out[4]) {
     if (L.kind == kNorm) {
         out[0] = L.g;
         return 1;
+    }
+    if (L.kind == kAccNorm) {
+        out[0] = L.g;
+        out[1] = L.m;  // the addends
+        return 2;
     }
     if (L.kind == kSGD || L.kind == kMomentum) {
         out[0] = reinterpret_cast<const void* const*>(L.w);
@@ -463,7 +468,12 @@ static mica_status build_plan(const ListDesc& L, int device, uint64_t h, Plan** 
         r.g = L.g[k];
         spans.push_back({(uintptr_t)ptr_u(r.g), (uintptr_t)(ptr_u(r.g) + gb), 1, k});
         bool vec = (ptr_u(r.g) % (L.gdt == kF16 ? 16 : 32)) == 0;
-        if (L.kind == kAdamW) {
+        if (L.kind == kAccNorm) {
+            if ((s = check_device_span(L.m[k], gb, elem_bytes(L.gdt), device, "a", k)) != MICA_OK) return s;
+            r.m = L.m[k];
+            spans.push_back({(uintptr_t)ptr_u(r.m), (uintptr_t)(ptr_u(r.m) + gb), 6, k});
+            vec = vec && (ptr_u(r.m) % (L.gdt == kF16 ? 16 : 32)) == 0;
+        } else if (L.kind == kAdamW) {
             const size_t wb = (size_t)n * 4;
             const size_t packed_b = (size_t)((n + 1) / 2) * 4, f32_b = (size_t)n * 4;
             const size_t mb = (L.mdt == kBF16x2 || L.mdt == kBF16x2M) ? packed_b : f32_b;
@@ -510,14 +520,17 @@ static mica_status build_plan(const ListDesc& L, int device, uint64_t h, Plan** 
     std::vector<int32_t> first;
     int64_t nonempty = 0;
     for (int32_t k = 0; k < L.T; ++k) nonempty += L.n[k] > 0;
-    const bool chunked = L.kind == kNorm;
+    const bool chunked = L.kind == kNorm || L.kind == kAccNorm;
     if (chunked) {
-        // contiguous equal chunks (see choose_norm_shape)
+        // contiguous equal chunks (see choose_norm_shape; the accumulating norm: the register-streaming layout)
         prefix.resize((size_t)L.T + 1);
         prefix[0] = 0;
         for (int32_t k = 0; k < L.T; ++k) prefix[k + 1] = prefix[k] + (L.n[k] + kOct - 1) / kOct;
-        int32_t grid = 1, direct = 0;
-        choose_norm_shape(total_octs, nonempty, L.gdt == kF16 ? 16 : 32, sms, INT32_MAX, &grid, &direct);
+        int32_t grid = 1, direct = 1;
+        if (L.kind == kNorm)
+            choose_norm_shape(total_octs, nonempty, L.gdt == kF16 ? 16 : 32, sms, INT32_MAX, &grid, &direct);
+        else
+            grid = choose_accumulate_grid(total_octs, L.gdt == kF16 ? 16 : 32, sms);
         plan->chunks.direct = direct;
         first.resize((size_t)grid);
         for (int32_t b = 0; b < grid; ++b) {
@@ -548,11 +561,11 @@ static mica_status build_plan(const ListDesc& L, int device, uint64_t h, Plan** 
     const size_t first_off = up(prefix_off + prefix_b);
     const size_t first_b = first.size() * sizeof(int32_t);
     const size_t part_off = up(first_off + first_b);
-    const size_t part_b = (L.kind == kNorm) ? first.size() * sizeof(double) : 0;
+    const size_t part_b = chunked ? first.size() * sizeof(double) : 0;
     const size_t ticket_off = up(part_off + part_b);
-    const size_t ticket_b = (L.kind == kNorm) ? 256 : 0;
+    const size_t ticket_b = chunked ? 256 : 0;
     const size_t queue_off = up(ticket_off + ticket_b);
-    const size_t queue_b = (L.kind == kNorm || L.kind == kScale) ? 0 : kQueues * 2 * sizeof(unsigned int);
+    const size_t queue_b = (chunked || L.kind == kScale) ? 0 : kQueues * 2 * sizeof(unsigned int);
     const size_t total = queue_off + queue_b;
     cudaError_t e = cudaMalloc(&plan->dev, std::max<size_t>(total, 256));
     if (e != cudaSuccess) {
@@ -570,7 +583,7 @@ static mica_status build_plan(const ListDesc& L, int device, uint64_t h, Plan** 
         plan->chunks.prefix = reinterpret_cast<const int64_t*>(base + prefix_off);
         plan->chunks.first = reinterpret_cast<const int32_t*>(base + first_off);
     }
-    if (L.kind == kNorm) {
+    if (chunked) {
         plan->partials = reinterpret_cast<double*>(base + part_off);
         plan->ticket = reinterpret_cast<unsigned int*>(base + ticket_off);
     }
@@ -822,6 +835,37 @@ extern "C" mica_status mica_clip_grad_norms(const void* const* g, const int64_t*
     return after_launch(launch_norm(p->chunks, (Dtype)gdt, inv_scale, p->partials, p->ticket, max_norm, d_norm,
                                     d_factor, nullptr, keep_l2, stream),
                         stream, "ClipGradNorms launch");
+}
+
+extern "C" mica_status mica_accumulate_clip_grad_norms(void* const* g, const void* const* a, const int64_t* n,
+                                                       int32_t T, mica_dtype gdt, float max_norm, float inv_scale,
+                                                       float* d_norm, float* d_factor, void* stream) {
+    if (gdt != MICA_F32 && gdt != MICA_F16) return fail(MICA_ERR_DTYPE, "gradients must be float32 or float16");
+    if (!d_factor) return fail(MICA_ERR_NULL, "d_factor is NULL");
+    if (std::isnan(max_norm) || !(max_norm > 0.0f))
+        return fail(MICA_ERR_HYPER, "max_norm %g is not > 0", (double)max_norm);
+    if (!std::isfinite(inv_scale) || !(inv_scale > 0.0f))
+        return fail(MICA_ERR_HYPER, "inv_scale %g is not finite and > 0", (double)inv_scale);
+    if (T < 0 || T > MICA_MAX_TENSORS) return fail(MICA_ERR_COUNT, "T = %d is outside [0, %d]", T, MICA_MAX_TENSORS);
+    if (T > 0 && (!g || !a || !n)) return fail(MICA_ERR_NULL, "a pointer array is NULL");
+    mica_status s;
+    int dev = 0;
+    ListDesc L{kAccNorm, T, n, nullptr, g, const_cast<void* const*>(reinterpret_cast<const void* const*>(a)),
+               nullptr, (Dtype)gdt, kF32};
+    Plan* p = nullptr;
+    if (T > 0 && current_device(&dev) == MICA_OK) p = cached_plan(L, dev);
+    if (!p) {
+        int64_t total = 0;
+        if ((s = check_list(T, n, {reinterpret_cast<const void* const*>(g), a}, &total)) != MICA_OK) return s;
+        if ((s = current_device(&dev)) != MICA_OK) return s;
+        if (total == 0) L.T = 0;  // an empty list still gets its norm (0) and factor written
+        if ((s = get_plan(L, dev, &p, stream)) != MICA_OK) return s;
+    }
+    if ((s = check_scalars(p, dev, d_factor, d_norm, "a gradient or an addend")) != MICA_OK) return s;
+    const bool keep_l2 = p->total * (int64_t)elem_bytes((Dtype)gdt) <= kKeepL2MaxGradBytes;
+    return after_launch(launch_accumulate_norm(p->chunks, (Dtype)gdt, inv_scale, p->partials, p->ticket, max_norm,
+                                               d_norm, d_factor, keep_l2, stream),
+                        stream, "AccumulateClipGradNorms launch");
 }
 
 extern "C" mica_status mica_grad_sumsq(const void* const* g, const int64_t* n, int32_t T, mica_dtype gdt,
@@ -1189,4 +1233,4 @@ extern "C" mica_status mica_work_items(const int64_t* n, const int32_t* vec, int
     return ok();
 }
 
-extern "C" int32_t mica_abi_version(void) { return 4; }
+extern "C" int32_t mica_abi_version(void) { return 5; }

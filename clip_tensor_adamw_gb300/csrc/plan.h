@@ -167,6 +167,28 @@ constexpr int64_t kKeepL2MaxGradBytes = (int64_t)96 << 20;
 int launch_scale(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_octs, Dtype dt,
                  float factor, const float* d_factor, void* stream);
 
+// The gradient's last write fused with the norm (accnorm.cu): for every tensor k of ct, g += a (g in recs[k].g, the
+// addend in recs[k].m, each sum rounded to the gradient's type), and the joint norm and factor of the result, as
+// launch_norm computes them (one partial per CTA into `partials`, the CTA that finishes last writing d_norm when not
+// null and d_factor). ct is laid out as for the register-streaming norm, with ct.grid CTAs from
+// choose_accumulate_grid. keep_l2: the new gradient's stores carry an evict-last L2 policy (for gradients that fit
+// in L2, which the update reads next).
+int launch_accumulate_norm(const ChunkTable& ct, Dtype gdt, float inv_scale, double* partials, unsigned int* ticket,
+                           float max_norm, float* d_norm, float* d_factor, bool keep_l2, void* stream);
+constexpr int kAccCtasPerSm = 4;
+// kAccCtasPerSm CTAs per SM in one wave per 192 KB of gradient that a CTA of a single wave would take, from 2 to 8
+// waves (measured on GB300: the loss-scaled list's 76 MB best in 2 waves, GPT-2 small's 498 MB in 4, GPT-2 XL's
+// 6.2 GB in 8), no more than one CTA per 256 octets and at least one. `oct_bytes`: one gradient octet's bytes.
+constexpr int64_t kAccWaveBytes = 192 * 1024;
+inline int32_t choose_accumulate_grid(int64_t total_octs, int oct_bytes, int sms) {
+    const int64_t wave = (int64_t)kAccCtasPerSm * (sms > 0 ? sms : 1);
+    int64_t waves = total_octs * oct_bytes / wave / kAccWaveBytes;
+    waves = waves < 2 ? 2 : (waves > 8 ? 8 : waves);
+    const int64_t g = wave * waves;
+    const int64_t want = total_octs > 256 ? (total_octs + 255) / 256 : 1;
+    return (int32_t)(g < want ? g : want);
+}
+
 // The norm and the AdamW update in one cooperative launch of ct.grid CTAs (fused.cu): CTA b sums the squares of
 // chunk b of ct (the register-streaming layout, ct.first holding ct.grid entries) into partials[b]; the CTAs meet
 // at a bounded grid-wide wait on `bar` (two words, zero before the first launch, left ready by each); every CTA then

@@ -70,10 +70,12 @@ def lib() -> ctypes.CDLL:
         L.mica_clip_adamw_step.argtypes = [_P, _P, _P, _P, _I64P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                            ctypes.POINTER(_HP), ctypes.c_float, ctypes.c_float, _P, _P, _P]
         L.mica_grad_sumsq.argtypes = [_P, _I64P, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, _P, _P]
+        L.mica_accumulate_clip_grad_norms.argtypes = [_P, _P, _I64P, ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
+                                                      ctypes.c_float, _P, _P, _P]
         L.mica_clip_factor_from_sumsq.argtypes = [_P, ctypes.c_int32, ctypes.c_float, ctypes.c_float, _P, _P, _P]
         for f in ("mica_scale_tensors", "mica_clip_grad_norms", "mica_adamw_steps", "mica_adamw_steps_grouped",
                   "mica_sgd_steps", "mica_clip_adamw_step", "mica_grad_sumsq", "mica_clip_factor_from_sumsq",
-                  "mica_sync", "mica_release_cache"):
+                  "mica_accumulate_clip_grad_norms", "mica_sync", "mica_release_cache"):
             getattr(L, f).restype = ctypes.c_int
         for f in ("mica_selftest_wait_timeout", "mica_selftest_grid_wait_timeout"):
             getattr(L, f).argtypes = [ctypes.c_uint32, _P]
@@ -118,6 +120,7 @@ class TensorList:
         counts = [t.numel() for t in self.tensors] if sizes is None else list(sizes)
         self.n = (ctypes.c_int64 * max(T, 1))(*counts)
         self.counts = counts
+        self.total = sum(counts)
 
 
 def _as_list(x, sizes=None) -> TensorList:
@@ -166,6 +169,29 @@ def mica_clip_grad_norms(grads, max_norm: float, inv_scale: float = 1.0, norm_ou
     gdt = _dtype_code(L.tensors[0] if L.T else None, "grads")
     _check(lib().mica_clip_grad_norms(L.ptrs, L.n, L.T, gdt, float(max_norm), float(inv_scale), _ptr(norm_out),
                                       _ptr(factor_out), _stream(stream)))
+    return norm_out, factor_out
+
+
+def mica_accumulate_clip_grad_norms(grads, addends, max_norm: float, inv_scale: float = 1.0,
+                                    norm_out: torch.Tensor | None = None, factor_out: torch.Tensor | None = None,
+                                    stream=None):
+    """The gradients' last write as an add, fused with ClipGradNorms: ``grads[k] += addends[k]`` in place (each sum
+    rounded to the gradients' type), then the joint norm and clip factor of the result, in one pass over the list.
+    Returns the device (norm, factor) as ``mica_clip_grad_norms`` does."""
+    G = _as_list(grads)
+    A = _as_list(addends)
+    if A.T != G.T or A.total != G.total:  # the call passes the gradients' counts for both lists
+        raise ValueError("addends must match the gradients tensor for tensor")
+    if G.T and A.tensors[0].dtype != G.tensors[0].dtype:
+        raise TypeError("addends must have the gradients' dtype")
+    dev = G.tensors[0].device if G.T else torch.device("cuda", torch.cuda.current_device())
+    if norm_out is None:
+        norm_out = torch.empty(1, dtype=torch.float32, device=dev)
+    if factor_out is None:
+        factor_out = torch.empty(1, dtype=torch.float32, device=dev)
+    gdt = _dtype_code(G.tensors[0] if G.T else None, "grads")
+    _check(lib().mica_accumulate_clip_grad_norms(G.ptrs, A.ptrs, G.n, G.T, gdt, float(max_norm), float(inv_scale),
+                                                 _ptr(norm_out), _ptr(factor_out), _stream(stream)))
     return norm_out, factor_out
 
 

@@ -17,6 +17,9 @@
  *                             their own lr and weight decay, still one launch.
  *   mica_sgd_steps            SGD, and SGD with momentum, over every (w, g[, buf]) group in one launch.
  *
+ * and mica_accumulate_clip_grad_norms, ClipGradNorms fused into the gradient's last write when that write is an
+ * add (a gradient with several contributions), so that the norm reads no gradient a second time.
+ *
  * The per-element arithmetic is BendTorch "main.bend", section "Optimizers" (AdamW in PyTorch's order of operations;
  * the part "AdamW over packed BF16 moments (CAdamWBF16)" for packed moments), with PyTorch's scalars:
  *   step = lr / (1 - beta1^t), bc2 = sqrt(1 - beta2^t), decay w *= 1 - lr*wd,
@@ -134,6 +137,29 @@ MICA_API mica_status mica_scale_tensors(void* const* t, const int64_t* n, int32_
  */
 MICA_API mica_status mica_clip_grad_norms(const void* const* g, const int64_t* n, int32_t T, mica_dtype gdt, float max_norm,
                                  float inv_scale, float* d_norm, float* d_factor, void* stream);
+
+/*
+ * AccumulateClipGradNorms: a gradient's last write, when it has several contributions, fused with ClipGradNorms.
+ * An operand that several recorded steps read gets the sum of what each hands it ("Mica 7.7 ...", section "Values
+ * that stay on the card": the tape walks the steps backwards and hands each operand its gradient), so the last
+ * write to such a gradient (a weight read twice, or micro-batches summed) is an add; this call makes that add and
+ * measures the joint norm of the result in one pass, so the norm costs no second read of the gradient.
+ * For every tensor k and element i < n[k]:
+ *   g[k][i] = g[k][i] + a[k][i], in place, rounded once to the gradient type: float32 cells add in float32;
+ *             float16 cells are widened, added in float32 and rounded back to nearest-even (the correctly rounded
+ *             float16 sum); a NaN sum is stored as a NaN (payload unspecified);
+ * then *d_norm and *d_factor exactly as mica_clip_grad_norms computes them over the updated g (same sums, same
+ * rounding, same handling of NaN and infinity). a[k] is only read. gdt (MICA_F32 or MICA_F16) is the type of both.
+ * Layout and ownership as mica_clip_grad_norms; every g[k] and a[k] must be disjoint from every other buffer of
+ * the call (MICA_ERR_OVERLAP otherwise, also when d_norm or d_factor lies inside one). Like the norm, it allocates
+ * one device table per distinct list (g, a and n), kept until mica_release_cache().
+ * Sources: "Mica 7.7 ...", sections "The whole model in one call" (ClipGradNorms) and "Values that stay on the
+ * card" (the tape).
+ * Errors: NULL / COUNT / DTYPE / HYPER / ADDRESS / OVERLAP / DEVICE / CUDA / NOMEM.
+ */
+MICA_API mica_status mica_accumulate_clip_grad_norms(void* const* g, const void* const* a, const int64_t* n, int32_t T,
+                                                     mica_dtype gdt, float max_norm, float inv_scale, float* d_norm,
+                                                     float* d_factor, void* stream);
 
 /*
  * The joint norm of a list sharded over several GPUs (each rank holding a contiguous part of the parameters, as a
@@ -335,9 +361,9 @@ MICA_API mica_status mica_work_items(const int64_t* n, const int32_t* vec, int32
                                      int64_t* items, int32_t max_items, int32_t* pack, int32_t max_pack,
                                      int32_t* num_items, int32_t* pack_len, int32_t* used_item_octs);
 
-/* The ABI version of this header: 4 (3 had none of mica_clip_adamw_step, mica_grad_sumsq,
- * mica_clip_factor_from_sumsq, mica_selftest_grid_wait_timeout and MICA_ERR_CAPTURE; 2 had no mica_work_items; 1 had
- * neither mica_adamw_steps_grouped nor mica_sgd_steps). */
+/* The ABI version of this header: 5 (4 had no mica_accumulate_clip_grad_norms; 3 had none of mica_clip_adamw_step,
+ * mica_grad_sumsq, mica_clip_factor_from_sumsq, mica_selftest_grid_wait_timeout and MICA_ERR_CAPTURE; 2 had no
+ * mica_work_items; 1 had neither mica_adamw_steps_grouped nor mica_sgd_steps). */
 MICA_API int32_t mica_abi_version(void);
 
 #ifdef __cplusplus

@@ -29,7 +29,7 @@ def test_exports_every_declared_symbol():
     assert len(names) >= 9
     for name in names:
         assert hasattr(L, name), name
-    assert L.mica_abi_version() == 4
+    assert L.mica_abi_version() == 5
 
 
 def test_status_strings():
@@ -148,6 +148,27 @@ def test_clip_host_validation():
     for mx, inv in ((0.0, 1.0), (-1.0, 1.0), (math.nan, 1.0), (1.0, 0.0), (1.0, math.inf), (1.0, -2.0)):
         assert L.mica_clip_grad_norms(G, N, 1, 0, mx, inv, None, f, None) == HYPER, (mx, inv)
     assert L.mica_clip_grad_norms(G, N, -2, 0, 1.0, 1.0, None, f, None) == COUNT
+
+
+def test_accumulate_host_validation():
+    """The fused add + norm checks its arguments on the host before anything is queued."""
+    L = mica.lib()
+    G = _arr(ctypes.c_void_p, [0x1000])
+    A = _arr(ctypes.c_void_p, [0x3000])
+    N = _arr(ctypes.c_int64, [4])
+    f = ctypes.c_void_p(0x2000)
+    acc = L.mica_accumulate_clip_grad_norms
+    assert acc(G, A, N, 1, 0, 1.0, 1.0, None, None, None) == NULL         # no d_factor
+    assert acc(G, None, N, 1, 0, 1.0, 1.0, None, f, None) == NULL         # no addend array
+    assert acc(G, A, N, 1, 3, 1.0, 1.0, None, f, None) == DTYPE           # packed words are not gradients
+    for mx, inv in ((0.0, 1.0), (math.nan, 1.0), (1.0, 0.0), (1.0, math.inf)):
+        assert acc(G, A, N, 1, 0, mx, inv, None, f, None) == HYPER, (mx, inv)
+    assert acc(G, A, N, -1, 0, 1.0, 1.0, None, f, None) == COUNT
+    assert acc(G, A, _arr(ctypes.c_int64, [-4]), 1, 0, 1.0, 1.0, None, f, None) == COUNT
+    nullA = _arr(ctypes.c_void_p, [None])
+    assert acc(G, nullA, N, 1, 0, 1.0, 1.0, None, f, None) == NULL        # a NULL addend with n > 0
+    assert acc(G, A, N, 1, 0, 1.0, 1.0, None, f, None) in (ADDRESS, DEVICE)  # host addresses: refused
+    assert mica.lib().mica_last_error_detail().decode()
 
 
 def test_clip_adamw_step_host_validation():
