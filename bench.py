@@ -547,6 +547,9 @@ def main():
     ap.add_argument("--shard", action="store_true",
                     help="split the list over the ranks (each steps its own part; one all-gather of the norm's "
                          "square sums a step) instead of stepping a replica on every rank")
+    ap.add_argument("--step", default="clip_adamw", choices=["clip_adamw", "accumulate"],
+                    help="the timed step: the norm then AdamW (default), or g += a with the norm fused into that "
+                         "add, then AdamW (for profiling that kernel)")
     ap.add_argument("--subset-params", type=int, default=0,
                     help="keep only the workload's first tensors up to this many parameters (small profiling case)")
     args = ap.parse_args()
@@ -588,7 +591,8 @@ def main():
     if args.shard:
         main_fig = measure_sharded(wl, args.steps, args.warmup, dist, world, rank)
     else:
-        main_fig = measure(wl, args.steps, args.warmup, zero_grad=False, dist=dist)
+        main_fig = measure(wl, args.steps, args.warmup, zero_grad=False, dist=dist,
+                           opt="accumulate" if args.step == "accumulate" else "adamw")
     if sampler:
         sampler.stop()
     clocks = sampler.summary(*main_fig["t_wall"]) if sampler else None
@@ -614,7 +618,7 @@ def main():
     P = wl.params
     sec = main_fig["total_ms"] / 1e3
     value = job_value(world, P, args.steps, main_fig["total_ms"])
-    step_bpp = step_bytes_per_param(wl)
+    step_bpp = step_bytes_per_param(wl, opt="accumulate" if args.step == "accumulate" else "adamw")
     step_gbs = P * step_bpp * args.steps / sec / 1e9
     a_bpp = adamw_bytes_per_param(wl)
     a_gbs = P * a_bpp / (main_fig["adamw_ms"] / 1e3) / 1e9
@@ -698,7 +702,9 @@ def main():
             "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": main_fig["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": run_config(wl, world),
+            "config": dict(run_config(wl, world), **({"step": "g += a with the norm fused, then AdamW",
+                                                       "bytes_per_param": step_bpp}
+                                                      if args.step == "accumulate" else {})),
             "hbm_gbs": step_gbs, "pct_of_8tbs": 100 * step_gbs / NOMINAL_HBM_GBS,
             "pct_of_measured_copy": 100 * step_gbs / peak if peak_src == "measured" else None,
             "roofline": {"bound": "hbm", "kernel": "adamw_kernel", "achieved": a_gbs, "peak": peak, "unit": "GB/s",
