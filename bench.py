@@ -418,6 +418,29 @@ def measure(wl: workloads.Workload, steps: int, warmup: int, zero_grad: bool, di
     return out
 
 
+def measure_scale(wl: workloads.Workload, steps: int, warmup: int) -> float:
+    """ScaleTensors alone over the workload's gradient list: the mean device time of one call (ms), from events around
+    `steps` back-to-back calls (factors 2 and 0.5 in turn, so the values stay as they were)."""
+    import clip_tensor_adamw_gb300 as mica
+    st = workloads.make_state(wl, "cuda")
+    workloads.fill_grad(st, 1)
+    G = mica.TensorList(st.g)
+    for i in range(warmup):
+        mica.mica_scale_tensors(G, 2.0 if i % 2 == 0 else 0.5)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for i in range(steps):
+        mica.mica_scale_tensors(G, 2.0 if i % 2 == 0 else 0.5)
+    end.record()
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / steps
+    del st, G
+    mica.mica_release_cache()
+    torch.cuda.empty_cache()
+    return ms
+
+
 def measure_sharded(wl: workloads.Workload, steps: int, warmup: int, dist, world: int, rank: int):
     """The sharded step (the list split over the ranks, ZeRO-style): each rank's square sum of its own part
     (mica_grad_sumsq), an all-gather of one double per rank, the factor from the sums in rank order
@@ -688,6 +711,15 @@ def main():
                     "sample": f"{len(times)} steps of the first {ntens} of {len(owl.sizes)} tensors ({params:,} of "
                               f"{owl.params:,} params) of {owl.name}, single-threaded C oracle"}
                 torch.cuda.empty_cache()
+        for sname, swl in (("scale_tensors_fp16_scaled", workloads.WORKLOADS["fp16_scaled"]),
+                           ("scale_tensors_gpt2_small", small)):
+            sms_ = measure_scale(swl, extra_steps(0.1), args.warmup)
+            sbpp = 2 * (2.0 if swl.grad_dtype == "f16" else 4.0)  # each cell read and written
+            extras[sname] = {"params": swl.params, "ms_per_call": sms_, "bytes_per_param": sbpp,
+                             "roofline": {"bound": "hbm", "kernel": "scale_kernel",
+                                          "achieved": swl.params * sbpp / sms_ / 1e6, "peak": peak, "unit": "GB/s",
+                                          "frac": swl.params * sbpp / sms_ / 1e6 / peak, "peak_source": peak_src,
+                                          "bytes_per_param": sbpp, "launch_ms": sms_}}
         ms, h2d, d2h = measure_e2e(wl, extra_steps(main_fig["ms_per_step"]), args.warmup)
         e2e = {"value": P / (ms / 1e3), "unit": "params/s", "ms_per_step": ms, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h}
