@@ -1,5 +1,6 @@
 // ScaleTensors ("Mica 7.7 ...", section "The whole model in one call"): each element of each listed tensor times one
-// factor, float32 or binary16 (widened, multiplied, rounded back to nearest-even), one CTA per work item.
+// factor, float32 or binary16 (widened, multiplied, rounded back to nearest-even), one CTA per work item, launched as
+// a programmatic dependent of the kernel queued before it.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -73,6 +74,8 @@ __global__ void __launch_bounds__(kThreads) scale_kernel(const TensorRec* __rest
                                                          const WorkItem* __restrict__ items, int32_t num_items,
                                                          int32_t item_octs, float factor,
                                                          const float* __restrict__ d_factor) {
+    wait_prerequisite();  // the kernel queued before may still be writing these tensors or the factor
+    allow_dependents();   // the kernel queued next may launch (it waits for this one before touching its data)
     const float f = d_factor ? __ldcg(d_factor) : factor;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int32_t it = blockIdx.x; it < num_items; it += gridDim.x) {
@@ -96,14 +99,23 @@ __global__ void __launch_bounds__(kThreads) scale_kernel(const TensorRec* __rest
 int launch_scale(const TensorRec* recs, const WorkItem* items, int32_t num_items, int32_t item_octs, Dtype dt,
                  float factor, const float* d_factor, void* stream) {
     if (num_items <= 0) return (int)cudaSuccess;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const dim3 grid(num_items), block(kThreads);
-    if (dt == kF16)
-        scale_kernel<kF16><<<grid, block, 0, st>>>(recs, items, num_items, item_octs, factor, d_factor);
-    else
-        scale_kernel<kF32><<<grid, block, 0, st>>>(recs, items, num_items, item_octs, factor, d_factor);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_items);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];  // a programmatic dependent of the kernel queued before (as the other kernels are)
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = (dt == kF16)
+                              ? cudaLaunchKernelEx(&cfg, scale_kernel<kF16>, recs, items, num_items, item_octs, factor,
+                                                   d_factor)
+                              : cudaLaunchKernelEx(&cfg, scale_kernel<kF32>, recs, items, num_items, item_octs, factor,
+                                                   d_factor);
     count_launches(1);
-    return (int)cudaGetLastError();
+    return (int)(e != cudaSuccess ? e : cudaGetLastError());
 }
 
 }  // namespace mica
