@@ -204,7 +204,8 @@ template <Dtype G, int kMode, bool kKeepL2>
 __global__ void __launch_bounds__(kThreads, kAccCtasPerSm) accumulate_norm_kernel(ChunkTable ct, float inv_scale,
                                                                            double* __restrict__ partials,
                                                                            unsigned int* ticket, float max_norm,
-                                                                           float* d_norm, float* d_factor) {
+                                                                           float* d_norm, float* d_factor,
+                                                                           double* d_sumsq) {
     __shared__ double red[kWarps];
     __shared__ int last;
     __shared__ AccSpan sp;
@@ -221,14 +222,14 @@ __global__ void __launch_bounds__(kThreads, kAccCtasPerSm) accumulate_norm_kerne
     __syncthreads();
     if (last) {  // every other CTA's partial is written: sum them all, in order
         __threadfence();
-        finalize_norm(partials, ct.grid, max_norm, inv_scale, d_norm, d_factor, nullptr, red);
+        finalize_norm(partials, ct.grid, max_norm, inv_scale, d_norm, d_factor, d_sumsq, red);
         if (t == 0) *ticket = 0u;  // ready for the next launch on this list
     }
 }
 
 template <Dtype G, int kMode, bool kKeepL2>
 cudaError_t launch_acc_t(const ChunkTable& ct, cudaStream_t st, float inv_scale, double* partials,
-                         unsigned int* ticket, float max_norm, float* d_norm, float* d_factor) {
+                         unsigned int* ticket, float max_norm, float* d_norm, float* d_factor, double* d_sumsq) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ct.grid > 0 ? ct.grid : 1);
     cfg.blockDim = dim3(kThreads);
@@ -240,34 +241,40 @@ cudaError_t launch_acc_t(const ChunkTable& ct, cudaStream_t st, float inv_scale,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, accumulate_norm_kernel<G, kMode, kKeepL2>, ct, inv_scale, partials, ticket,
-                              max_norm, d_norm, d_factor);
+                              max_norm, d_norm, d_factor, d_sumsq);
 }
 
 template <Dtype G, int kMode>
 cudaError_t launch_acc_k(bool keep_l2, const ChunkTable& ct, cudaStream_t st, float inv_scale, double* partials,
-                         unsigned int* ticket, float max_norm, float* d_norm, float* d_factor) {
-    return keep_l2 ? launch_acc_t<G, kMode, true>(ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor)
-                   : launch_acc_t<G, kMode, false>(ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
+                         unsigned int* ticket, float max_norm, float* d_norm, float* d_factor, double* d_sumsq) {
+    return keep_l2 ? launch_acc_t<G, kMode, true>(ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor,
+                                                  d_sumsq)
+                   : launch_acc_t<G, kMode, false>(ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor,
+                                                   d_sumsq);
 }
 
 }  // namespace
 
 int launch_accumulate_norm(const ChunkTable& ct, Dtype gdt, float inv_scale, double* partials, unsigned int* ticket,
-                           float max_norm, float* d_norm, float* d_factor, bool keep_l2, void* stream) {
+                           float max_norm, float* d_norm, float* d_factor, double* d_sumsq, bool keep_l2,
+                           void* stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool scaled = inv_scale != 1.0f;
     int ex = 0;  // binary16 times a power of two in [2^-102, 2^111]: every product is an exact normal float32
     const bool pow2 = std::frexp(inv_scale, &ex) == 0.5f && inv_scale >= 0x1p-102f && inv_scale <= 0x1p111f;
     cudaError_t e;
     if (gdt == kF16 && pow2)
-        e = launch_acc_k<kF16, kSumHalfPow2>(keep_l2, ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
+        e = launch_acc_k<kF16, kSumHalfPow2>(keep_l2, ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor,
+                                              d_sumsq);
     else if (gdt == kF16)
-        e = launch_acc_k<kF16, kSumScaled>(keep_l2, ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
+        e = launch_acc_k<kF16, kSumScaled>(keep_l2, ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor,
+                                              d_sumsq);
     else if (scaled)
-        e = launch_acc_k<kF32, kSumScaled>(keep_l2, ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor);
+        e = launch_acc_k<kF32, kSumScaled>(keep_l2, ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor,
+                                              d_sumsq);
     else
-        e = launch_acc_k<kF32, kSumUnscaled>(keep_l2, ct, st, inv_scale, partials, ticket, max_norm, d_norm,
-                                             d_factor);
+        e = launch_acc_k<kF32, kSumUnscaled>(keep_l2, ct, st, inv_scale, partials, ticket, max_norm, d_norm, d_factor,
+                                              d_sumsq);
     count_launches(1);
     return (int)e;
 }

@@ -837,13 +837,12 @@ extern "C" mica_status mica_clip_grad_norms(const void* const* g, const int64_t*
                         stream, "ClipGradNorms launch");
 }
 
-extern "C" mica_status mica_accumulate_clip_grad_norms(void* const* g, const void* const* a, const int64_t* n,
-                                                       int32_t T, mica_dtype gdt, float max_norm, float inv_scale,
-                                                       float* d_norm, float* d_factor, void* stream) {
+// The add g += a with the norm fused into it (both entry points below): the list's checks and cached table, then one
+// launch writing d_norm / d_factor (the norm's call) or d_sumsq (one rank's square sum), each when not null.
+static mica_status accumulate_call(void* const* g, const void* const* a, const int64_t* n, int32_t T, mica_dtype gdt,
+                                   float max_norm, float inv_scale, float* d_norm, float* d_factor, double* d_sumsq,
+                                   void* stream) {
     if (gdt != MICA_F32 && gdt != MICA_F16) return fail(MICA_ERR_DTYPE, "gradients must be float32 or float16");
-    if (!d_factor) return fail(MICA_ERR_NULL, "d_factor is NULL");
-    if (std::isnan(max_norm) || !(max_norm > 0.0f))
-        return fail(MICA_ERR_HYPER, "max_norm %g is not > 0", (double)max_norm);
     if (!std::isfinite(inv_scale) || !(inv_scale > 0.0f))
         return fail(MICA_ERR_HYPER, "inv_scale %g is not finite and > 0", (double)inv_scale);
     if (T < 0 || T > MICA_MAX_TENSORS) return fail(MICA_ERR_COUNT, "T = %d is outside [0, %d]", T, MICA_MAX_TENSORS);
@@ -858,14 +857,34 @@ extern "C" mica_status mica_accumulate_clip_grad_norms(void* const* g, const voi
         int64_t total = 0;
         if ((s = check_list(T, n, {reinterpret_cast<const void* const*>(g), a}, &total)) != MICA_OK) return s;
         if ((s = current_device(&dev)) != MICA_OK) return s;
-        if (total == 0) L.T = 0;  // an empty list still gets its norm (0) and factor written
+        if (total == 0) L.T = 0;  // an empty list still gets its outputs written
         if ((s = get_plan(L, dev, &p, stream)) != MICA_OK) return s;
     }
-    if ((s = check_scalars(p, dev, d_factor, d_norm, "a gradient or an addend")) != MICA_OK) return s;
+    if (d_sumsq) {
+        if ((s = check_device_span(d_sumsq, 8, 8, dev, "d_sumsq", 0)) != MICA_OK) return s;
+        if (overlaps_any(p->spans, d_sumsq, 8)) return fail(MICA_ERR_OVERLAP, "d_sumsq lies inside a gradient or an addend");
+    } else if ((s = check_scalars(p, dev, d_factor, d_norm, "a gradient or an addend")) != MICA_OK) {
+        return s;
+    }
     const bool keep_l2 = p->total * (int64_t)elem_bytes((Dtype)gdt) <= kKeepL2MaxGradBytes;
     return after_launch(launch_accumulate_norm(p->chunks, (Dtype)gdt, inv_scale, p->partials, p->ticket, max_norm,
-                                               d_norm, d_factor, keep_l2, stream),
-                        stream, "AccumulateClipGradNorms launch");
+                                               d_norm, d_factor, d_sumsq, keep_l2, stream),
+                        stream, d_sumsq ? "accumulating square-sum launch" : "AccumulateClipGradNorms launch");
+}
+
+extern "C" mica_status mica_accumulate_clip_grad_norms(void* const* g, const void* const* a, const int64_t* n,
+                                                       int32_t T, mica_dtype gdt, float max_norm, float inv_scale,
+                                                       float* d_norm, float* d_factor, void* stream) {
+    if (!d_factor) return fail(MICA_ERR_NULL, "d_factor is NULL");
+    if (std::isnan(max_norm) || !(max_norm > 0.0f))
+        return fail(MICA_ERR_HYPER, "max_norm %g is not > 0", (double)max_norm);
+    return accumulate_call(g, a, n, T, gdt, max_norm, inv_scale, d_norm, d_factor, nullptr, stream);
+}
+
+extern "C" mica_status mica_accumulate_grad_sumsq(void* const* g, const void* const* a, const int64_t* n, int32_t T,
+                                                  mica_dtype gdt, float inv_scale, double* d_sumsq, void* stream) {
+    if (!d_sumsq) return fail(MICA_ERR_NULL, "d_sumsq is NULL");
+    return accumulate_call(g, a, n, T, gdt, 1.0f, inv_scale, nullptr, nullptr, d_sumsq, stream);
 }
 
 extern "C" mica_status mica_grad_sumsq(const void* const* g, const int64_t* n, int32_t T, mica_dtype gdt,

@@ -169,12 +169,13 @@ int launch_scale(const TensorRec* recs, const WorkItem* items, int32_t num_items
 
 // The gradient's last write fused with the norm (accnorm.cu): for every tensor k of ct, g += a (g in recs[k].g, the
 // addend in recs[k].m, each sum rounded to the gradient's type), and the joint norm and factor of the result, as
-// launch_norm computes them (one partial per CTA into `partials`, the CTA that finishes last writing d_norm when not
-// null and d_factor). ct is laid out as for the register-streaming norm, with ct.grid CTAs from
+// launch_norm computes them (one partial per CTA into `partials`, the CTA that finishes last writing d_norm,
+// d_factor and d_sumsq, each when not null). ct is laid out as for the register-streaming norm, with ct.grid CTAs from
 // choose_accumulate_grid. keep_l2: the new gradient's stores carry an evict-last L2 policy (for gradients that fit
 // in L2, which the update reads next).
 int launch_accumulate_norm(const ChunkTable& ct, Dtype gdt, float inv_scale, double* partials, unsigned int* ticket,
-                           float max_norm, float* d_norm, float* d_factor, bool keep_l2, void* stream);
+                           float max_norm, float* d_norm, float* d_factor, double* d_sumsq, bool keep_l2,
+                           void* stream);
 constexpr int kAccCtasPerSm = 4;
 // kAccCtasPerSm CTAs per SM in one wave per 192 KB of gradient that a CTA of a single wave would take, from 2 to 8
 // waves (measured on GB300: the loss-scaled list's 76 MB best in 2 waves, GPT-2 small's 498 MB in 4, GPT-2 XL's

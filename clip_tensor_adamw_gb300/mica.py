@@ -72,10 +72,11 @@ def lib() -> ctypes.CDLL:
         L.mica_grad_sumsq.argtypes = [_P, _I64P, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, _P, _P]
         L.mica_accumulate_clip_grad_norms.argtypes = [_P, _P, _I64P, ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
                                                       ctypes.c_float, _P, _P, _P]
+        L.mica_accumulate_grad_sumsq.argtypes = [_P, _P, _I64P, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, _P, _P]
         L.mica_clip_factor_from_sumsq.argtypes = [_P, ctypes.c_int32, ctypes.c_float, ctypes.c_float, _P, _P, _P]
         for f in ("mica_scale_tensors", "mica_clip_grad_norms", "mica_adamw_steps", "mica_adamw_steps_grouped",
                   "mica_sgd_steps", "mica_clip_adamw_step", "mica_grad_sumsq", "mica_clip_factor_from_sumsq",
-                  "mica_accumulate_clip_grad_norms", "mica_sync", "mica_release_cache"):
+                  "mica_accumulate_clip_grad_norms", "mica_accumulate_grad_sumsq", "mica_sync", "mica_release_cache"):
             getattr(L, f).restype = ctypes.c_int
         for f in ("mica_selftest_wait_timeout", "mica_selftest_grid_wait_timeout"):
             getattr(L, f).argtypes = [ctypes.c_uint32, _P]
@@ -193,6 +194,26 @@ def mica_accumulate_clip_grad_norms(grads, addends, max_norm: float, inv_scale: 
     _check(lib().mica_accumulate_clip_grad_norms(G.ptrs, A.ptrs, G.n, G.T, gdt, float(max_norm), float(inv_scale),
                                                  _ptr(norm_out), _ptr(factor_out), _stream(stream)))
     return norm_out, factor_out
+
+
+def mica_accumulate_grad_sumsq(grads, addends, inv_scale: float = 1.0, out: torch.Tensor | None = None,
+                               stream=None) -> torch.Tensor:
+    """``grads[k] += addends[k]`` in place, then the sum of squares of the unscaled result, exactly as the norm sums
+    it, as a one-element float64 device tensor (``out`` when given): one rank's share of a sharded list's joint
+    norm, with the add fused into its pass."""
+    G = _as_list(grads)
+    A = _as_list(addends)
+    if A.T != G.T or A.total != G.total:  # the call passes the gradients' counts for both lists
+        raise ValueError("addends must match the gradients tensor for tensor")
+    if G.T and A.tensors[0].dtype != G.tensors[0].dtype:
+        raise TypeError("addends must have the gradients' dtype")
+    dev = G.tensors[0].device if G.T else torch.device("cuda", torch.cuda.current_device())
+    if out is None:
+        out = torch.empty(1, dtype=torch.float64, device=dev)
+    gdt = _dtype_code(G.tensors[0] if G.T else None, "grads")
+    _check(lib().mica_accumulate_grad_sumsq(G.ptrs, A.ptrs, G.n, G.T, gdt, float(inv_scale), _ptr(out),
+                                            _stream(stream)))
+    return out
 
 
 def mica_grad_sumsq(grads, inv_scale: float = 1.0, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:

@@ -162,6 +162,19 @@ MICA_API mica_status mica_accumulate_clip_grad_norms(void* const* g, const void*
                                                      float* d_factor, void* stream);
 
 /*
+ * mica_accumulate_grad_sumsq: the same add over one rank's part of a sharded list, fused with that part's square sum
+ * (the sharded step's counterpart of mica_accumulate_clip_grad_norms, as mica_grad_sumsq is mica_clip_grad_norms's):
+ * g[k] += a[k] exactly as mica_accumulate_clip_grad_norms adds, then *d_sumsq (a device double) = the sum over the
+ * list of x^2, x = f32(g * inv_scale), of the updated g, summed exactly as mica_grad_sumsq sums it. The ranks' sums
+ * then go to mica_clip_factor_from_sumsq.
+ * Sources: as mica_accumulate_clip_grad_norms and mica_grad_sumsq.
+ * Errors: NULL / COUNT / DTYPE / HYPER (inv_scale) / ADDRESS / OVERLAP (also d_sumsq inside a gradient or an
+ * addend) / DEVICE / CUDA / NOMEM.
+ */
+MICA_API mica_status mica_accumulate_grad_sumsq(void* const* g, const void* const* a, const int64_t* n, int32_t T,
+                                                mica_dtype gdt, float inv_scale, double* d_sumsq, void* stream);
+
+/*
  * The joint norm of a list sharded over several GPUs (each rank holding a contiguous part of the parameters, as a
  * ZeRO-style partition does), in two calls around one exchange that the caller makes (an all-gather of one double
  * per rank): ClipGradNorms's joint norm ("Mica 7.7 ...", section "The whole model in one call") is that of every
@@ -361,7 +374,7 @@ MICA_API mica_status mica_work_items(const int64_t* n, const int32_t* vec, int32
                                      int64_t* items, int32_t max_items, int32_t* pack, int32_t max_pack,
                                      int32_t* num_items, int32_t* pack_len, int32_t* used_item_octs);
 
-/* The ABI version of this header: 5 (4 had no mica_accumulate_clip_grad_norms; 3 had none of mica_clip_adamw_step,
+/* The ABI version of this header: 5 (4 had neither mica_accumulate_clip_grad_norms nor mica_accumulate_grad_sumsq; 3 had none of mica_clip_adamw_step,
  * mica_grad_sumsq, mica_clip_factor_from_sumsq, mica_selftest_grid_wait_timeout and MICA_ERR_CAPTURE; 2 had no
  * mica_work_items; 1 had neither mica_adamw_steps_grouped nor mica_sgd_steps). */
 MICA_API int32_t mica_abi_version(void);

@@ -169,6 +169,14 @@ def test_accumulate_host_validation():
     assert acc(G, nullA, N, 1, 0, 1.0, 1.0, None, f, None) == NULL        # a NULL addend with n > 0
     assert acc(G, A, N, 1, 0, 1.0, 1.0, None, f, None) in (ADDRESS, DEVICE)  # host addresses: refused
     assert mica.lib().mica_last_error_detail().decode()
+    sq = L.mica_accumulate_grad_sumsq
+    assert sq(G, A, N, 1, 0, 1.0, None, None) == NULL                      # no d_sumsq
+    assert sq(G, None, N, 1, 0, 1.0, f, None) == NULL
+    assert sq(G, A, N, 1, 2, 1.0, f, None) == DTYPE
+    for inv in (0.0, -1.0, math.inf, math.nan):
+        assert sq(G, A, N, 1, 0, inv, f, None) == HYPER, inv
+    assert sq(G, A, N, -3, 0, 1.0, f, None) == COUNT
+    assert sq(G, A, N, 1, 0, 1.0, f, None) in (ADDRESS, DEVICE)
 
 
 def test_clip_adamw_step_host_validation():

@@ -71,3 +71,34 @@ def test_factor_from_sumsq_rank_order_and_validation():
     assert L.mica_clip_factor_from_sumsq(None, 2, 1.0, 1.0, None, factor.data_ptr(), None) == 1  # NULL
     with pytest.raises(mica.MicaError, match="HYPER"):
         mica.mica_clip_factor_from_sumsq(parts, 0.0, 1.0)
+
+
+@pytest.mark.parametrize("world", [2, 3])
+@pytest.mark.parametrize("name", ["gpt2_small", "fp16_scaled"])
+def test_sharded_accumulate_matches_the_whole_list(ora, name, world):
+    """The sharded form of the norm fused into the gradient's last write: each rank's g += a with its part's square
+    sum (mica_accumulate_grad_sumsq), the factor from the sums in rank order, against the oracle's add and norm of
+    the whole list; every added element bit-exact, each rank's sum that of its part."""
+    wl = W[name]
+    sizes = small_gpt2_sizes() + [1, 7, 4097] if name != "fp16_scaled" else list(wl.sizes[:500]) + [768 * 3072]
+    st = workloads.make_state(wl, "cuda", sizes=sizes)
+    add = workloads.make_state(wl, "cuda", sizes=sizes)
+    workloads.fill_grad(st, 1)
+    workloads.fill_grad(add, 1, seed=91)
+    g_host = [x.detach().cpu().numpy().copy() for x in st.g]
+    a_host = [x.detach().cpu().numpy().copy() for x in add.g]
+    parts = torch.zeros(world, dtype=torch.float64, device="cuda")
+    for r in range(world):
+        pieces = shard_pieces(sizes, world, r)
+        mica.mica_accumulate_grad_sumsq(piece_views(st.g, pieces), piece_views(add.g, pieces), wl.inv_scale,
+                                        out=parts[r:r + 1])
+    d_norm, d_factor = mica.mica_clip_factor_from_sumsq(parts, wl.max_norm, wl.inv_scale)
+    o_norm, o_factor = ora.accumulate_clip_grad_norms(g_host, a_host, wl.max_norm, wl.inv_scale)
+    torch.cuda.synchronize()
+    for k, x in enumerate(st.g):
+        parity.exact(x.detach().cpu().numpy(), g_host[k], f"g[{k}]")
+    parity.check_norm(np.float32(d_norm.item()), o_norm, 0)
+    assert np.float32(d_factor.item()).view(np.uint32) == o_factor.view(np.uint32)
+    o_parts = [ora.sum_squares([g_host[k][a:b] for k, a, b in shard_pieces(sizes, world, r)] or
+                               [np.zeros(0, g_host[0].dtype)], wl.inv_scale) for r in range(world)]
+    np.testing.assert_allclose(parts.cpu().numpy(), o_parts, rtol=1e-12)

@@ -122,3 +122,54 @@ def test_two_rank_sharded_step_equals_the_whole_list():
             assert np.array_equal(rw[k][a:b].view(np.uint32), w[k][a:b].view(np.uint32))
             assert np.array_equal(rm[k][a // 2:(b + 1) // 2], m[k][a // 2:(b + 1) // 2])
             assert np.array_equal(rv[k][a // 2:(b + 1) // 2], v[k][a // 2:(b + 1) // 2])
+
+
+def _rank_accumulate(rank, world, port, out):
+    sys.path.insert(0, ROOT)
+    import oracle
+    from clip_tensor_adamw_gb300.shard import shard_pieces
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ora = oracle.Oracle()
+        g, a, sizes = _accumulate_inputs()
+        pieces = shard_pieces(sizes, world, rank)
+        gp = [g[k][x:y].copy() for k, x, y in pieces]
+        ap = [a[k][x:y].copy() for k, x, y in pieces]
+        ora.accumulate_grads(gp, ap)  # this rank's part of the gradients' last write ...
+        mine = torch.tensor([ora.sum_squares(gp, 1.0) if gp else 0.0], dtype=torch.float64)  # ... and its sum
+        parts = [torch.zeros(1, dtype=torch.float64) for _ in range(world)]
+        dist.all_gather(parts, mine)
+        S = 0.0
+        for p in parts:
+            S += float(p.item())
+        norm = np.float32(np.sqrt(S))
+        factor = ora.clip_factor(norm, 1.0, 1.0)
+        out[rank] = (float(norm), int(factor.view(np.uint32)), pieces, gp)
+    finally:
+        dist.destroy_process_group()
+
+
+def _accumulate_inputs():
+    rng = np.random.Generator(np.random.PCG64(17))
+    sizes = [5000, 1, 0, 777, 64, 9, 40000]
+    g = [rng.normal(0, 0.05, size=n).astype(np.float32) for n in sizes]
+    a = [rng.normal(0, 0.05, size=n).astype(np.float32) for n in sizes]
+    return g, a, sizes
+
+
+def test_two_rank_sharded_accumulate_equals_the_whole_list():
+    """The sharded form of the norm fused into the gradients' last write, with the oracle's arithmetic on each rank:
+    every rank's part of g + a, the rank-ordered sum of the parts' square sums, and the factor, equal to the
+    single-process add and norm of the whole list."""
+    import oracle
+    world, port = 2, _free_port()
+    out = mp.Manager().dict()
+    mp.spawn(_rank_accumulate, args=(world, port, out), nprocs=world, join=True)
+    g, a, sizes = _accumulate_inputs()
+    norm, factor = oracle.Oracle().accumulate_clip_grad_norms(g, a, 1.0)
+    assert out[0][:2] == out[1][:2] == (float(norm), int(factor.view(np.uint32)))
+    for rank in range(world):
+        _, _, pieces, gp = out[rank]
+        for (k, x, y), part in zip(pieces, gp):
+            assert np.array_equal(part.view(np.uint32), g[k][x:y].view(np.uint32))
