@@ -156,7 +156,7 @@ __device__ __forceinline__ double accumulate_chunk_share(const ChunkTable& ct, i
         }
         __syncthreads();
         const int64_t oe = sp.lo[cnt] < c1 ? sp.lo[cnt] : c1;
-        int32_t j = 0, jp = 0;
+        int32_t j = 0;
         const int64_t first = ob + ((t - (int32_t)((ob - c0) & (kThreads - 1))) & (kThreads - 1));
         for (int64_t o = first; o < oe; o += U * kThreads) {
             RawOctet<G> gr[U], ar[U];
