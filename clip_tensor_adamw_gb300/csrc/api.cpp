@@ -202,6 +202,7 @@ struct Plan {
     ChunkTable fchunks{};
     double* fpartials = nullptr;
     unsigned int* fbar = nullptr;
+    int32_t pins = 0;  // calls in progress that hold this table (under g_mu; see CallScope)
     ~Plan() {
         if (dev || fdev) {
             int cur = 0;
@@ -222,6 +223,47 @@ static std::mutex g_mu;
 static std::unordered_map<uint64_t, std::vector<std::unique_ptr<Plan>>> g_plans;
 static size_t g_plan_count = 0;
 constexpr size_t kMaxPlans = 1024;
+
+// Tables a call in progress holds. Every table a call looks up is pinned until the outermost library call of its
+// thread returns (each entry point opens a CallScope), and neither the cache's eviction nor mica_release_cache frees
+// a pinned table: so a call that looks up a second list after its first (mica_clip_adamw_step's norm) never loses
+// the first, and calls in progress on other threads keep theirs.
+static thread_local int t_call_depth = 0;
+static thread_local std::vector<Plan*> t_pinned;
+
+struct CallScope {
+    CallScope() { ++t_call_depth; }
+    ~CallScope() {
+        if (--t_call_depth == 0 && !t_pinned.empty()) {
+            std::lock_guard<std::mutex> lock(g_mu);
+            for (Plan* p : t_pinned) --p->pins;
+            t_pinned.clear();
+        }
+    }
+    CallScope(const CallScope&) = delete;
+    CallScope& operator=(const CallScope&) = delete;
+};
+
+// Pins a table for the calling thread's outermost call (g_mu held).
+static void pin_plan(Plan* p) {
+    if (p && t_call_depth > 0) {
+        ++p->pins;
+        t_pinned.push_back(p);
+    }
+}
+
+// Frees every cached table that no call in progress holds (g_mu held; the device is idle).
+static void evict_unpinned() {
+    size_t kept = 0;
+    for (auto it = g_plans.begin(); it != g_plans.end();) {
+        auto& v = it->second;
+        v.erase(std::remove_if(v.begin(), v.end(), [](const std::unique_ptr<Plan>& p) { return p->pins == 0; }),
+                v.end());
+        kept += v.size();
+        it = v.empty() ? g_plans.erase(it) : std::next(it);
+    }
+    g_plan_count = kept;
+}
 
 static uint64_t mix(uint64_t h, uint64_t x) {
     h ^= x + 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
@@ -614,8 +656,7 @@ static mica_status build_plan(const ListDesc& L, int device, uint64_t h, Plan** 
 
     if (g_plan_count >= kMaxPlans) {
         cudaDeviceSynchronize();
-        g_plans.clear();
-        g_plan_count = 0;
+        evict_unpinned();
     }
     g_plans[h].push_back(std::move(plan));
     ++g_plan_count;
@@ -699,8 +740,10 @@ static Plan* find_plan(const ListDesc& L, int device, uint64_t h) {
 static mica_status get_plan(const ListDesc& L, int device, Plan** out, void* stream) {
     const uint64_t h = list_hash(L, device);
     std::lock_guard<std::mutex> lock(g_mu);
-    if ((*out = find_plan(L, device, h)) != nullptr) return MICA_OK;
-    return build_plan(L, device, h, out, stream);
+    mica_status s = MICA_OK;
+    if ((*out = find_plan(L, device, h)) == nullptr) s = build_plan(L, device, h, out, stream);
+    if (s == MICA_OK) pin_plan(*out);
+    return s;
 }
 
 // A list seen before needs none of the per-tensor checks again: its counts and pointers equal those of a list that
@@ -709,7 +752,9 @@ static Plan* cached_plan(const ListDesc& L, int device) {
     if (L.T <= 0) return nullptr;
     const uint64_t h = list_hash(L, device);
     std::lock_guard<std::mutex> lock(g_mu);
-    return find_plan(L, device, h);
+    Plan* p = find_plan(L, device, h);
+    pin_plan(p);
+    return p;
 }
 
 // The device scalars of a call (d_factor, d_norm): device memory of the current device, aligned, outside the list's
@@ -783,6 +828,7 @@ using namespace mica;
 
 extern "C" mica_status mica_scale_tensors(void* const* t, const int64_t* n, int32_t T, mica_dtype dt, float factor,
                                           const float* d_factor, void* stream) {
+    CallScope scope;  // the tables this call looks up stay pinned until it returns
     if (dt != MICA_F32 && dt != MICA_F16) return fail(MICA_ERR_DTYPE, "ScaleTensors takes float32 or float16 tensors");
     if (!d_factor && !std::isfinite(factor)) return fail(MICA_ERR_HYPER, "factor %g is not finite", (double)factor);
     if (T < 0 || T > MICA_MAX_TENSORS) return fail(MICA_ERR_COUNT, "T = %d is outside [0, %d]", T, MICA_MAX_TENSORS);
@@ -808,6 +854,7 @@ extern "C" mica_status mica_scale_tensors(void* const* t, const int64_t* n, int3
 extern "C" mica_status mica_clip_grad_norms(const void* const* g, const int64_t* n, int32_t T, mica_dtype gdt,
                                             float max_norm, float inv_scale, float* d_norm, float* d_factor,
                                             void* stream) {
+    CallScope scope;  // the tables this call looks up stay pinned until it returns
     if (gdt != MICA_F32 && gdt != MICA_F16) return fail(MICA_ERR_DTYPE, "gradients must be float32 or float16");
     if (!d_factor) return fail(MICA_ERR_NULL, "d_factor is NULL");
     if (std::isnan(max_norm) || !(max_norm > 0.0f))
@@ -875,6 +922,7 @@ static mica_status accumulate_call(void* const* g, const void* const* a, const i
 extern "C" mica_status mica_accumulate_clip_grad_norms(void* const* g, const void* const* a, const int64_t* n,
                                                        int32_t T, mica_dtype gdt, float max_norm, float inv_scale,
                                                        float* d_norm, float* d_factor, void* stream) {
+    CallScope scope;  // the tables this call looks up stay pinned until it returns
     if (!d_factor) return fail(MICA_ERR_NULL, "d_factor is NULL");
     if (std::isnan(max_norm) || !(max_norm > 0.0f))
         return fail(MICA_ERR_HYPER, "max_norm %g is not > 0", (double)max_norm);
@@ -883,12 +931,14 @@ extern "C" mica_status mica_accumulate_clip_grad_norms(void* const* g, const voi
 
 extern "C" mica_status mica_accumulate_grad_sumsq(void* const* g, const void* const* a, const int64_t* n, int32_t T,
                                                   mica_dtype gdt, float inv_scale, double* d_sumsq, void* stream) {
+    CallScope scope;  // the tables this call looks up stay pinned until it returns
     if (!d_sumsq) return fail(MICA_ERR_NULL, "d_sumsq is NULL");
     return accumulate_call(g, a, n, T, gdt, 1.0f, inv_scale, nullptr, nullptr, d_sumsq, stream);
 }
 
 extern "C" mica_status mica_grad_sumsq(const void* const* g, const int64_t* n, int32_t T, mica_dtype gdt,
                                        float inv_scale, double* d_sumsq, void* stream) {
+    CallScope scope;  // the tables this call looks up stay pinned until it returns
     if (gdt != MICA_F32 && gdt != MICA_F16) return fail(MICA_ERR_DTYPE, "gradients must be float32 or float16");
     if (!d_sumsq) return fail(MICA_ERR_NULL, "d_sumsq is NULL");
     if (!std::isfinite(inv_scale) || !(inv_scale > 0.0f))
@@ -1065,6 +1115,7 @@ static bool use_fused() {
 extern "C" mica_status mica_adamw_steps(float* const* w, void* const* g, void* const* m, void* const* v,
                                         const int64_t* n, int32_t T, mica_dtype gdt, mica_dtype mdt,
                                         const mica_adamw_hp* hp, const float* d_factor, void* stream) {
+    CallScope scope;  // the tables this call looks up stay pinned until it returns
     return adamw_steps(w, g, m, v, n, T, gdt, mdt, nullptr, hp, 1, d_factor, stream);
 }
 
@@ -1072,6 +1123,7 @@ extern "C" mica_status mica_adamw_steps_grouped(float* const* w, void* const* g,
                                                 const int64_t* n, int32_t T, mica_dtype gdt, mica_dtype mdt,
                                                 const int32_t* group, const mica_adamw_hp* hp, int32_t num_groups,
                                                 const float* d_factor, void* stream) {
+    CallScope scope;  // the tables this call looks up stay pinned until it returns
     if (num_groups < 1 || num_groups > MICA_MAX_GROUPS)
         return fail(MICA_ERR_COUNT, "num_groups = %d is outside [1, %d]", num_groups, MICA_MAX_GROUPS);
     if (T > 0 && !group) return fail(MICA_ERR_NULL, "group is NULL");
@@ -1082,6 +1134,7 @@ extern "C" mica_status mica_clip_adamw_step(float* const* w, void* const* g, voi
                                             const int64_t* n, int32_t T, mica_dtype gdt, mica_dtype mdt,
                                             const mica_adamw_hp* hp, float max_norm, float inv_scale, float* d_norm,
                                             float* d_factor, void* stream) {
+    CallScope scope;  // the tables this call looks up stay pinned until it returns
     // the norm's own checks (those of mica_clip_grad_norms), then the update's (those of mica_adamw_steps)
     if (gdt != MICA_F32 && gdt != MICA_F16) return fail(MICA_ERR_DTYPE, "gradients must be float32 or float16");
     if (!d_factor) return fail(MICA_ERR_NULL, "d_factor is NULL");
@@ -1117,6 +1170,7 @@ extern "C" mica_status mica_clip_adamw_step(float* const* w, void* const* g, voi
 extern "C" mica_status mica_sgd_steps(float* const* w, void* const* g, float* const* buf, const int64_t* n,
                                       int32_t T, mica_dtype gdt, const mica_sgd_hp* hp, const float* d_factor,
                                       void* stream) {
+    CallScope scope;  // the tables this call looks up stay pinned until it returns
     if (!hp) return fail(MICA_ERR_NULL, "hp is NULL");
     if (gdt != MICA_F32 && gdt != MICA_F16) return fail(MICA_ERR_DTYPE, "gradients must be float32 or float16");
     if (!finite_nonneg(hp->lr)) return fail(MICA_ERR_HYPER, "lr %g is not finite and >= 0", hp->lr);
@@ -1184,8 +1238,7 @@ extern "C" mica_status mica_release_cache(void) {
     std::lock_guard<std::mutex> lock(g_mu);
     cudaError_t e = cudaSuccess;
     if (g_plan_count) e = cudaDeviceSynchronize();
-    g_plans.clear();
-    g_plan_count = 0;
+    evict_unpinned();
     noalloc_forget_addresses();
     if (e != cudaSuccess) return cuda_fail(e, "mica_release_cache");
     return ok();

@@ -343,7 +343,9 @@ MICA_API mica_status mica_selftest_wait_timeout(uint32_t polls, void* stream);
  */
 MICA_API mica_status mica_selftest_grid_wait_timeout(uint32_t polls, void* stream);
 
-/* Waits for the current device, then frees every cached per-list device table. Returns MICA_OK or MICA_ERR_CUDA. */
+/* Waits for the current device, then frees every cached per-list device table (but those a call in progress on
+ * another thread holds, which stay cached). Returns MICA_OK or MICA_ERR_CUDA. The cache holds at most 1,024 tables;
+ * a new table beyond that first frees, the same way, every table no call in progress holds. */
 MICA_API mica_status mica_release_cache(void);
 
 /* A static, human-readable name for a status. */
