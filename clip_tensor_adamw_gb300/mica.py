@@ -107,7 +107,8 @@ def _check(status: int) -> None:
 class TensorList:
     """The pointer and size arrays of a list of tensors, built once and reusable across calls (the tensors must stay
     alive and in place). Element counts are those of the tensors, or ``sizes`` when given (packed moments hold
-    ceil(n/2) words for n elements, so their list carries the elements' counts)."""
+    ceil(n/2) words for n elements, so their list carries the elements' counts). Every tensor of a list must have
+    the same dtype (checked here, once, so that a call reads one dtype for the whole list)."""
 
     def __init__(self, tensors: Sequence[torch.Tensor], sizes: Sequence[int] | None = None):
         self.tensors = list(tensors)
@@ -122,22 +123,30 @@ class TensorList:
         self.n = (ctypes.c_int64 * max(T, 1))(*counts)
         self.counts = counts
         self.total = sum(counts)
+        dtypes = {t.dtype for t in self.tensors}
+        if len(dtypes) > 1:
+            raise TypeError(f"a tensor list mixes dtypes {sorted(str(d) for d in dtypes)}")
+        self.dtype = dtypes.pop() if dtypes else None
 
 
 def _as_list(x, sizes=None) -> TensorList:
     return x if isinstance(x, TensorList) else TensorList(x, sizes)
 
 
-def _dtype_code(t: torch.Tensor | None, what: str) -> int:
-    if t is None:
+def _dtype_code(L: TensorList, what: str) -> int:
+    """The ABI dtype of a list's tensors (float32 for an empty list)."""
+    if L.dtype is None or L.dtype == torch.float32:
         return MICA_F32
-    if t.dtype == torch.float32:
-        return MICA_F32
-    if t.dtype == torch.float16:
+    if L.dtype == torch.float16:
         return MICA_F16
-    if t.dtype == torch.int32 or str(t.dtype) == "torch.uint32":  # packed BF16 words
+    if L.dtype == torch.int32 or str(L.dtype) == "torch.uint32":  # packed BF16 words
         return MICA_BF16X2
-    raise TypeError(f"{what}: unsupported dtype {t.dtype}")
+    raise TypeError(f"{what}: unsupported dtype {L.dtype}")
+
+
+def _weights(W: TensorList) -> None:
+    if W.dtype is not None and W.dtype != torch.float32:
+        raise TypeError(f"w: the weights must be float32, not {W.dtype}")
 
 
 def _stream(stream) -> int | None:
@@ -153,7 +162,7 @@ def _ptr(t: torch.Tensor | None):
 def mica_scale_tensors(tensors, factor: float = 1.0, d_factor: torch.Tensor | None = None, stream=None) -> None:
     """ScaleTensors: every cell of every tensor times ``factor`` (or the device scalar ``d_factor``), in place."""
     L = _as_list(tensors)
-    dt = _dtype_code(L.tensors[0] if L.T else None, "tensors")
+    dt = _dtype_code(L, "tensors")
     _check(lib().mica_scale_tensors(L.ptrs, L.n, L.T, dt, float(factor), _ptr(d_factor), _stream(stream)))
 
 
@@ -167,7 +176,7 @@ def mica_clip_grad_norms(grads, max_norm: float, inv_scale: float = 1.0, norm_ou
         norm_out = torch.empty(1, dtype=torch.float32, device=dev)
     if factor_out is None:
         factor_out = torch.empty(1, dtype=torch.float32, device=dev)
-    gdt = _dtype_code(L.tensors[0] if L.T else None, "grads")
+    gdt = _dtype_code(L, "grads")
     _check(lib().mica_clip_grad_norms(L.ptrs, L.n, L.T, gdt, float(max_norm), float(inv_scale), _ptr(norm_out),
                                       _ptr(factor_out), _stream(stream)))
     return norm_out, factor_out
@@ -183,14 +192,14 @@ def mica_accumulate_clip_grad_norms(grads, addends, max_norm: float, inv_scale: 
     A = _as_list(addends)
     if A.T != G.T or A.total != G.total:  # the call passes the gradients' counts for both lists
         raise ValueError("addends must match the gradients tensor for tensor")
-    if G.T and A.tensors[0].dtype != G.tensors[0].dtype:
+    if G.T and A.dtype != G.dtype:
         raise TypeError("addends must have the gradients' dtype")
     dev = G.tensors[0].device if G.T else torch.device("cuda", torch.cuda.current_device())
     if norm_out is None:
         norm_out = torch.empty(1, dtype=torch.float32, device=dev)
     if factor_out is None:
         factor_out = torch.empty(1, dtype=torch.float32, device=dev)
-    gdt = _dtype_code(G.tensors[0] if G.T else None, "grads")
+    gdt = _dtype_code(G, "grads")
     _check(lib().mica_accumulate_clip_grad_norms(G.ptrs, A.ptrs, G.n, G.T, gdt, float(max_norm), float(inv_scale),
                                                  _ptr(norm_out), _ptr(factor_out), _stream(stream)))
     return norm_out, factor_out
@@ -205,12 +214,12 @@ def mica_accumulate_grad_sumsq(grads, addends, inv_scale: float = 1.0, out: torc
     A = _as_list(addends)
     if A.T != G.T or A.total != G.total:  # the call passes the gradients' counts for both lists
         raise ValueError("addends must match the gradients tensor for tensor")
-    if G.T and A.tensors[0].dtype != G.tensors[0].dtype:
+    if G.T and A.dtype != G.dtype:
         raise TypeError("addends must have the gradients' dtype")
     dev = G.tensors[0].device if G.T else torch.device("cuda", torch.cuda.current_device())
     if out is None:
         out = torch.empty(1, dtype=torch.float64, device=dev)
-    gdt = _dtype_code(G.tensors[0] if G.T else None, "grads")
+    gdt = _dtype_code(G, "grads")
     _check(lib().mica_accumulate_grad_sumsq(G.ptrs, A.ptrs, G.n, G.T, gdt, float(inv_scale), _ptr(out),
                                             _stream(stream)))
     return out
@@ -223,7 +232,7 @@ def mica_grad_sumsq(grads, inv_scale: float = 1.0, out: torch.Tensor | None = No
     dev = L.tensors[0].device if L.T else torch.device("cuda", torch.cuda.current_device())
     if out is None:
         out = torch.empty(1, dtype=torch.float64, device=dev)
-    gdt = _dtype_code(L.tensors[0] if L.T else None, "grads")
+    gdt = _dtype_code(L, "grads")
     _check(lib().mica_grad_sumsq(L.ptrs, L.n, L.T, gdt, float(inv_scale), _ptr(out), _stream(stream)))
     return out
 
@@ -261,15 +270,16 @@ def mica_adamw_steps(w, g, m, v, *, lr: float, beta1: float, beta2: float, eps: 
     device scalar from mica_clip_grad_norms (None: 1). ``skip_nonfinite`` leaves w, m, v as they are when the factor
     is not > 0 (the norm was not finite); ``coupled_l2`` is Adam's coupled L2 form instead of AdamW's decay."""
     W = _as_list(w)
+    _weights(W)
     sizes = W.counts
     G = _as_list(g)
     M = _as_list(m, sizes)
     V = _as_list(v, sizes)
     if not (W.T == G.T == M.T == V.T):
         raise ValueError("w, g, m and v must list the same number of tensors")
-    gdt = _dtype_code(G.tensors[0] if G.T else None, "g")
-    mdt = _dtype_code(M.tensors[0] if M.T else None, "m")
-    if mdt == MICA_BF16X2 and V.T and _dtype_code(V.tensors[0], "v") == MICA_F32:
+    gdt = _dtype_code(G, "g")
+    mdt = _dtype_code(M, "m")
+    if mdt == MICA_BF16X2 and V.T and _dtype_code(V, "v") == MICA_F32:
         mdt = MICA_BF16X2_M
     flags = (MICA_STEP_SKIP_NONFINITE if skip_nonfinite else 0) | (MICA_STEP_COUPLED_L2 if coupled_l2 else 0)
     hp = _HP(float(lr), float(beta1), float(beta2), float(eps), float(weight_decay), int(step), int(bool(zero_grad)),
@@ -285,6 +295,7 @@ def mica_clip_adamw_step(w, g, m, v, *, max_norm: float, inv_scale: float = 1.0,
     """One whole step: ClipGradNorms then AdamWSteps on the same list (one cooperative launch when the gradient
     fits in L2). Arguments as mica_clip_grad_norms and mica_adamw_steps; returns the device (norm, factor)."""
     W = _as_list(w)
+    _weights(W)
     sizes = W.counts
     G = _as_list(g)
     M = _as_list(m, sizes)
@@ -296,9 +307,9 @@ def mica_clip_adamw_step(w, g, m, v, *, max_norm: float, inv_scale: float = 1.0,
         norm_out = torch.empty(1, dtype=torch.float32, device=dev)
     if factor_out is None:
         factor_out = torch.empty(1, dtype=torch.float32, device=dev)
-    gdt = _dtype_code(G.tensors[0] if G.T else None, "g")
-    mdt = _dtype_code(M.tensors[0] if M.T else None, "m")
-    if mdt == MICA_BF16X2 and V.T and _dtype_code(V.tensors[0], "v") == MICA_F32:
+    gdt = _dtype_code(G, "g")
+    mdt = _dtype_code(M, "m")
+    if mdt == MICA_BF16X2 and V.T and _dtype_code(V, "v") == MICA_F32:
         mdt = MICA_BF16X2_M
     flags = (MICA_STEP_SKIP_NONFINITE if skip_nonfinite else 0) | (MICA_STEP_COUPLED_L2 if coupled_l2 else 0)
     hp = _HP(float(lr), float(beta1), float(beta2), float(eps), float(weight_decay), int(step), int(bool(zero_grad)),
@@ -324,6 +335,7 @@ def mica_adamw_steps_grouped(w, g, m, v, group, groups: Sequence[dict], *, beta1
     ``lr`` and ``weight_decay`` (the other hyperparameters are shared). ``group`` is a sequence of ints or a
     GroupIndex; the rest is as mica_adamw_steps."""
     W = _as_list(w)
+    _weights(W)
     sizes = W.counts
     G = _as_list(g)
     M = _as_list(m, sizes)
@@ -333,9 +345,9 @@ def mica_adamw_steps_grouped(w, g, m, v, group, groups: Sequence[dict], *, beta1
     gi = group if isinstance(group, GroupIndex) else GroupIndex(group)
     if len(gi.values) != W.T:
         raise ValueError("group must hold one index per tensor")
-    gdt = _dtype_code(G.tensors[0] if G.T else None, "g")
-    mdt = _dtype_code(M.tensors[0] if M.T else None, "m")
-    if mdt == MICA_BF16X2 and V.T and _dtype_code(V.tensors[0], "v") == MICA_F32:
+    gdt = _dtype_code(G, "g")
+    mdt = _dtype_code(M, "m")
+    if mdt == MICA_BF16X2 and V.T and _dtype_code(V, "v") == MICA_F32:
         mdt = MICA_BF16X2_M
     flags = (MICA_STEP_SKIP_NONFINITE if skip_nonfinite else 0) | (MICA_STEP_COUPLED_L2 if coupled_l2 else 0)
     hps = (_HP * max(len(groups), 1))(*[
@@ -350,11 +362,14 @@ def mica_sgd_steps(w, g, buf=None, *, lr: float, momentum: float = 0.0, zero_gra
     """SGD (``buf`` None) or SGD with momentum (one float32 buffer per tensor, zeros before the first step) over
     every tensor in one launch, in place; ``factor`` is the device scalar from mica_clip_grad_norms (None: 1)."""
     W = _as_list(w)
+    _weights(W)
     G = _as_list(g)
     B = None if buf is None else _as_list(buf)
     if W.T != G.T or (B is not None and B.T != W.T):
         raise ValueError("w, g (and buf) must list the same number of tensors")
-    gdt = _dtype_code(G.tensors[0] if G.T else None, "g")
+    if B is not None and B.dtype not in (None, torch.float32):
+        raise TypeError(f"buf: the momentum buffers must be float32, not {B.dtype}")
+    gdt = _dtype_code(G, "g")
     hp = _SgdHP(float(lr), float(momentum), int(bool(zero_grad)), MICA_STEP_SKIP_NONFINITE if skip_nonfinite else 0)
     _check(lib().mica_sgd_steps(W.ptrs, G.ptrs, None if B is None else B.ptrs, W.n, W.T, gdt, ctypes.byref(hp),
                                 _ptr(factor), _stream(stream)))

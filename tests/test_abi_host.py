@@ -232,3 +232,23 @@ def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(m, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         m.lib()
+
+
+def test_binding_checks_each_list_dtype_once():
+    """The binding refuses, before any call, a list that mixes dtypes (it passes one dtype for the whole list to
+    the library) and weights or momentum buffers that are not float32."""
+    import torch
+    with pytest.raises(TypeError, match="mixes dtypes"):
+        mica.TensorList([torch.zeros(4), torch.zeros(4, dtype=torch.float16)])
+    L = mica.TensorList([torch.zeros(4), torch.zeros(8)])
+    assert L.dtype == torch.float32 and L.total == 12
+    assert mica.TensorList([]).dtype is None
+    half = [torch.zeros(8, dtype=torch.float16)]
+    f32 = [torch.zeros(8)]
+    kw = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, step=1)
+    with pytest.raises(TypeError, match="float32"):
+        mica.mica_adamw_steps(half, f32, f32, f32, **kw)
+    with pytest.raises(TypeError, match="float32"):
+        mica.mica_sgd_steps(f32, f32, half, lr=0.1, momentum=0.9)
+    with pytest.raises(TypeError, match="dtype"):
+        mica.mica_accumulate_clip_grad_norms(f32, half, 1.0)
