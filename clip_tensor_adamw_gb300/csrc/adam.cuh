@@ -283,17 +283,6 @@ __device__ __forceinline__ StepScalars group_scalars(const StepScalars& s, const
     return x;
 }
 
-// The last j in [j, count) with pre[j] <= q, given pre[j] <= q already (pre non-decreasing).
-__device__ __forceinline__ int32_t pack_search(const int32_t* __restrict__ pre, int32_t j, int32_t count, int32_t q) {
-    int32_t hi = count - 1;
-    while (j < hi) {
-        const int32_t mid = (j + hi + 1) >> 1;
-        if (__ldg(pre + mid) <= q) j = mid;
-        else hi = mid - 1;
-    }
-    return j;
-}
-
 // A pack of small tensors (t .. t+count-1, whole): their octets are spread over the CTA's threads, thread i taking
 // pack octets i, i + 256, ..., so that every thread has work however small the tensors are. The pack numbers the
 // whole octets of its aligned tensors first, then the octets taken element by element (see the pack table in

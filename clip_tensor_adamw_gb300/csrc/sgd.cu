@@ -129,17 +129,6 @@ __device__ __forceinline__ void sgd_range(const TensorRec& r, int64_t ob, int64_
     }
 }
 
-// The last j in [j, count) with pre[j] <= q, given pre[j] <= q already (pre non-decreasing).
-__device__ __forceinline__ int32_t pack_search(const int32_t* __restrict__ pre, int32_t j, int32_t count, int32_t q) {
-    int32_t hi = count - 1;
-    while (j < hi) {
-        const int32_t mid = (j + hi + 1) >> 1;
-        if (__ldg(pre + mid) <= q) j = mid;
-        else hi = mid - 1;
-    }
-    return j;
-}
-
 // A pack of small tensors, its octets spread over the CTA's threads, whole octets first (as the AdamW kernel's
 // packs).
 template <Dtype G, bool kMomentum, bool kSkip>

@@ -1,6 +1,6 @@
 // Device helpers shared by the streaming kernels (adamw.cu, norm.cu, sgd.cu, scale.cu): 32- and 16-byte streaming
-// accesses, binary16 widening, programmatic dependent launch, the gradient factor read, L2 prefetch, and the
-// persistent grids' work queue.
+// accesses, binary16 widening, programmatic dependent launch, the gradient factor read, L2 prefetch, the search in a
+// pack's table, and the persistent grids' work queue.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -85,6 +85,18 @@ __device__ __forceinline__ bool skip_step(float f) { return kSkip && !(f > 0.0f)
 // Asks L2 to fetch `bytes` (a multiple of 16) from `p` (16-byte aligned), without waiting for them.
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// In a pack's table (non-decreasing first octets of its tensors): the last j in [j, count) with pre[j] <= q, given
+// pre[j] <= q already.
+__device__ __forceinline__ int32_t pack_search(const int32_t* __restrict__ pre, int32_t j, int32_t count, int32_t q) {
+    int32_t hi = count - 1;
+    while (j < hi) {
+        const int32_t mid = (j + hi + 1) >> 1;
+        if (__ldg(pre + mid) <= q) j = mid;
+        else hi = mid - 1;
+    }
+    return j;
 }
 
 // A persistent grid's work queue: q[0] counts the items handed out, q[1] the CTAs that have finished. Each CTA's
