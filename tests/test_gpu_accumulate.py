@@ -8,8 +8,6 @@ ragged tails, the loss-scaled list's small tensors (binary16, unscaled inside th
 vector accesses, special values, a list whose chunks span several staged runs of 256 tensors, GPT-2 small at full
 size, and three accumulate-then-update steps against the oracle's.
 """
-import dataclasses
-
 import numpy as np
 import pytest
 import torch
@@ -194,3 +192,27 @@ def test_accumulate_then_update_three_steps(ora, name):
             parity.exact(gw[k], w[k], f"w[{k}] t={t}")
             parity.exact(gm[k], m[k], f"m[{k}] t={t}")
             parity.exact(gv[k], v[k], f"v[{k}] t={t}")
+
+
+@pytest.mark.parametrize("gdt,inv_scale", [("f32", 1.0), ("f32", 0.3), ("f16", 2.0 ** -16), ("f16", 0.3)],
+                         ids=["f32_unscaled", "f32_scaled", "f16_pow2", "f16_scaled"])
+def test_accumulate_every_unscale_mode(ora, gdt, inv_scale):
+    """Each of the kernel's ways to sum the squares (float32 unscaled or scaled, binary16 with a power-of-two or any
+    other unscale) against the oracle, on a GPT-2-shaped list with ragged tails."""
+    wl = W["gpt2_small"] if gdt == "f32" else W["fp16_scaled"]
+    st = workloads.make_state(wl, "cuda", sizes=_gpt_sizes())
+    workloads.fill_grad(st, 1)
+    _check(ora, st, _addend(st, 81), max_norm=1.0, inv_scale=inv_scale)
+
+
+def test_accumulate_f16_list_larger_than_l2(ora):
+    """A binary16 gradient of 120 MB (more than the 96 MB below which the stores ask L2 to keep the lines): every
+    added element against the oracle, and the norm."""
+    wl = W["fp16_scaled"]
+    st = workloads.make_state(wl, "cuda", sizes=[768 * 3072] * 26 + [4097])
+    workloads.fill_grad(st, 1)
+    assert st.g_flat.numel() * 2 > 96 << 20
+    _check(ora, st, _addend(st, 82))
+    del st
+    mica.mica_release_cache()
+    torch.cuda.empty_cache()
