@@ -30,7 +30,7 @@
  *     counts. The library reads them during the call only and keeps no reference to the host arrays.
  *   - Every tensor buffer belongs to the caller and must be device memory of the current CUDA device. The library
  *     never allocates per call; it allocates once, per distinct tensor list, a small device table (tensor records,
- *     work items and, for the norm, one double per work item), kept until mica_release_cache().
+ *     work items and, for the norms, one double per CTA), kept until mica_release_cache().
  *   - Work is queued on `stream` (a cudaStream_t; NULL is the legacy default stream) and returns at once. Calls that
  *     share a tensor list must be ordered on one stream: they share that list's cached table.
  *   - Validation happens on the host before anything is queued; a call that returns an error has queued nothing.
