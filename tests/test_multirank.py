@@ -94,3 +94,23 @@ def test_profiled_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
     assert bench.profiled_traffic() is None
     monkeypatch.setattr(bench, "PROFILE", str(tmp_path / "missing.md"))
     assert bench.profiled_traffic() is None
+
+
+def test_byte_model_of_every_benchmarked_step():
+    """The bytes per parameter the benchmark's GB/s and roofline fractions are computed from, for each step it times:
+    AdamW reads w, g, m, v and writes w, m, v (28 B with float32 moments, 20 packed, 24 with m packed alone; 26 with
+    binary16 gradients), plus the norm's read of g; with the norm fused into the gradient's add, that kernel reads g
+    and a and writes g instead (12 B) and the norm reads nothing more; SGD moves w and g (and its buffer)."""
+    import dataclasses
+    import bench
+    import workloads
+    W = workloads.WORKLOADS
+    small = W["gpt2_small"]
+    assert bench.adamw_bytes_per_param(small) == 28 and bench.step_bytes_per_param(small) == 32
+    assert bench.adamw_bytes_per_param(W["gpt2_small_bf16"]) == 20 and bench.step_bytes_per_param(W["gpt2_xl"]) == 24
+    assert bench.adamw_bytes_per_param(dataclasses.replace(small, moments="bf16x2_m")) == 24
+    assert bench.adamw_bytes_per_param(W["fp16_scaled"]) == 26 and bench.step_bytes_per_param(W["fp16_scaled"]) == 28
+    assert bench.step_bytes_per_param(small, zero_grad=True) == 36
+    assert bench.step_bytes_per_param(small, opt="accumulate") == 12 + 28
+    assert bench.step_bytes_per_param(W["fp16_scaled"], opt="accumulate") == 6 + 26
+    assert bench.adamw_bytes_per_param(small, opt="sgd") == 12 and bench.adamw_bytes_per_param(small, opt="momentum") == 20
